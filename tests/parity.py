@@ -1,0 +1,39 @@
+"""Per-element acceptance checks shared by the parity tests.
+
+Bounds (stated per element against the fp64 oracle, S = |A| x |B|):
+  exact mode:  |C - C64| <= 2 * K * 2**-24 * S
+  tf32 mode:   |C - C64| <= 2 * K * 2**-11 * S
+and no NaN or Inf in C.
+"""
+
+import numpy as np
+
+EXACT_MODES = ("exact", "exact_simt")
+
+
+def tolerance_factor(mode: str, k: int) -> float:
+    if mode in EXACT_MODES:
+        return 2.0 * k * 2.0 ** -24
+    if mode == "tf32":
+        return 2.0 * k * 2.0 ** -11
+    raise ValueError(mode)
+
+
+def check_within_bound(c, c64, s, k, mode, what=""):
+    c = np.asarray(c, dtype=np.float32)
+    assert c.shape == c64.shape, (c.shape, c64.shape)
+    finite = np.isfinite(c)
+    assert finite.all(), f"{what}: {int((~finite).sum())} non-finite outputs"
+    tol = tolerance_factor(mode, k) * s
+    err = np.abs(c.astype(np.float64) - c64)
+    bad = err > tol
+    if bad.any():
+        idx = np.argwhere(bad)[0]
+        i = tuple(int(v) for v in idx)
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} outputs outside the {mode} bound; "
+            f"first at {i}: C={c[i]!r} C64={c64[i]!r} err={err[i]:.3e} tol={tol[i]:.3e}")
+    # normalised error: fraction of the bound actually used
+    with np.errstate(divide="ignore", invalid="ignore"):
+        used = np.where(tol > 0, err / tol, 0.0)
+    return float(used.max()) if used.size else 0.0
