@@ -1,0 +1,397 @@
+"""Benchmark: fp32 GEMM C = A x B at M = N = K = 4096 on GB300 (libgemm_f32).
+
+One step = one gemm_f32 call in `exact` mode (FP32-accurate 3xTF32 on the
+tensor cores) on the square 4096^3 workload: A, B i.i.d. uniform[-1, 1) from
+fixed seeds, row-major, C overwritten. Inputs are resident in HBM before the
+timed region; L2 is flushed (a 256 MiB write) between timed steps, outside the
+per-step CUDA events. Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own replica of the workload on its own GPU
+(no collective on the data path; weak scaling); the time is the max over ranks.
+`--impl reference` times the fp64 CPU oracle on the host cores instead (rank 0
+only), a bounded sample of the same workload per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GFLOP/s (2MNK/t) for fp32 GEMM at 4096³; % of TF32/FP32 roofline"
+WORKLOAD = "square fp32 GEMM M=N=K=4096, row-major, A,B uniform[-1,1) from seed (headline size)"
+M = N = K = 4096
+FLUSH_BYTES = 256 << 20
+TF32_PER_BF16 = 1.1 / 2.25          # nominal dense TF32 : BF16 tensor rate
+SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the other modes, e2e and CPU legs")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(bf16=float(p["bf16_tflops"]), bf16_sustained=float(p["bf16_tflops_sustained"]),
+                    hbm=float(p["hbm_gbs"]), sm_max_mhz=float(p.get("sm_max_mhz", 2070.0)),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, sm_max_mhz=2070.0,
+                    source="fallback")
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+        self.error = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except OSError as e:
+            self.error = str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"unavailable": self.error or "nvidia-smi not started"}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(t=t, sm=float(parts[1]), sm_max=float(parts[2]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t_start - 0.06 <= r["t"] <= self.t_stop + 0.06]
+        used = inside or [r for r in rows if self.t_start - 0.5 <= r["t"] <= self.t_stop + 0.5]
+        if not used:
+            return {"unavailable": "no nvidia-smi samples during the timed region"}
+        reasons = set()
+        for r in used:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in used),
+                "sm_max_mhz": max(r["sm_max"] for r in used),
+                "reasons": sorted(reasons), "samples": len(used),
+                "window": "timed region" if inside else "timed region +-0.5 s"}
+
+
+# ----------------------------------------------------------- GPU timing --
+
+def time_steps(torch, fn, steps, warmup, flush_buf, stream, barrier=None):
+    """Per-step device times (ms) of fn() with an L2 flush between steps."""
+    for _ in range(warmup):
+        flush_buf.zero_()
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    if barrier:
+        barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush_buf.zero_()
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    wall = time.perf_counter() - t0
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], wall
+
+
+def traffic_lookup(kernel: str, workload: str, mode: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    src = hashlib.sha256()
+    for f in ("tc_gemm.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "dense_fp32_gemm_major_gb300", "csrc", f), "rb") as fh:
+            src.update(fh.read())
+    sha = src.hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None, sha
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            kv = dict(x.split("=", 1) for x in line.split())
+            if (kv.get("kernel") == kernel and kv.get("workload") == workload
+                    and kv.get("mode") == mode and kv.get("src_sha256") == sha):
+                return int(kv["dram_bytes_per_launch"]), sha
+    return None, sha
+
+
+# -------------------------------------------------------------- CPU legs --
+
+def oracle_rows_gflops(a, b, budget_s: float, max_rows: int | None = None):
+    """Time the fp64 oracle on whole rows of the product until ~budget_s."""
+    import numpy as np
+    import oracle
+
+    threads = oracle.num_threads()
+    batch = max(1, threads)
+    rows_done, elapsed, start = 0, 0.0, 0
+    m, k = a.shape
+    n = b.shape[1]
+    while elapsed < budget_s and (max_rows is None or rows_done < max_rows):
+        rows = (np.arange(batch) + start) % m
+        t0 = time.perf_counter()
+        oracle.gemm_rows(a, b, rows)
+        elapsed += time.perf_counter() - t0
+        rows_done += batch
+        start += batch
+    flops = 2.0 * rows_done * n * k
+    return flops / elapsed / 1e9, threads, rows_done, elapsed
+
+
+def run_reference(args, rank):
+    import synth
+
+    if rank != 0:
+        return
+    a, b, cfg = synth.config_operands("c4")
+    import oracle
+
+    threads = oracle.num_threads()
+    rows_per_step = max(1, threads)
+    # untimed warm-up steps, then exactly `steps` timed steps of rows_per_step rows each
+    for w in range(args.warmup):
+        oracle.gemm_rows(a, b, [(w * rows_per_step + i) % M for i in range(rows_per_step)])
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        oracle.gemm_rows(a, b, [(s * rows_per_step + i) % M for i in range(rows_per_step)])
+    wall = time.perf_counter() - t0
+    flops = 2.0 * args.steps * rows_per_step * N * K
+    value = flops / wall / 1e9
+    sample = (f"{rows_per_step} whole rows of the 4096^3 product per step "
+              f"({rows_per_step}x4096x4096 multiply-adds, fp64)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(wall / max(args.steps, 1) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "sample": sample},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main --
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import numpy as np
+    import torch
+
+    import dense_fp32_gemm_major_gb300 as g
+    import synth
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier(device_ids=[local])
+
+    a, b, cfg = synth.config_operands("c4")
+    dA = torch.from_numpy(a).cuda()
+    dB = torch.from_numpy(b).cuda()
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    def gemm_call(mode):
+        def fn():
+            st = g.gemm_f32(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N, mode, sptr)
+            if st != g.OK:
+                raise g.GemmError(st)
+        return fn
+
+    kernel = g.gemm_f32_select(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N,
+                               g.EXACT, g.KERNEL_AUTO)
+    kernel_name = {g.KERNEL_SIMT: "simt_gemm", g.KERNEL_TC_TMA: "tc_gemm_tma_3xtf32",
+                   g.KERNEL_TC_LSU: "tc_gemm_lsu_3xtf32"}.get(kernel, str(kernel))
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    fn = gemm_call(g.EXACT)
+    for _ in range(args.warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_start()
+    times, wall = time_steps(torch, fn, args.steps, 0, flush, stream, barrier)
+    if sampler:
+        sampler.mark_stop()
+    clocks = sampler.stop() if sampler else None
+    st = g.gemm_f32_poll_device_status(sptr)
+    if st != g.OK:
+        raise g.GemmError(st, "device status")
+
+    total_ms = sum(times)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops = 2.0 * M * N * K
+    value = world * args.steps * flops / (total_ms / 1e3) / 1e9
+    ms_per_step = total_ms / args.steps
+
+    pk = peaks()
+    tf32_peak = pk["bf16"] * TF32_PER_BF16
+    achieved = 3 * flops / (ms_per_step / 1e3) / 1e12  # 3 TF32 MMAs per FMA (3xTF32)
+    traffic, sha = traffic_lookup("tc_gemm_tma_3xtf32", "c4", "exact")
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(tf32_peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / tf32_peak, 4), "traffic": traffic,
+                "kernel": kernel_name,
+                "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x nominal "
+                               f"TF32/BF16 ratio {TF32_PER_BF16:.4f}",
+                "achieved_counts": "3 x 2MNK (three TF32 MMAs per fp32 multiply-add)"}
+
+    extras = {}
+    cpu = None
+    e2e = None
+    if rank == 0 and not args.no_extras:
+        # the other modes, fewer steps, same protocol
+        for mname, mode, bound, peak, mult in (
+                ("tf32", g.TF32, "tensor", tf32_peak, 1),
+                ("exact_simt", g.EXACT_SIMT, "alu",
+                 SMS * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12, 1)):
+            steps = 200 if mname == "tf32" else 30
+            ts, _ = time_steps(torch, gemm_call(mode), steps, 5, flush, stream)
+            ms = statistics.mean(ts)
+            ach = mult * flops / (ms / 1e3) / 1e12
+            extras[mname] = {"value": round(flops / (ms / 1e3) / 1e9, 1), "unit": "GFLOP/s",
+                             "ms_per_step": round(ms, 4), "steps": steps,
+                             "roofline": {"bound": bound, "achieved": round(ach, 2),
+                                          "peak": round(peak, 1), "unit": "TFLOP/s",
+                                          "frac": round(ach / peak, 4)}}
+        # end to end through the host-buffer entry point (pinned host memory)
+        ha = torch.from_numpy(a).pin_memory().numpy()
+        hb = torch.from_numpy(b).pin_memory().numpy()
+        hc = torch.empty((M, N), dtype=torch.float32).pin_memory().numpy()
+        e2e_steps = max(3, min(args.steps, 30))
+        for _ in range(3):
+            g.matmul_host(ha, hb, "exact", out=hc)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            g.matmul_host(ha, hb, "exact", out=hc)
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        e2e = {"value": round(flops / e2e_s / 1e9, 1), "unit": "GFLOP/s",
+               "h2d_bytes_per_step": 4 * (M * K + K * N), "d2h_bytes_per_step": 4 * M * N,
+               "api": "gemm_f32_host (blocking; pinned host buffers)", "steps": e2e_steps}
+        # the oracle on the host cores, a bounded sample of the same workload
+        gf, threads, rows, secs = oracle_rows_gflops(a, b, budget_s=12.0)
+        cpu = {"value": round(gf, 3), "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} whole rows of the 4096^3 product ({rows}x4096x4096 "
+                         f"multiply-adds in fp64), {secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "mode": "exact",
+                       "kernel": kernel_name, "l2": "flushed (256 MiB write) between timed steps",
+                       "replicas": world, "parallelism": "replicas" if world > 1 else "single"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "modes": extras,
+            "timing": {"per_step_ms_median": round(statistics.median(times), 4),
+                       "per_step_ms_min": round(min(times), 4),
+                       "per_step_ms_max": round(max(times), 4), "wall_s": round(wall, 3),
+                       "kernel_src_sha256": sha},
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+"""Python binding of libgemm_f32.so: dense row-major fp32 GEMM on GB300.
+
+Argument marshalling only. Every step of the product runs in the library's
+CUDA kernels; there is no CPU or PyTorch fallback. Importing the package does
+not need a GPU, but it does need the built library: if libgemm_f32.so is
+missing the import fails loudly (build it with ``__graft_entry__.build()`` or
+``python -m dense_fp32_gemm_major_gb300._build``).
+
+The entry points mirror include/gemm_f32.h one to one (same names, same
+argument order; pointers are plain integers, streams are ``cudaStream_t``
+values as integers, 0 = the legacy default stream). ``matmul`` is a
+convenience wrapper over ``gemm_f32`` for torch CUDA tensors.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgemm_f32.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "gemm_f32.h")
+
+# gemm_f32_mode
+EXACT, TF32, EXACT_SIMT = 0, 1, 2
+MODES = {"exact": EXACT, "tf32": TF32, "exact_simt": EXACT_SIMT}
+# gemm_f32_status
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_ALIAS = range(6)
+# gemm_f32_kernel
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC_TMA, KERNEL_TC_LSU = range(4)
+KERNELS = {"auto": KERNEL_AUTO, "simt": KERNEL_SIMT, "tc_tma": KERNEL_TC_TMA, "tc_lsu": KERNEL_TC_LSU}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = "gemm_f32"):
+        self.status = status
+        super().__init__(f"{what} failed: {gemm_f32_status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"libgemm_f32.so is not built ({LIB_PATH}); run __graft_entry__.build(). "
+            "There is no fallback implementation.")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64, i32, p = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    sig = [i64, i64, i64, p, i64, p, i64, p, i64]
+    lib.gemm_f32.argtypes = sig + [i32, p]
+    lib.gemm_f32.restype = i32
+    lib.gemm_f32_ex.argtypes = sig + [i32, i32, p]
+    lib.gemm_f32_ex.restype = i32
+    lib.gemm_f32_select.argtypes = sig + [i32, i32]
+    lib.gemm_f32_select.restype = i32
+    lib.gemm_f32_host.argtypes = sig + [i32]
+    lib.gemm_f32_host.restype = i32
+    lib.gemm_f32_status_string.argtypes = [i32]
+    lib.gemm_f32_status_string.restype = ctypes.c_char_p
+    lib.gemm_f32_poll_device_status.argtypes = [p]
+    lib.gemm_f32_poll_device_status.restype = i32
+    lib.gemm_f32_selftest_wait_timeout.argtypes = [i64, p]
+    lib.gemm_f32_selftest_wait_timeout.restype = i32
+    _lib = lib
+    return lib
+
+
+def reload():
+    """Drop the cached handle (after a rebuild) and load the library again."""
+    global _lib
+    _lib = None
+    return _load()
+
+
+def library():
+    return _load()
+
+
+def declared_symbols() -> list[str]:
+    """Function names declared in include/gemm_f32.h."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gemm_f32\w*)\s*\(", text, flags=re.M)))
+
+
+# ------------------------------------------------------------ raw C ABI --
+
+def gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, mode, stream=0) -> int:
+    return _load().gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, mode, stream or None)
+
+
+def gemm_f32_ex(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel, stream=0) -> int:
+    return _load().gemm_f32_ex(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel, stream or None)
+
+
+def gemm_f32_select(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel=KERNEL_AUTO) -> int:
+    return _load().gemm_f32_select(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel)
+
+
+def gemm_f32_host(M, N, K, A, lda, B, ldb, C, ldc, mode) -> int:
+    return _load().gemm_f32_host(M, N, K, A, lda, B, ldb, C, ldc, mode)
+
+
+def gemm_f32_status_string(status: int) -> str:
+    return _load().gemm_f32_status_string(status).decode()
+
+
+def gemm_f32_poll_device_status(stream=0) -> int:
+    return _load().gemm_f32_poll_device_status(stream or None)
+
+
+def gemm_f32_selftest_wait_timeout(timeout_ns: int, stream=0) -> int:
+    return _load().gemm_f32_selftest_wait_timeout(timeout_ns, stream or None)
+
+
+# ---------------------------------------------------------- conveniences --
+
+def _mode(mode) -> int:
+    return MODES[mode] if isinstance(mode, str) else int(mode)
+
+
+def _kernel(kernel) -> int:
+    return KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
+
+
+def _check_operand(t, name):
+    import torch
+
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda or t.dim() != 2:
+        raise TypeError(f"{name} must be a 2-D float32 CUDA tensor")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be row-major (unit column stride)")
+
+
+def _ld(t) -> int:
+    return max(int(t.stride(0)), int(t.shape[1]), 1) if t.shape[0] > 1 else max(int(t.shape[1]), 1)
+
+
+def matmul(a, b, mode="exact", out=None, kernel="auto", stream=None):
+    """C = A x B for row-major float32 CUDA tensors (stream ordered).
+
+    ``a`` is M x K, ``b`` K x N; ``out`` (M x N, row-major, may have a padded
+    row stride) is overwritten and returned. ``stream`` defaults to torch's
+    current stream.
+    """
+    import torch
+
+    _check_operand(a, "a")
+    _check_operand(b, "b")
+    m, k = a.shape
+    k2, n = b.shape
+    if k != k2:
+        raise ValueError(f"inner dimensions differ: {tuple(a.shape)} x {tuple(b.shape)}")
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float32, device=a.device)
+    else:
+        _check_operand(out, "out")
+        if tuple(out.shape) != (m, n):
+            raise ValueError("out has the wrong shape")
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device).cuda_stream
+    with torch.cuda.device(a.device):
+        st = gemm_f32_ex(m, n, k, a.data_ptr(), _ld(a), b.data_ptr(), _ld(b), out.data_ptr(),
+                         _ld(out), _mode(mode), _kernel(kernel), stream)
+    if st != OK:
+        raise GemmError(st)
+    return out
+
+
+def matmul_host(a, b, mode="exact", out=None):
+    """C = A x B for host numpy float32 arrays through gemm_f32_host (blocking)."""
+    import numpy as np
+
+    for x, name in ((a, "a"), (b, "b")):
+        if not isinstance(x, np.ndarray) or x.dtype != np.float32 or x.ndim != 2 or x.strides[1] != 4:
+            raise TypeError(f"{name} must be a row-major 2-D float32 numpy array")
+    m, k = a.shape
+    k2, n = b.shape
+    if k != k2:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = np.empty((m, n), dtype=np.float32)
+    ld = lambda x: max(x.strides[0] // 4, x.shape[1], 1) if x.shape[0] > 1 else max(x.shape[1], 1)
+    st = gemm_f32_host(m, n, k, a.ctypes.data, ld(a), b.ctypes.data, ld(b), out.ctypes.data,
+                       ld(out), _mode(mode))
+    if st != OK:
+        raise GemmError(st, "gemm_f32_host")
+    return out

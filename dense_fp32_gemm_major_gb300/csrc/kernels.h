@@ -1,0 +1,47 @@
+// kernels.h -- host-side interface between the C ABI (api.cu) and the kernel
+// translation units. Internal to libgemm_f32.so.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gemm {
+
+struct GemmArgs {
+  int64_t M, N, K;
+  const float *A;
+  int64_t lda;
+  const float *B;
+  int64_t ldb;
+  float *C;
+  int64_t ldc;
+};
+
+// Status codes (values of gemm_f32_status).
+enum : int {
+  kOk = 0,
+  kErrInvalidArg = 1,
+  kErrUnsupportedDevice = 2,
+  kErrLaunch = 3,
+  kErrTimeout = 4,
+  kErrAlias = 5,
+};
+
+// True when A and B can be described by TMA tensor maps: 16-byte aligned
+// base addresses and row pitches that are multiples of 16 bytes.
+bool tc_tma_legal(const GemmArgs &a);
+
+// tcgen05 GEMM: exact = 3xTF32, else single-pass TF32; lsu = operands staged
+// by plain loads instead of TMA. Requires K >= 1, M >= 1, N >= 1.
+int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream);
+
+// SIMT FP32 GEMM. Requires K >= 1, M >= 1, N >= 1.
+int simt_launch(const GemmArgs &a, cudaStream_t stream);
+
+// Synchronise `stream`, then read and clear the device status word.
+int tc_poll_status(cudaStream_t stream);
+
+// Bounded-wait self-test (see gemm_f32_selftest_wait_timeout).
+int tc_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace gemm

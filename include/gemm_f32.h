@@ -1,0 +1,168 @@
+/*
+ * gemm_f32.h -- C ABI of libgemm_f32.so: dense row-major single-precision
+ * matrix multiplication C = A x B on an NVIDIA GB300 (sm_103a).
+ *
+ * Operation. A is M x K, B is K x N, C is M x N, all fp32 and row-major with
+ * leading dimensions lda, ldb, ldc counted in elements (element (i, j) of A is
+ * A[i * lda + j]). Every call overwrites C with the product:
+ *
+ *     C[i][j] = sum_{k < K} A[i][k] * B[k][j]
+ *
+ * This is the product that "Optimizing a WebGPU Matmul Kernel using
+ * Subgroups" builds up one output cell at a time (section 1, "Naive"; its
+ * later sections tile, vectorise and hand it to matrix units), with the
+ * M x K by K x N problem statement of "WebGPU WGSL Compute Shaders: Custom
+ * Matrix Multiplication (GEMM) Optimization Guide" (section 1) and the caller
+ * owned A, B (read) and C (written) buffers of its section 5 dispatch routine.
+ * C is overwritten, never accumulated into, as in every kernel on those pages.
+ * Out-of-range tile elements contribute zero and are never stored, the
+ * zero-filled boundary of section 4 of the same guide.
+ *
+ * Accuracy classes (stated per element against the exact product, with
+ * S = |A| x |B|):
+ *   GEMM_F32_EXACT       |C - AB| <= 2 K 2^-24 S  (FP32 class). Tensor cores
+ *                        with a 3xTF32 split (hi/lo operand decomposition),
+ *                        or the SIMT FP32 kernel when K < 16.
+ *   GEMM_F32_TF32        |C - AB| <= 2 K 2^-11 S  (TF32 class). One TF32 pass
+ *                        on the tensor cores; the low 13 mantissa bits of each
+ *                        operand are dropped by the hardware.
+ *   GEMM_F32_EXACT_SIMT  FP32 class, always on the SIMT FP32 kernel.
+ * No call returns a result of a lower class than the mode asks for.
+ *
+ * Streams and ownership. All matrix pointers passed to gemm_f32 and
+ * gemm_f32_ex are DEVICE pointers owned by the caller; the library keeps no
+ * reference to them after the call returns. `stream` is a cudaStream_t passed
+ * as void* (NULL = the legacy default stream). The call is stream ordered: it
+ * enqueues work and returns without synchronising. The library allocates no
+ * memory per call.
+ *
+ * Errors are returned synchronously as gemm_f32_status codes. Argument errors
+ * are detected on the host before anything is enqueued, and no CUDA call is
+ * made for them. A kernel whose pipeline wait runs out of time (a hardware or
+ * scheduling failure; never expected) records GEMM_ERR_TIMEOUT in a device
+ * status word, leaves C unspecified and exits cleanly; read it with
+ * gemm_f32_poll_device_status.
+ *
+ * Thread safety: all entry points may be called from several host threads.
+ */
+#ifndef GEMM_F32_H
+#define GEMM_F32_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_F32_EXACT = 0,      /* FP32-accurate: 3xTF32 tensor cores (SIMT if K < 16) */
+    GEMM_F32_TF32 = 1,       /* single-pass TF32 on tensor cores */
+    GEMM_F32_EXACT_SIMT = 2  /* FP32-accurate on the SIMT FP32 kernel */
+} gemm_f32_mode;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,         /* bad size, leading dimension, pointer, mode or kernel */
+    GEMM_ERR_UNSUPPORTED_DEVICE = 2,  /* current device is not compute capability 10.3 */
+    GEMM_ERR_LAUNCH = 3,              /* a CUDA launch or API call failed */
+    GEMM_ERR_TIMEOUT = 4,             /* a device-side pipeline wait ran out of time */
+    GEMM_ERR_ALIAS = 5                /* C overlaps A or B */
+} gemm_f32_status;
+
+/* Kernel choice for gemm_f32_ex. */
+typedef enum {
+    GEMM_KERNEL_AUTO = 0,    /* what gemm_f32 picks */
+    GEMM_KERNEL_SIMT = 1,    /* SIMT FP32 register-tiled kernel (exact modes only) */
+    GEMM_KERNEL_TC_TMA = 2,  /* tcgen05 kernel fed by TMA (needs TMA-legal A and B) */
+    GEMM_KERNEL_TC_LSU = 3   /* tcgen05 kernel fed by plain loads (any strides) */
+} gemm_f32_kernel;
+
+/*
+ * gemm_f32 -- C = A x B, stream ordered.
+ *   M, N, K   sizes, >= 0. M == 0 or N == 0 is a no-op; K == 0 sets C to zero
+ *             (the empty sum).
+ *   A, lda    device pointer to M x K fp32, 4-byte aligned, lda >= max(1, K)
+ *   B, ldb    device pointer to K x N fp32, 4-byte aligned, ldb >= max(1, N)
+ *   C, ldc    device pointer to M x N fp32, 4-byte aligned, ldc >= max(1, N);
+ *             must not overlap A or B (GEMM_ERR_ALIAS)
+ *   mode      a gemm_f32_mode
+ *   stream    cudaStream_t as void*
+ * Sizes and leading dimensions must stay below 2^31 elements.
+ * Returns a gemm_f32_status. Stream-ordered and non-blocking.
+ */
+int gemm_f32(int64_t M, int64_t N, int64_t K,
+             const float *A, int64_t lda,
+             const float *B, int64_t ldb,
+             float *C, int64_t ldc,
+             int mode, void *stream);
+
+/*
+ * gemm_f32_ex -- gemm_f32 with an explicit kernel choice (a gemm_f32_kernel).
+ * GEMM_KERNEL_AUTO behaves exactly like gemm_f32. A kernel that cannot serve
+ * the arguments returns GEMM_ERR_INVALID_ARG: GEMM_KERNEL_SIMT with mode
+ * GEMM_F32_TF32 (it would change the accuracy class), or GEMM_KERNEL_TC_TMA
+ * when A or B is not 16-byte aligned or lda, ldb is not a multiple of 4.
+ * Mode GEMM_F32_EXACT with a tensor-core kernel forced runs 3xTF32 for every
+ * K, including K < 16.
+ */
+int gemm_f32_ex(int64_t M, int64_t N, int64_t K,
+                const float *A, int64_t lda,
+                const float *B, int64_t ldb,
+                float *C, int64_t ldc,
+                int mode, int kernel, void *stream);
+
+/*
+ * gemm_f32_select -- the kernel gemm_f32_ex would run for these arguments (a
+ * gemm_f32_kernel value, never AUTO), or a negative gemm_f32_status if the
+ * arguments are invalid. Host-only: it inspects sizes, leading dimensions and
+ * pointer alignment and makes no CUDA call.
+ */
+int gemm_f32_select(int64_t M, int64_t N, int64_t K,
+                    const float *A, int64_t lda,
+                    const float *B, int64_t ldb,
+                    float *C, int64_t ldc,
+                    int mode, int kernel);
+
+/*
+ * gemm_f32_host -- C = A x B for matrices in HOST memory (pageable or pinned).
+ * Copies A and B to device buffers that the library owns and reuses (grown on
+ * demand, one set per device, held until process exit), runs gemm_f32 on a
+ * library-owned stream of the current device, copies C back and waits for
+ * completion. Blocking. Same size, leading-dimension, mode and alias rules as
+ * gemm_f32 (alias checked on the host ranges). Device-side leading dimensions
+ * are padded to multiples of 4 so the TMA-fed kernels apply at any K and N.
+ * Calls on one device are serialised by a lock.
+ */
+int gemm_f32_host(int64_t M, int64_t N, int64_t K,
+                  const float *A, int64_t lda,
+                  const float *B, int64_t ldb,
+                  float *C, int64_t ldc,
+                  int mode);
+
+/* gemm_f32_status_string -- static, NUL-terminated name of a status code. */
+const char *gemm_f32_status_string(int status);
+
+/*
+ * gemm_f32_poll_device_status -- synchronise `stream`, then return and clear
+ * the device status word of the current device (GEMM_OK if no kernel has
+ * recorded an error since the last poll). Returns GEMM_ERR_LAUNCH if the
+ * synchronisation itself fails.
+ */
+int gemm_f32_poll_device_status(void *stream);
+
+/*
+ * gemm_f32_selftest_wait_timeout -- failure-detection self-test. Launches one
+ * warp that waits, through the same bounded pipeline wait the GEMM kernels
+ * use, on a shared-memory barrier that nothing ever signals; after
+ * `timeout_ns` (1e6 .. 1e10) the wait gives up, records GEMM_ERR_TIMEOUT in
+ * the device status word and the kernel returns. Synchronises `stream` and
+ * returns what gemm_f32_poll_device_status then reads (GEMM_ERR_TIMEOUT when
+ * the mechanism works). The context stays usable afterwards.
+ */
+int gemm_f32_selftest_wait_timeout(int64_t timeout_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F32_H */

@@ -1,0 +1,107 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and validates arguments and picks kernels on the host
+before touching CUDA."""
+
+import ctypes
+
+import pytest
+
+EXPECTED = {
+    "gemm_f32", "gemm_f32_ex", "gemm_f32_select", "gemm_f32_host", "gemm_f32_status_string",
+    "gemm_f32_poll_device_status", "gemm_f32_selftest_wait_timeout",
+}
+
+# Fake, never dereferenced, 256-byte aligned "device" addresses for host-only paths.
+PA, PB, PC = 0x10000000, 0x20000000, 0x30000000
+
+
+def test_header_declares_expected_symbols(gemm_lib):
+    assert set(gemm_lib.declared_symbols()) >= EXPECTED
+
+
+def test_library_exports_every_declared_symbol(gemm_lib):
+    lib = ctypes.CDLL(gemm_lib.LIB_PATH)
+    for name in gemm_lib.declared_symbols():
+        assert hasattr(lib, name), f"{name} declared in include/gemm_f32.h but not exported"
+
+
+def test_status_strings(gemm_lib):
+    names = ["GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED_DEVICE", "GEMM_ERR_LAUNCH",
+             "GEMM_ERR_TIMEOUT", "GEMM_ERR_ALIAS"]
+    for code, name in enumerate(names):
+        assert gemm_lib.gemm_f32_status_string(code) == name
+    assert gemm_lib.gemm_f32_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("args", [
+    dict(M=-1), dict(N=-1), dict(K=-1),
+    dict(lda=63), dict(ldb=31), dict(ldc=31),          # leading dimension below the width
+    dict(mode=3), dict(mode=-1),
+    dict(A=0), dict(B=0), dict(C=0),                   # null with non-zero extents
+    dict(A=PA + 2), dict(C=PC + 1),                    # not 4-byte aligned
+    dict(M=1 << 31), dict(lda=1 << 31),                # beyond the 2^31 element limit
+])
+def test_invalid_arguments_rejected_before_any_cuda_call(gemm_lib, args):
+    a = dict(M=16, N=32, K=64, A=PA, lda=64, B=PB, ldb=32, C=PC, ldc=32, mode=0)
+    a.update(args)
+    st = gemm_lib.gemm_f32(a["M"], a["N"], a["K"], a["A"], a["lda"], a["B"], a["ldb"], a["C"],
+                           a["ldc"], a["mode"], 0)
+    assert st == gemm_lib.ERR_INVALID_ARG
+
+
+def test_alias_rejected(gemm_lib):
+    # C overlapping A, then C overlapping B
+    assert gemm_lib.gemm_f32(64, 64, 64, PA, 64, PB, 64, PA + 4 * 100, 64, 0, 0) == gemm_lib.ERR_ALIAS
+    assert gemm_lib.gemm_f32(64, 64, 64, PA, 64, PB, 64, PB + 4 * 4032, 64, 0, 0) == gemm_lib.ERR_ALIAS
+    # adjacent but not overlapping is fine for validation (selection succeeds)
+    assert gemm_lib.gemm_f32_select(64, 64, 64, PA, 64, PA + 4 * 64 * 64, 64, PA + 8 * 64 * 64, 64,
+                                    0, 0) > 0
+
+
+def test_empty_outputs_are_noops(gemm_lib):
+    # M == 0 or N == 0: nothing to do, OK without any CUDA call (null pointers allowed)
+    assert gemm_lib.gemm_f32(0, 32, 64, 0, 64, 0, 32, 0, 32, 0, 0) == gemm_lib.OK
+    assert gemm_lib.gemm_f32(16, 0, 64, 0, 64, 0, 1, 0, 1, 1, 0) == gemm_lib.OK
+
+
+def test_kernel_selection(gemm_lib):
+    sel = gemm_lib.gemm_f32_select
+    E, T, S = gemm_lib.EXACT, gemm_lib.TF32, gemm_lib.EXACT_SIMT
+    # TMA-legal operands go to the TMA-fed tensor-core kernel in both TC modes
+    assert sel(4096, 4096, 4096, PA, 4096, PB, 4096, PC, 4096, E, 0) == gemm_lib.KERNEL_TC_TMA
+    assert sel(4096, 4096, 4096, PA, 4096, PB, 4096, PC, 4096, T, 0) == gemm_lib.KERNEL_TC_TMA
+    # the ragged workload (row pitches 3108 and 6124 bytes) is not TMA-legal
+    assert sel(1000, 1531, 777, PA, 777, PB, 1531, PC, 1531, E, 0) == gemm_lib.KERNEL_TC_LSU
+    assert sel(1000, 1531, 777, PA, 777, PB, 1531, PC, 1531, T, 0) == gemm_lib.KERNEL_TC_LSU
+    # misaligned base address also rules TMA out
+    assert sel(64, 64, 64, PA + 4, 64, PB, 64, PC, 64, T, 0) == gemm_lib.KERNEL_TC_LSU
+    # exact mode with K < 16 uses the FP32 FMA kernel; EXACT_SIMT always does
+    assert sel(64, 64, 15, PA, 16, PB, 64, PC, 64, E, 0) == gemm_lib.KERNEL_SIMT
+    assert sel(64, 64, 16, PA, 16, PB, 64, PC, 64, E, 0) == gemm_lib.KERNEL_TC_TMA
+    assert sel(4096, 4096, 4096, PA, 4096, PB, 4096, PC, 4096, S, 0) == gemm_lib.KERNEL_SIMT
+    # forced kernels: SIMT cannot serve TF32 (accuracy class), TMA needs legal strides
+    assert sel(64, 64, 64, PA, 64, PB, 64, PC, 64, T, gemm_lib.KERNEL_SIMT) == -gemm_lib.ERR_INVALID_ARG
+    assert sel(64, 64, 64, PA, 65, PB, 64, PC, 64, T, gemm_lib.KERNEL_TC_TMA) == -gemm_lib.ERR_INVALID_ARG
+    assert sel(64, 64, 64, PA, 64, PB, 64, PC, 64, E, gemm_lib.KERNEL_TC_LSU) == gemm_lib.KERNEL_TC_LSU
+    assert sel(64, 64, 64, PA, 64, PB, 64, PC, 64, S, gemm_lib.KERNEL_TC_LSU) == -gemm_lib.ERR_INVALID_ARG
+    assert sel(64, 64, 64, PA, 64, PB, 64, PC, 64, E, 9) == -gemm_lib.ERR_INVALID_ARG
+    # invalid arguments are reported as negative status codes
+    assert sel(-1, 64, 64, PA, 64, PB, 64, PC, 64, E, 0) == -gemm_lib.ERR_INVALID_ARG
+
+
+def test_valid_call_without_gpu_fails_cleanly(gemm_lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = gemm_lib.gemm_f32(64, 64, 64, PA, 64, PB, 64, PC, 64, 0, 0)
+    assert st in (gemm_lib.ERR_LAUNCH, gemm_lib.ERR_UNSUPPORTED_DEVICE)
+
+
+def test_missing_library_fails_loudly(gemm_lib, monkeypatch, tmp_path):
+    import dense_fp32_gemm_major_gb300 as g
+
+    monkeypatch.setattr(g, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(g, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        g.gemm_f32(1, 1, 1, PA, 1, PB, 1, PC, 1, 0, 0)

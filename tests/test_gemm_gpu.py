@@ -1,0 +1,244 @@
+"""Parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Every comparison is element by element: within the mode's bound for random
+inputs, bitwise for integer-valued inputs (where every kernel's result is
+exact). Inputs come from ``synth``; expected values only from ``oracle``.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import check_within_bound
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["exact", "tf32", "exact_simt"]
+# (mode, kernel) pairs that are legal for TMA-legal operands
+VARIANTS = [("exact", "auto"), ("exact", "tc_tma"), ("exact", "tc_lsu"), ("exact", "simt"),
+            ("tf32", "tc_tma"), ("tf32", "tc_lsu"), ("exact_simt", "auto")]
+
+
+@pytest.fixture(scope="module")
+def g(gemm_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return gemm_lib
+
+
+def to_dev(x, ld=None, fill=float("nan")):
+    """Upload a rows x cols fp32 matrix into a (rows x ld) device buffer."""
+    rows, cols = x.shape
+    ld = ld or max(cols, 1)
+    buf = torch.full((max(rows, 1), ld), fill, dtype=torch.float32, device="cuda")
+    if rows and cols:
+        buf[:rows, :cols] = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    return buf
+
+
+def run(g, a, b, mode="exact", kernel="auto", lda=None, ldb=None, ldc=None, c_fill=float("nan")):
+    """C = A x B through gemm_f32_ex; returns (C as numpy, full C buffer as numpy)."""
+    m, k = a.shape
+    _, n = b.shape
+    da, db = to_dev(a, lda), to_dev(b, ldb)
+    ldc = ldc or max(n, 1)
+    dc = torch.full((max(m, 1), ldc), c_fill, dtype=torch.float32, device="cuda")
+    st = g.gemm_f32_ex(m, n, k, da.data_ptr(), da.shape[1], db.data_ptr(), db.shape[1],
+                       dc.data_ptr(), ldc, g.MODES[mode], g.KERNELS[kernel],
+                       torch.cuda.current_stream().cuda_stream)
+    assert st == g.OK, g.gemm_f32_status_string(st)
+    assert g.gemm_f32_poll_device_status(torch.cuda.current_stream().cuda_stream) == g.OK
+    full = dc.cpu().numpy()
+    return full[:m, :n], full
+
+
+_CONFIG_CACHE = {}
+
+
+def config_operands(name):
+    if name not in _CONFIG_CACHE:
+        _CONFIG_CACHE.clear()  # keep at most one full-size workload in host memory
+        _CONFIG_CACHE[name] = synth.config_operands(name)
+    return _CONFIG_CACHE[name]
+
+
+def operands(m, n, k, dist="uniform", seed=0):
+    return (synth.draw(dist, (m, k), 100 + seed), synth.draw(dist, (k, n), 200 + seed))
+
+
+@pytest.mark.parametrize("mode,kernel", VARIANTS)
+@pytest.mark.parametrize("m,n,k", [(300, 700, 200), (257, 513, 129), (128, 256, 32),
+                                   (1, 1, 64), (129, 33, 1000)])
+def test_random_within_bound(g, mode, kernel, m, n, k):
+    a, b = operands(m, n, k, "normal", seed=m + n + k)
+    c, _ = run(g, a, b, mode, kernel)
+    c64, s = oracle.gemm(a, b)
+    check_within_bound(c, c64, s, k, mode, f"{mode}/{kernel} {m}x{n}x{k}")
+
+
+@pytest.mark.parametrize("mode,kernel", VARIANTS)
+def test_integer_inputs_bitwise(g, mode, kernel):
+    # small integers: every kernel's result is exact, so it equals the oracle bitwise
+    for (m, n, k) in [(300, 700, 200), (32, 24, 16), (257, 129, 77)]:
+        a = synth.small_integers((m, k), 31 + k)
+        b = synth.small_integers((k, n), 32 + k)
+        c, _ = run(g, a, b, mode, kernel)
+        c64, _ = oracle.gemm(a, b)
+        assert np.array_equal(c.astype(np.float64), c64), f"{mode}/{kernel} {m}x{n}x{k}"
+
+
+@pytest.mark.parametrize("mode,kernel", [("exact", "tc_tma"), ("tf32", "tc_tma"), ("exact", "simt")])
+def test_integer_selftest_pattern(g, mode, kernel):
+    # the integer pattern of "GPU compute shaders" (section "Code"), m, n, k = 32, 24, 16
+    m, n, k = 32, 24, 16
+    a = (np.arange(m * k) % 7 - 3).astype(np.float32).reshape(m, k)
+    b = (np.arange(k * n) % 5 - 2).astype(np.float32).reshape(k, n)
+    c, _ = run(g, a, b, mode, kernel)
+    assert np.array_equal(c.astype(np.float64), oracle.gemm(a, b)[0])
+
+
+@pytest.mark.parametrize("mode,kernel", VARIANTS)
+def test_all_ones_closed_form(g, mode, kernel):
+    for (m, n, k) in [(1, 1, 1), (129, 257, 33), (200, 300, 1000)]:
+        c, _ = run(g, np.ones((m, k), np.float32), np.ones((k, n), np.float32), mode, kernel)
+        assert np.all(c == k), f"{mode}/{kernel} {m}x{n}x{k}"
+
+
+@pytest.mark.parametrize("mode,kernel", [("exact", "tc_lsu"), ("tf32", "tc_lsu"), ("exact", "simt"),
+                                         ("exact", "auto"), ("tf32", "auto")])
+def test_ragged_strides_and_guard_bands(g, mode, kernel):
+    # odd leading dimensions (not TMA-legal), NaN padding in A and B, sentinel padding in C:
+    # padding must never be read into a result or written
+    m, n, k = 203, 301, 117
+    a, b = operands(m, n, k, "normal", seed=5)
+    c, full = run(g, a, b, mode, kernel, lda=k + 3, ldb=n + 5, ldc=n + 7, c_fill=-12345.0)
+    c64, s = oracle.gemm(a, b)
+    check_within_bound(c, c64, s, k, mode, f"ragged {mode}/{kernel}")
+    assert np.all(full[:, n:] == -12345.0), "write outside C's columns"
+
+
+def test_ragged_sweep(g):
+    # brute-force sweep of small shapes around tile edges, every kernel
+    sizes = [1, 2, 3, 7, 8, 9, 15, 16, 17, 31, 32, 33, 127, 128, 129, 255, 256, 257]
+    rng = np.random.default_rng(2024)
+    combos = {(int(rng.choice(sizes)), int(rng.choice(sizes)), int(rng.choice(sizes)))
+              for _ in range(60)}
+    combos |= {(1, 1, 1), (257, 257, 257), (1, 257, 17), (257, 1, 129), (17, 17, 17)}
+    for (m, n, k) in sorted(combos):
+        a = synth.small_integers((m, k), m * 7 + k)
+        b = synth.small_integers((k, n), n * 11 + k)
+        c64, _ = oracle.gemm(a, b)
+        ar, br = operands(m, n, k, "uniform", seed=m * n + k)
+        r64, rs = oracle.gemm(ar, br)
+        for mode, kernel in VARIANTS:
+            c, _ = run(g, a, b, mode, kernel)
+            assert np.array_equal(c.astype(np.float64), c64), f"int {mode}/{kernel} {m}x{n}x{k}"
+            if mode == "exact" and kernel in ("tc_tma", "tc_lsu") and k < 8:
+                continue  # 3xTF32 is outside the FP32 bound for K < 8 on random data
+            if mode == "tf32" and k < 4:
+                continue  # truncated TF32 operands: the bound needs K >= 2 (worst case)
+            c, _ = run(g, ar, br, mode, kernel)
+            check_within_bound(c, r64, rs, k, mode, f"rand {mode}/{kernel} {m}x{n}x{k}")
+
+
+def test_nan_prefilled_output_fully_written(g):
+    for mode, kernel in VARIANTS:
+        a, b = operands(385, 519, 96, "uniform", seed=9)
+        c, _ = run(g, a, b, mode, kernel, c_fill=float("nan"))
+        assert np.isfinite(c).all(), f"{mode}/{kernel} left outputs unwritten"
+
+
+def test_rerun_is_bitwise_identical(g):
+    a, b = operands(640, 768, 512, "normal", seed=3)
+    for mode, kernel in VARIANTS:
+        c1, _ = run(g, a, b, mode, kernel)
+        c2, _ = run(g, a, b, mode, kernel)
+        assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32)), f"{mode}/{kernel}"
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop(g):
+    for mode in MODES:
+        c, _ = run(g, np.zeros((5, 0), np.float32), np.zeros((0, 7), np.float32), mode, c_fill=3.0)
+        assert np.all(c == 0.0)
+    # M == 0: C untouched
+    dc = torch.full((4, 4), 7.0, device="cuda")
+    st = g.gemm_f32(0, 4, 4, 0, 4, 0, 4, dc.data_ptr(), 4, g.EXACT, 0)
+    torch.cuda.synchronize()
+    assert st == g.OK and torch.all(dc == 7.0)
+
+
+def test_alias_error_on_device(g):
+    x = torch.zeros((64, 64), device="cuda")
+    assert g.gemm_f32(64, 64, 64, x.data_ptr(), 64, x.data_ptr(), 64, x.data_ptr(), 64,
+                      g.EXACT, 0) == g.ERR_ALIAS
+
+
+def test_torch_wrapper_and_streams(g):
+    a, b = operands(256, 384, 128, "uniform", seed=1)
+    s = torch.cuda.Stream()
+    ta, tb = torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda()
+    with torch.cuda.stream(s):
+        out = g.matmul(ta, tb, "exact")
+    s.synchronize()
+    c64, sc = oracle.gemm(a, b)
+    check_within_bound(out.cpu().numpy(), c64, sc, 128, "exact", "matmul on a side stream")
+
+
+def test_host_entry_point(g):
+    for (m, n, k), mode in [((1000, 1531, 777), "exact"), ((1000, 1531, 777), "tf32"),
+                            ((64, 96, 5), "exact"), ((3, 5, 0), "tf32")]:
+        a, b = operands(m, n, k, "normal", seed=k)
+        c = g.matmul_host(a, b, mode)
+        c64, s = oracle.gemm(a, b)
+        check_within_bound(c, c64, s, k, mode, f"host {mode} {m}x{n}x{k}")
+
+
+def test_bounded_wait_times_out_cleanly(g):
+    stream = torch.cuda.current_stream().cuda_stream
+    assert g.gemm_f32_selftest_wait_timeout(20_000_000, stream) == g.ERR_TIMEOUT
+    # status was cleared by the read, and the context still works
+    assert g.gemm_f32_poll_device_status(stream) == g.OK
+    a, b = operands(128, 256, 64, "uniform", seed=2)
+    c, _ = run(g, a, b, "exact", "tc_tma")
+    c64, s = oracle.gemm(a, b)
+    check_within_bound(c, c64, s, 64, "exact", "after timeout self-test")
+
+
+# ---------------------------------------------------------- full sizes --
+
+def _sample_rows(m, count, seed):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(m, size=min(count, m), replace=False).tolist())
+    rows |= {0, m - 1, 127, 128, min(m - 1, 1000)}
+    return np.array(sorted(r for r in rows if r < m), dtype=np.int64)
+
+
+@pytest.mark.parametrize("cfg", ["c1", "c2", "c3", "c5a"])
+@pytest.mark.parametrize("mode", MODES)
+def test_config_full_comparison(g, cfg, mode):
+    a, b, c = config_operands(cfg)
+    out, _ = run(g, a, b, mode)
+    if cfg == "c3":
+        rows = _sample_rows(c["M"], 512, 3)
+        c64, s = oracle.gemm_rows(a, b, rows)
+        check_within_bound(out[rows], c64, s, c["K"], mode, f"{cfg} {mode}")
+    else:
+        c64, s = oracle.gemm(a, b)
+        check_within_bound(out, c64, s, c["K"], mode, f"{cfg} {mode}")
+
+
+@pytest.mark.parametrize("cfg", ["c4", "c5b"])
+@pytest.mark.parametrize("mode", ["exact", "tf32"])
+def test_config_full_size_sampled_rows(g, cfg, mode):
+    # full-size workload in the benchmark's launch configuration (dense leading
+    # dimensions, default kernel choice, torch's current stream); the oracle
+    # computes a sample of whole rows, including first and last
+    a, b, c = config_operands(cfg)
+    out, _ = run(g, a, b, mode)
+    assert np.isfinite(out).all()
+    rows = _sample_rows(c["M"], 96, 4)
+    c64, s = oracle.gemm_rows(a, b, rows)
+    check_within_bound(out[rows], c64, s, c["K"], mode, f"{cfg} {mode}")
