@@ -1,35 +1,47 @@
 // tc_gemm.cu -- tensor-core fp32 GEMM for sm_103a (tcgen05 + TMEM).
 //
-// C[M x N] = A[M x K] * B[K x N], all row-major fp32. One persistent CTA per
-// SM walks a grouped (L2-friendly) sequence of 128 x BN output tiles. Roles
-// are warp-specialised and talk through mbarriers:
+// C[M x N] = A[M x K] * B[K x N], all row-major fp32.
 //
-//   producer  stages 128 x 32 tiles of A and 32 x BN tiles of B into a ring of
-//             shared-memory stages in the 128-byte swizzled layouts tcgen05
-//             reads: either one thread issuing TMA tile loads (TMA-legal
-//             operands) or four warps issuing plain loads (any strides).
-//   transform (3xTF32 with TMA only) splits every staged value x into
-//             hi = tf32(x) and lo = tf32(x - hi), hi in place, lo in a
-//             sibling tile at the same offset.
-//   MMA       one thread issues tcgen05.mma kind::tf32 (M = 128, N = BN,
-//             K = 8) into a TMEM accumulator; 3xTF32 issues A_lo*B_hi,
-//             A_hi*B_lo, A_hi*B_hi per k-step (small terms first). Two TMEM
-//             accumulators let the epilogue of one tile overlap the mainloop
-//             of the next.
-//   epilogue  four warps move the accumulator TMEM -> registers -> global
-//             memory with row/column predication.
+// Formulation. kind::tf32 MMAs need both operands K-major (k contiguous). A
+// (row-major M x K) already is; B (row-major K x N) is N-contiguous. Each
+// output tile is therefore computed transposed,
+//
+//     D = C_tile^T  (128 n x 256 m)  =  B_tile^T (128 n x K)  *  A_tile^T (K x 256 m),
+//
+// with B_tile^T as the MMA's A operand held in TMEM (lane = n, one 32-bit
+// column per k: the transpose happens on the way from shared memory through
+// registers into TMEM) and the A tile, staged K-major by TMA, as the MMA's B
+// operand in shared memory. The accumulator D lives in TMEM with lane = n and
+// column = m, so each epilogue store writes 32 consecutive columns of one row
+// of C (a coalesced 128-byte segment).
+//
+// Roles (warp-specialised, persistent, one CTA per SM, grouped raster):
+//   producer   TMA: one thread loads the 256 x 32 A tile (128-byte swizzle)
+//              and the 32 x 128 B tile per stage into a ring of stages.
+//              LSU (operands TMA cannot describe): four warps load both with
+//              plain loads and place the A tile in shared memory and B^T in
+//              TMEM themselves.
+//   transform  (TMA variant) four warps move B^T into TMEM and, in 3xTF32
+//              mode, split the A tile into hi (in place) and lo (sibling tile).
+//   MMA        one thread issues tcgen05.mma kind::tf32, M = 128, N = 256,
+//              K = 8. 3xTF32 issues B_lo*A_hi, B_hi*A_lo, B_hi*A_hi per k-step
+//              (small terms first), hi = tf32(x), lo = tf32(x - hi).
+//   epilogue   four warps read D from TMEM and store C with row/column
+//              guards.
 //
 // This is the tiled product of "Optimizing a WebGPU Matmul Kernel using
-// Subgroups" (sections 4-8: shared-memory tiles, per-thread register tiles,
-// vector loads, matrix-unit multiply-accumulate over staged tiles, output
-// staged before the store) mapped onto Blackwell's tensor memory and async
-// copy engine; the zero-filled out-of-range loads and guarded stores are
-// those of section 4 of "WebGPU WGSL Compute Shaders: Custom Matrix
-// Multiplication (GEMM) Optimization Guide".
+// Subgroups" (sections 4-8: shared-memory tiles, register tiles, vector
+// loads, matrix-unit multiply-accumulate over staged tiles, output staged
+// before the store) mapped onto Blackwell's tensor memory and copy engine;
+// out-of-range elements load as zero and stores are guarded, as in section 4
+// of "WebGPU WGSL Compute Shaders: Custom Matrix Multiplication (GEMM)
+// Optimization Guide". Section 6 of that guide transposes a shared-memory
+// tile to avoid bank conflicts; here the transpose of B is what makes the
+// operand K-major for the tensor core.
 //
-// Every barrier wait is bounded (see mbar_wait_bounded); on a timeout the CTA
-// drains its in-flight copies and MMAs, frees TMEM and exits, and the host
-// reads kErrTimeout from the status word.
+// Every barrier wait is bounded (mbar_wait_bounded). On a timeout the CTA
+// lets its in-flight copies and MMAs finish (bounded), frees TMEM and exits;
+// the host reads kErrTimeout from the status word.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -47,11 +59,15 @@ __device__ int g_tc_status;  // first error recorded by any kernel of this unit
 
 namespace {
 
-constexpr int kBM = 128;       // rows of A / C per tile (= TMEM lanes)
-constexpr int kBK = 32;        // K per stage: 32 fp32 = one 128-byte swizzle row
-constexpr int kUmmaK = 8;      // K per tcgen05.mma of kind::tf32
-constexpr int kGroupM = 8;     // m-blocks per raster group
-constexpr uint32_t kSw128 = 2; // descriptor layout type: 128-byte swizzle
+constexpr int kTM = 256;        // rows of C per tile   (MMA N)
+constexpr int kTN = 128;        // columns of C per tile (MMA M = TMEM lanes)
+constexpr int kBK = 32;         // K per stage: 32 fp32 = one 128-byte swizzle row of A
+constexpr int kUmmaK = 8;       // K per tcgen05.mma of kind::tf32
+constexpr int kGroupM = 8;      // m-blocks per raster group
+constexpr uint32_t kSw128 = 2;  // descriptor layout type: 128-byte swizzle
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol = 0;    // D: columns [0, 256)
+constexpr uint32_t kBtCol = 256;   // B^T stage buffers from column 256
 
 struct TcParams {
   int M, N, K;
@@ -62,40 +78,38 @@ struct TcParams {
   float *C;
   long long ldc;
   int num_m_blocks, num_n_blocks, num_tiles, num_k_blocks;
-  int vec_store;  // C 16-byte aligned and ldc % 4 == 0
   unsigned long long timeout_ns;
 };
 
-template <int BN, int STAGES, bool EXACT, bool LSU>
+template <int STAGES, bool EXACT, bool LSU>
 struct TcConfig {
-  static constexpr int kABytes = kBM * kBK * 4;               // 16 KiB
-  static constexpr int kBChunkBytes = kBK * 128;              // 32 rows x 32 columns
-  static constexpr int kBBytes = (BN / 32) * kBChunkBytes;    // BN / 32 chunks
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kLoOffset = STAGES * kStageBytes;      // sibling lo tiles (3xTF32)
-  static constexpr int kTileBytes = (EXACT ? 2 : 1) * STAGES * kStageBytes;
+  static constexpr int kABytes = kTM * kBK * 4;                  // 32 KiB, K-major, swizzled
+  static constexpr int kBBytes = LSU ? 0 : kBK * kTN * 4;        // 16 KiB, row-major (TMA)
+  static constexpr int kALoBytes = EXACT ? kABytes : 0;          // 3xTF32 lo tile of A
+  static constexpr int kStageBytes = kABytes + kBBytes + kALoBytes;
+  static constexpr int kBOffset = kABytes;
+  static constexpr int kALoOffset = kABytes + kBBytes;
+  static constexpr int kTileBytes = STAGES * kStageBytes;
+  static constexpr uint32_t kBtColsPerStage = EXACT ? 2 * kBK : kBK;  // hi (+ lo)
   static constexpr int kProdWarps = LSU ? 4 : 1;
   static constexpr int kMmaWarp = kProdWarps;
   static constexpr int kEpiWarp0 = kMmaWarp + 1;
-  static constexpr int kXformWarps = (EXACT && !LSU) ? 4 : 0;
+  static constexpr int kXformWarps = LSU ? 0 : 4;
   static constexpr int kXformWarp0 = kEpiWarp0 + 4;
   static constexpr int kThreads = 32 * (kXformWarp0 + kXformWarps);
-  static constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
-  static constexpr uint32_t kIdesc = idesc_tf32(kBM, BN, /*b_mn_major=*/true);
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
-  static_assert(kTmemCols == 64 || kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512,
-                "TMEM allocation must be a power of two");
+  static constexpr uint32_t kIdesc = idesc_tf32(kTN, kTM);
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(kBtCol + STAGES * kBtColsPerStage <= kTmemCols, "TMEM budget");
 };
 
 template <int STAGES>
 struct alignas(8) TcShared {
-  uint64_t full[STAGES];   // stage filled (TMA bytes, or LSU producer warps)
-  uint64_t ready[STAGES];  // stage split into hi/lo (3xTF32 with TMA)
+  uint64_t full[STAGES];   // stage loaded (TMA bytes, or the LSU producer warps)
+  uint64_t ready[STAGES];  // B^T in TMEM (and A split) by the transform warps
   uint64_t empty[STAGES];  // stage consumed by the MMAs (tcgen05.commit)
-  uint64_t acc_full[2];    // accumulator complete (tcgen05.commit)
-  uint64_t acc_empty[2];   // accumulator drained by the epilogue warps
-  uint64_t drain;          // all MMAs issued by this CTA have completed
+  uint64_t acc_full;       // accumulator complete (tcgen05.commit)
+  uint64_t acc_empty;      // accumulator drained by the epilogue warps
+  uint64_t drain;          // every MMA of this CTA has completed
   uint32_t tmem_base;
   int abort;
 };
@@ -110,17 +124,16 @@ __device__ __forceinline__ void tile_coords(const TcParams &p, int t, int &mb, i
   nb = r / gm;
 }
 
-// Byte offset of element (row, col4 * 4 bytes) inside a tile whose rows are
-// 128 bytes and whose 1024-byte groups of 8 rows carry the 128-byte swizzle:
-// 16-byte chunk index XOR (row mod 8).
+// 128-byte swizzle inside 1024-byte groups of eight 128-byte rows: the
+// 16-byte chunk index is XORed with the row index mod 8.
 __device__ __forceinline__ uint32_t sw128(uint32_t linear) {
   return linear ^ (((linear >> 7) & 7u) << 4);
 }
 
-// Wait with a warp-uniform outcome (all lanes of the warp wait).
+// Wait with a warp-uniform outcome (every lane of the warp waits).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const TcParams &p,
                                           volatile int *abort) {
-  bool ok = mbar_wait_bounded(bar, parity, p.timeout_ns, abort, &g_tc_status);
+  const bool ok = mbar_wait_bounded(bar, parity, p.timeout_ns, abort, &g_tc_status);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -133,43 +146,45 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint6
   }
 }
 
-__device__ __forceinline__ void store_row_chunk(const TcParams &p, int gm, int gn,
-                                                const uint32_t (&r)[32]) {
-  if (gm >= p.M) return;
-  float *dst = p.C + static_cast<long long>(gm) * p.ldc + gn;
-  if (p.vec_store && gn + 32 <= p.N) {
+// 32 values of B^T row n (k = 0..31 of the stage) into TMEM, raw or as the
+// 3xTF32 pair hi = tf32(x), lo = tf32(x - hi).
+template <bool EXACT>
+__device__ __forceinline__ void bt_to_tmem(uint32_t t_hi, uint32_t t_lo, const float (&v)[32]) {
+  uint32_t hi[32];
+  if (EXACT) {
+    uint32_t lo[32];
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                             __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-      *reinterpret_cast<float4 *>(dst + j) = v;
+    for (int k = 0; k < 32; ++k) {
+      const float h = round_tf32(v[k]);
+      hi[k] = __float_as_uint(h);
+      lo[k] = __float_as_uint(round_tf32(v[k] - h));
     }
+    tmem_store_32cols(t_hi, hi);
+    tmem_store_32cols(t_lo, lo);
   } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (gn + j < p.N) dst[j] = __uint_as_float(r[j]);
+    for (int k = 0; k < 32; ++k) hi[k] = __float_as_uint(v[k]);
+    tmem_store_32cols(t_hi, hi);
   }
 }
 
-// Stage one value: raw (TF32 mode: the tensor core drops the low 13 bits) or
-// the 3xTF32 pair hi = tf32(x), lo = tf32(x - hi).
-template <bool EXACT, int LO_OFFSET>
-__device__ __forceinline__ void stage_value(uint8_t *tile, uint32_t off, float v) {
+template <bool EXACT>
+__device__ __forceinline__ void stage_a_value(uint8_t *stage, int lo_offset, uint32_t off,
+                                              float v) {
   if (EXACT) {
     const float hi = round_tf32(v);
-    const float lo = round_tf32(v - hi);
-    *reinterpret_cast<float *>(tile + off) = hi;
-    *reinterpret_cast<float *>(tile + LO_OFFSET + off) = lo;
+    *reinterpret_cast<float *>(stage + off) = hi;
+    *reinterpret_cast<float *>(stage + lo_offset + off) = round_tf32(v - hi);
   } else {
-    *reinterpret_cast<float *>(tile + off) = v;
+    *reinterpret_cast<float *>(stage + off) = v;
   }
 }
 
-template <int BN, int STAGES, bool EXACT, bool LSU>
-__global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
+template <int STAGES, bool EXACT, bool LSU>
+__global__ void __launch_bounds__(TcConfig<STAGES, EXACT, LSU>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
-  using Cfg = TcConfig<BN, STAGES, EXACT, LSU>;
+  using Cfg = TcConfig<STAGES, EXACT, LSU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -185,10 +200,8 @@ __global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
       mbar_init(&sh->ready[s], Cfg::kXformWarps > 0 ? Cfg::kXformWarps : 1);
       mbar_init(&sh->empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&sh->acc_full[a], 1);
-      mbar_init(&sh->acc_empty[a], 4);
-    }
+    mbar_init(&sh->acc_full, 1);
+    mbar_init(&sh->acc_empty, 4);
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_barrier_init();
@@ -198,7 +211,7 @@ __global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
     tma_prefetch_map(&tmap_b);
   }
   if (warp == Cfg::kMmaWarp) {
-    tmem_alloc(&sh->tmem_base, Cfg::kTmemCols);
+    tmem_alloc(&sh->tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
@@ -207,7 +220,7 @@ __global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
   const uint32_t tmem = sh->tmem_base;
 
   if (!LSU && warp == 0) {
-    // ---------------------------------------------------- TMA producer --
+    // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
@@ -220,14 +233,10 @@ __global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
             ok = false;
             break;
           }
-          uint8_t *a_dst = tiles + stage * Cfg::kStageBytes;
-          uint8_t *b_dst = a_dst + Cfg::kABytes;
-          mbar_arrive_expect_tx(&sh->full[stage], Cfg::kStageBytes);
-          tma_load_2d(a_dst, &tmap_a, &sh->full[stage], kb * kBK, mb * kBM);
-#pragma unroll
-          for (int c = 0; c < BN / 32; ++c)
-            tma_load_2d(b_dst + c * Cfg::kBChunkBytes, &tmap_b, &sh->full[stage],
-                        nb * BN + c * 32, kb * kBK);
+          uint8_t *st = tiles + stage * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(&sh->full[stage], Cfg::kABytes + kBK * kTN * 4);
+          tma_load_2d(st, &tmap_a, &sh->full[stage], kb * kBK, mb * kTM);
+          tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], nb * kTN, kb * kBK);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -243,62 +252,53 @@ __global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
       }
     }
   } else if (LSU && warp < Cfg::kProdWarps) {
-    // ---------------------------------------------------- LSU producer --
+    // ------------------------------------------------------ LSU producer --
+    // Warp w stages A rows w, w + 4, ... (lane = k) and B^T rows
+    // n = 32 w + lane (TMEM lanes of this warp's quadrant).
     uint32_t stage = 0, phase = 0;
+    const uint32_t quad = warp & 3;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(p, t, mb, nb);
-      const int m0 = mb * kBM, n0 = nb * BN;
+      const int m0 = mb * kTM, n0 = nb * kTN;
       bool ok = true;
       for (int kb = 0; kb < p.num_k_blocks; ++kb) {
         if (!warp_wait(&sh->empty[stage], phase ^ 1, p, abort)) {
           ok = false;
           break;
         }
-        uint8_t *a_st = tiles + stage * Cfg::kStageBytes;
-        uint8_t *b_st = a_st + Cfg::kABytes;
+        tc_fence_after_sync();
+        uint8_t *st = tiles + stage * Cfg::kStageBytes;
         const int k0 = kb * kBK;
-        {
-          // A: warp w stages rows w, w + 4, ..., lane = k within the stage.
-          const int gk = k0 + lane;
+        const int gk = k0 + lane;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int gm = m0 + warp + 4 * i;
+            const int gm = m0 + warp + 4 * (half * 32 + i);
             v[i] = (gm < p.M && gk < p.K) ? __ldg(p.A + static_cast<long long>(gm) * p.lda + gk)
                                           : 0.0f;
           }
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            stage_value<EXACT, Cfg::kLoOffset>(a_st, sw128((warp + 4 * i) * 128 + lane * 4),
-                                               v[i]);
+            stage_a_value<EXACT>(st, Cfg::kALoOffset,
+                                 sw128((warp + 4 * (half * 32 + i)) * 128 + lane * 4), v[i]);
         }
+        {
+          const int gn = n0 + quad * 32 + lane;
+          float v[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          // B: warp w stages k-rows w + 4 i (i in this half), lane = column in a chunk.
-          float v[4][BN / 32];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int kr = warp + 4 * (half * 4 + i);
-            const int gk = k0 + kr;
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-              const int gn = n0 + c * 32 + lane;
-              v[i][c] = (gk < p.K && gn < p.N)
-                            ? __ldg(p.B + static_cast<long long>(gk) * p.ldb + gn)
-                            : 0.0f;
-            }
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int kr = warp + 4 * (half * 4 + i);
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c)
-              stage_value<EXACT, Cfg::kLoOffset>(
-                  b_st, c * Cfg::kBChunkBytes + sw128(kr * 128 + lane * 4), v[i][c]);
-          }
+          for (int k = 0; k < 32; ++k)
+            v[k] = (gn < p.N && k0 + k < p.K)
+                       ? __ldg(p.B + static_cast<long long>(k0 + k) * p.ldb + gn)
+                       : 0.0f;
+          const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol + stage * Cfg::kBtColsPerStage;
+          bt_to_tmem<EXACT>(col, col + kBK, v);
         }
         fence_proxy_async_smem();
+        tmem_store_wait();
+        tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->full[stage]);
         if (++stage == STAGES) {
@@ -311,43 +311,38 @@ __global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
   } else if (warp == Cfg::kMmaWarp) {
     // -------------------------------------------------------------- MMA --
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true;
+      const uint32_t d_tmem = tmem + kAccCol;
       for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-        if (!mbar_wait_bounded(&sh->acc_empty[acc], acc_phase ^ 1, p.timeout_ns, abort,
+        if (!mbar_wait_bounded(&sh->acc_empty, acc_phase ^ 1, p.timeout_ns, abort,
                                &g_tc_status)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem + acc * BN;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          uint64_t *in_bar = (EXACT && !LSU) ? &sh->ready[stage] : &sh->full[stage];
+          uint64_t *in_bar = LSU ? &sh->full[stage] : &sh->ready[stage];
           if (!mbar_wait_bounded(in_bar, phase, p.timeout_ns, abort, &g_tc_status)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint32_t a_hi = smem_addr(tiles + stage * Cfg::kStageBytes);
-          const uint32_t b_hi = a_hi + Cfg::kABytes;
+          const uint32_t bt_hi = tmem + kBtCol + stage * Cfg::kBtColsPerStage;
 #pragma unroll
           for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
-            // A is K-major: a k-step of 8 fp32 is 32 bytes along the swizzled row.
-            // B is MN-major: a k-step is one 8-row, 1024-byte swizzle atom;
-            // 32-column chunks are kBChunkBytes apart (leading byte offset).
+            // A tile, K-major: a k-step of 8 fp32 is 32 bytes along the swizzled row;
+            // 8-row groups are 1024 bytes apart.
             const uint64_t da = smem_desc(a_hi + kk * 32, 16, 1024, kSw128);
-            const uint64_t db = smem_desc(b_hi + kk * 1024, Cfg::kBChunkBytes, 1024, kSw128);
             const uint32_t accumulate = (kb | kk) != 0;
             if (EXACT) {
-              const uint64_t da_lo =
-                  smem_desc(a_hi + Cfg::kLoOffset + kk * 32, 16, 1024, kSw128);
-              const uint64_t db_lo =
-                  smem_desc(b_hi + Cfg::kLoOffset + kk * 1024, Cfg::kBChunkBytes, 1024, kSw128);
-              mma_tf32(d_tmem, da_lo, db, Cfg::kIdesc, accumulate);
-              mma_tf32(d_tmem, da, db_lo, Cfg::kIdesc, 1);
-              mma_tf32(d_tmem, da, db, Cfg::kIdesc, 1);
+              const uint64_t da_lo = smem_desc(a_hi + Cfg::kALoOffset + kk * 32, 16, 1024, kSw128);
+              mma_tf32_ts(d_tmem, bt_hi + kBK + kk * kUmmaK, da, Cfg::kIdesc, accumulate);
+              mma_tf32_ts(d_tmem, bt_hi + kk * kUmmaK, da_lo, Cfg::kIdesc, 1);
+              mma_tf32_ts(d_tmem, bt_hi + kk * kUmmaK, da, Cfg::kIdesc, 1);
             } else {
-              mma_tf32(d_tmem, da, db, Cfg::kIdesc, accumulate);
+              mma_tf32_ts(d_tmem, bt_hi + kk * kUmmaK, da, Cfg::kIdesc, accumulate);
             }
           }
           mma_commit(&sh->empty[stage]);
@@ -357,9 +352,8 @@ __global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(&sh->acc_full[acc]);
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        mma_commit(&sh->acc_full);
+        acc_phase ^= 1;
       }
       // Every MMA this thread issued completes before TMEM is released.
       mma_commit(&sh->drain);
@@ -368,34 +362,45 @@ __global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
     __syncwarp();
   } else if (warp >= Cfg::kEpiWarp0 && warp < Cfg::kEpiWarp0 + 4) {
     // --------------------------------------------------------- epilogue --
-    const uint32_t quad = warp & 3;  // TMEM lanes this warp may read
-    uint32_t acc = 0, acc_phase = 0;
+    const uint32_t quad = warp & 3;  // TMEM lanes (columns of C) this warp may read
+    uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(p, t, mb, nb);
-      if (!warp_wait(&sh->acc_full[acc], acc_phase, p, abort)) break;
+      if (!warp_wait(&sh->acc_full, acc_phase, p, abort)) break;
       tc_fence_after_sync();
-      const int gm = mb * kBM + quad * 32 + lane;
-      const uint32_t t_row = tmem + ((quad * 32) << 16) + acc * BN;
+      const int gn = nb * kTN + quad * 32 + lane;
+      const bool n_ok = gn < p.N;
+      const uint32_t t_lane = tmem + ((quad * 32) << 16) + kAccCol;
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int gn = nb * BN + c * 32;
-        if (gn >= p.N) break;
+      for (int c = 0; c < kTM / 32; ++c) {
+        const int gm0 = mb * kTM + c * 32;
+        if (gm0 >= p.M) break;
         uint32_t r[32];
-        tmem_load_32cols(t_row + c * 32, r);
+        tmem_load_32cols(t_lane + c * 32, r);
         tmem_load_wait();
-        store_row_chunk(p, gm, gn, r);
+        float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
+        const int rows = min(32, p.M - gm0);
+        if (n_ok) {
+          if (rows == 32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < rows) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+          }
+        }
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if (lane == 0) mbar_arrive(&sh->acc_empty);
+      acc_phase ^= 1;
     }
   } else if (Cfg::kXformWarps > 0 && warp >= Cfg::kXformWarp0) {
-    // ---------------------------------------------- 3xTF32 split (TMA) --
-    const int xt = threadIdx.x - Cfg::kXformWarp0 * 32;
-    constexpr int kVecs = Cfg::kStageBytes / 16;
+    // -------------------------------------------- transform (TMA variant) --
+    const uint32_t quad = warp & 3;
+    const int xt = threadIdx.x - Cfg::kXformWarp0 * 32;  // 0..127
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
@@ -404,24 +409,40 @@ __global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
           ok = false;
           break;
         }
-        float4 *raw = reinterpret_cast<float4 *>(tiles + stage * Cfg::kStageBytes);
-        float4 *lo = reinterpret_cast<float4 *>(tiles + Cfg::kLoOffset + stage * Cfg::kStageBytes);
-#pragma unroll 4
-        for (int i = xt; i < kVecs; i += 32 * Cfg::kXformWarps) {
-          const float4 x = raw[i];
-          float4 h, l;
-          h.x = round_tf32(x.x);
-          h.y = round_tf32(x.y);
-          h.z = round_tf32(x.z);
-          h.w = round_tf32(x.w);
-          l.x = round_tf32(x.x - h.x);
-          l.y = round_tf32(x.y - h.y);
-          l.z = round_tf32(x.z - h.z);
-          l.w = round_tf32(x.w - h.w);
-          raw[i] = h;
-          lo[i] = l;
+        tc_fence_after_sync();
+        uint8_t *st = tiles + stage * Cfg::kStageBytes;
+        {
+          // B tile is row-major 32 k x 128 n (512-byte rows); this thread's
+          // column n = 32 quad + lane becomes TMEM lane n.
+          const float *bs = reinterpret_cast<const float *>(st + Cfg::kBOffset) + quad * 32 + lane;
+          float v[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = bs[k * kTN];
+          const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol + stage * Cfg::kBtColsPerStage;
+          bt_to_tmem<EXACT>(col, col + kBK, v);
         }
-        fence_proxy_async_smem();
+        if (EXACT) {
+          float4 *raw = reinterpret_cast<float4 *>(st);
+          float4 *lo = reinterpret_cast<float4 *>(st + Cfg::kALoOffset);
+#pragma unroll 4
+          for (int i = xt; i < Cfg::kABytes / 16; i += 32 * Cfg::kXformWarps) {
+            const float4 x = raw[i];
+            float4 h, l;
+            h.x = round_tf32(x.x);
+            h.y = round_tf32(x.y);
+            h.z = round_tf32(x.z);
+            h.w = round_tf32(x.w);
+            l.x = round_tf32(x.x - h.x);
+            l.y = round_tf32(x.y - h.y);
+            l.z = round_tf32(x.z - h.z);
+            l.w = round_tf32(x.w - h.w);
+            raw[i] = h;
+            lo[i] = l;
+          }
+          fence_proxy_async_smem();
+        }
+        tmem_store_wait();
+        tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->ready[stage]);
         if (++stage == STAGES) {
@@ -436,7 +457,7 @@ __global__ void __launch_bounds__(TcConfig<BN, STAGES, EXACT, LSU>::kThreads, 1)
   __syncthreads();
   if (warp == Cfg::kMmaWarp) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, Cfg::kTmemCols);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -474,14 +495,14 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Small cache of encoded tensor maps keyed by (address, extents, pitch, box).
+// Small cache of encoded tensor maps keyed by (address, extents, pitch, box, swizzle).
 struct MapKey {
   const void *ptr;
   uint64_t d0, d1, pitch;
-  uint32_t b0, b1;
+  uint32_t b0, b1, swizzle;
   bool operator==(const MapKey &o) const {
     return ptr == o.ptr && d0 == o.d0 && d1 == o.d1 && pitch == o.pitch && b0 == o.b0 &&
-           b1 == o.b1;
+           b1 == o.b1 && swizzle == o.swizzle;
   }
 };
 
@@ -495,11 +516,11 @@ struct MapCache {
 };
 
 // 2-D fp32 tensor map over a row-major matrix (d0 = columns, d1 = rows) with a
-// b0 x b1 box, 128-byte swizzle and zero fill outside the matrix.
+// b0 x b1 box, the given swizzle, and zero fill outside the matrix.
 bool get_map(const void *ptr, uint64_t d0, uint64_t d1, uint64_t pitch_bytes, uint32_t b0,
-             uint32_t b1, CUtensorMap *out) {
+             uint32_t b1, CUtensorMapSwizzle swizzle, CUtensorMap *out) {
   static MapCache cache;
-  const MapKey key{ptr, d0, d1, pitch_bytes, b0, b1};
+  const MapKey key{ptr, d0, d1, pitch_bytes, b0, b1, static_cast<uint32_t>(swizzle)};
   {
     std::lock_guard<std::mutex> g(cache.mu);
     for (int i = 0; i < MapCache::kSlots; ++i)
@@ -517,8 +538,8 @@ bool get_map(const void *ptr, uint64_t d0, uint64_t d1, uint64_t pitch_bytes, ui
   CUtensorMap m;
   std::memset(&m, 0, sizeof(m));
   if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box,
-         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
   std::lock_guard<std::mutex> g(cache.mu);
   const int slot = cache.next;
@@ -530,10 +551,10 @@ bool get_map(const void *ptr, uint64_t d0, uint64_t d1, uint64_t pitch_bytes, ui
   return true;
 }
 
-template <int BN, int STAGES, bool EXACT, bool LSU>
+template <int STAGES, bool EXACT, bool LSU>
 int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
-  using Cfg = TcConfig<BN, STAGES, EXACT, LSU>;
-  auto kernel = tc_gemm_kernel<BN, STAGES, EXACT, LSU>;
+  using Cfg = TcConfig<STAGES, EXACT, LSU>;
+  auto kernel = tc_gemm_kernel<STAGES, EXACT, LSU>;
   const int smem_bytes = Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
 
   int dev = 0;
@@ -554,8 +575,10 @@ int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   std::memset(&map_a, 0, sizeof(map_a));
   std::memset(&map_b, 0, sizeof(map_b));
   if (!LSU) {
-    if (!get_map(a.A, a.K, a.M, a.lda * 4, kBK, kBM, &map_a)) return kErrLaunch;
-    if (!get_map(a.B, a.N, a.K, a.ldb * 4, 32, kBK, &map_b)) return kErrLaunch;
+    if (!get_map(a.A, a.K, a.M, a.lda * 4, kBK, kTM, CU_TENSOR_MAP_SWIZZLE_128B, &map_a))
+      return kErrLaunch;
+    if (!get_map(a.B, a.N, a.K, a.ldb * 4, kTN, kBK, CU_TENSOR_MAP_SWIZZLE_NONE, &map_b))
+      return kErrLaunch;
   }
 
   TcParams p;
@@ -568,11 +591,10 @@ int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   p.ldb = a.ldb;
   p.C = a.C;
   p.ldc = a.ldc;
-  p.num_m_blocks = static_cast<int>((a.M + kBM - 1) / kBM);
-  p.num_n_blocks = static_cast<int>((a.N + BN - 1) / BN);
+  p.num_m_blocks = static_cast<int>((a.M + kTM - 1) / kTM);
+  p.num_n_blocks = static_cast<int>((a.N + kTN - 1) / kTN);
   p.num_tiles = p.num_m_blocks * p.num_n_blocks;
   p.num_k_blocks = static_cast<int>((a.K + kBK - 1) / kBK);
-  p.vec_store = (reinterpret_cast<uintptr_t>(a.C) % 16 == 0) && (a.ldc % 4 == 0);
   // Generous: a stage takes microseconds; one tile's mainloop about K * 25 ns.
   p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
 
@@ -597,11 +619,11 @@ bool tc_tma_legal(const GemmArgs &a) {
 
 int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream) {
   if (exact) {
-    if (lsu) return launch_variant<256, 2, true, true>(a, sm_count, stream);
-    return launch_variant<256, 2, true, false>(a, sm_count, stream);
+    if (lsu) return launch_variant<2, true, true>(a, sm_count, stream);
+    return launch_variant<2, true, false>(a, sm_count, stream);
   }
-  if (lsu) return launch_variant<256, 4, false, true>(a, sm_count, stream);
-  return launch_variant<256, 4, false, false>(a, sm_count, stream);
+  if (lsu) return launch_variant<4, false, true>(a, sm_count, stream);
+  return launch_variant<4, false, false>(a, sm_count, stream);
 }
 
 int tc_poll_status(cudaStream_t stream) {

@@ -43,6 +43,10 @@ def run(g, a, b, mode="exact", kernel="auto", lda=None, ldb=None, ldc=None, c_fi
     """C = A x B through gemm_f32_ex; returns (C as numpy, full C buffer as numpy)."""
     m, k = a.shape
     _, n = b.shape
+    if kernel == "tc_tma":
+        # the TMA-fed kernel needs row pitches that are multiples of 16 bytes
+        lda = lda or -(-max(k, 1) // 4) * 4
+        ldb = ldb or -(-max(n, 1) // 4) * 4
     da, db = to_dev(a, lda), to_dev(b, ldb)
     ldc = ldc or max(n, 1)
     dc = torch.full((max(m, 1), ldc), c_fill, dtype=torch.float32, device="cuda")
