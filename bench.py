@@ -1,7 +1,7 @@
 """Benchmark: fp32 GEMM C = A x B at M = N = K = 4096 on GB300 (libgemm_f32).
 
 One step = one gemm_f32 call in `exact` mode (FP32-accurate 3xTF32 on the
-tensor cores) on the square 4096^3 workload: A, B i.i.d. uniform[-1, 1) from
+tensor cores; `--mode` selects another mode) on the square 4096^3 workload: A, B i.i.d. uniform[-1, 1) from
 fixed seeds, row-major, C overwritten. Inputs are resident in HBM before the
 timed region; L2 is flushed (a 256 MiB write) between timed steps, outside the
 per-step CUDA events. Prints ONE JSON line (rank 0).
@@ -44,6 +44,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--mode", default="exact", choices=["exact", "tf32", "exact_simt"],
+                    help="accuracy mode of the timed steps (the headline is exact)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other modes, e2e and CPU legs")
     return ap.parse_args()
 
@@ -171,7 +173,8 @@ def traffic_lookup(kernel: str, workload: str, mode: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source."""
     src = hashlib.sha256()
-    for f in ("tc_gemm.cu", "ptx.cuh"):
+    files = ("simt_gemm.cu",) if kernel.startswith("simt") else ("tc_gemm.cu", "ptx.cuh")
+    for f in files:
         with open(os.path.join(ROOT, "dense_fp32_gemm_major_gb300", "csrc", f), "rb") as fh:
             src.update(fh.read())
     sha = src.hexdigest()[:16]
@@ -287,15 +290,17 @@ def main():
                 raise g.GemmError(st)
         return fn
 
+    mode = g.MODES[args.mode]
     kernel = g.gemm_f32_select(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N,
-                               g.EXACT, g.KERNEL_AUTO)
-    kernel_name = {g.KERNEL_SIMT: "simt_gemm", g.KERNEL_TC_TMA: "tc_gemm_tma_3xtf32",
-                   g.KERNEL_TC_LSU: "tc_gemm_lsu_3xtf32"}.get(kernel, str(kernel))
+                               mode, g.KERNEL_AUTO)
+    suffix = "3xtf32" if args.mode == "exact" else "tf32"
+    kernel_name = {g.KERNEL_SIMT: "simt_gemm", g.KERNEL_TC_TMA: f"tc_gemm_tma_{suffix}",
+                   g.KERNEL_TC_LSU: f"tc_gemm_lsu_{suffix}"}.get(kernel, str(kernel))
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
         sampler.start()
-    fn = gemm_call(g.EXACT)
+    fn = gemm_call(mode)
     for _ in range(args.warmup):
         flush.zero_()
         fn()
@@ -321,26 +326,37 @@ def main():
 
     pk = peaks()
     tf32_peak = pk["bf16"] * TF32_PER_BF16
-    achieved = 3 * flops / (ms_per_step / 1e3) / 1e12  # 3 TF32 MMAs per FMA (3xTF32)
-    traffic, sha = traffic_lookup("tc_gemm_tma_3xtf32", "c4", "exact")
-    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(tf32_peak, 1),
-                "unit": "TFLOP/s", "frac": round(achieved / tf32_peak, 4), "traffic": traffic,
-                "kernel": kernel_name,
-                "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x nominal "
-                               f"TF32/BF16 ratio {TF32_PER_BF16:.4f}",
-                "achieved_counts": "3 x 2MNK (three TF32 MMAs per fp32 multiply-add)"}
+    alu_peak = SMS * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+    traffic, sha = traffic_lookup(kernel_name, "c4", args.mode)
+    if args.mode == "exact_simt":
+        achieved = flops / (ms_per_step / 1e3) / 1e12
+        roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(alu_peak, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / alu_peak, 4), "traffic": traffic,
+                    "kernel": kernel_name,
+                    "peak_source": f"{SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x "
+                                   f"{pk['sm_max_mhz']:.0f} MHz"}
+    else:
+        mult = 3 if args.mode == "exact" else 1  # 3xTF32: three TF32 MMAs per fp32 multiply-add
+        achieved = mult * flops / (ms_per_step / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(tf32_peak, 1),
+                    "unit": "TFLOP/s", "frac": round(achieved / tf32_peak, 4), "traffic": traffic,
+                    "kernel": kernel_name,
+                    "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x nominal "
+                                   f"TF32/BF16 ratio {TF32_PER_BF16:.4f}",
+                    "achieved_counts": f"{mult} x 2MNK TF32 flops"}
 
     extras = {}
     cpu = None
     e2e = None
     if rank == 0 and not args.no_extras:
         # the other modes, fewer steps, same protocol
-        for mname, mode, bound, peak, mult in (
-                ("tf32", g.TF32, "tensor", tf32_peak, 1),
-                ("exact_simt", g.EXACT_SIMT, "alu",
-                 SMS * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12, 1)):
-            steps = 200 if mname == "tf32" else 30
-            ts, _ = time_steps(torch, gemm_call(mode), steps, 5, flush, stream)
+        others = [("exact", g.EXACT, "tensor", tf32_peak, 3), ("tf32", g.TF32, "tensor", tf32_peak, 1),
+                  ("exact_simt", g.EXACT_SIMT, "alu", alu_peak, 1)]
+        for mname, mcode, bound, peak, mult in others:
+            if mname == args.mode:
+                continue
+            steps = 30 if mname == "exact_simt" else 200
+            ts, _ = time_steps(torch, gemm_call(mcode), steps, 5, flush, stream)
             ms = statistics.mean(ts)
             ach = mult * flops / (ms / 1e3) / 1e12
             extras[mname] = {"value": round(flops / (ms / 1e3) / 1e9, 1), "unit": "GFLOP/s",
@@ -374,7 +390,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "mode": "exact",
+            "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "mode": args.mode,
                        "kernel": kernel_name, "l2": "flushed (256 MiB write) between timed steps",
                        "replicas": world, "parallelism": "replicas" if world > 1 else "single"},
             "roofline": roofline,

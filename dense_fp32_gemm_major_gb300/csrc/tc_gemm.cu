@@ -16,13 +16,15 @@
 // of C (a coalesced 128-byte segment).
 //
 // Roles (warp-specialised, persistent, one CTA per SM, grouped raster):
-//   producer   TMA: one thread loads the 256 x 32 A tile (128-byte swizzle)
-//              and the 32 x 128 B tile per stage into a ring of stages.
+//   producer   TMA: one thread loads the 256 x BK A tile (swizzled, K-major)
+//              and the BK x 128 B tile per stage into a ring of stages
+//              (BK = 16 or 32 k per stage).
 //              LSU (operands TMA cannot describe): four warps load both with
 //              plain loads and place the A tile in shared memory and B^T in
 //              TMEM themselves.
-//   transform  (TMA variant) four warps move B^T into TMEM and, in 3xTF32
-//              mode, split the A tile into hi (in place) and lo (sibling tile).
+//   transform  (TMA variant) 8 (tf32) or 16 (3xTF32) warps move B^T into TMEM
+//              and, in 3xTF32 mode, split the A tile into hi (in place) and lo
+//              (sibling tile).
 //   MMA        one thread issues tcgen05.mma kind::tf32, M = 128, N = 256,
 //              K = 8. 3xTF32 issues B_lo*A_hi, B_hi*A_lo, B_hi*A_hi per k-step
 //              (small terms first), hi = tf32(x), lo = tf32(x - hi).
@@ -61,10 +63,8 @@ namespace {
 
 constexpr int kTM = 256;        // rows of C per tile   (MMA N)
 constexpr int kTN = 128;        // columns of C per tile (MMA M = TMEM lanes)
-constexpr int kBK = 32;         // K per stage: 32 fp32 = one 128-byte swizzle row of A
 constexpr int kUmmaK = 8;       // K per tcgen05.mma of kind::tf32
 constexpr int kGroupM = 8;      // m-blocks per raster group
-constexpr uint32_t kSw128 = 2;  // descriptor layout type: 128-byte swizzle
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;    // D: columns [0, 256)
 constexpr uint32_t kBtCol = 256;   // B^T stage buffers from column 256
@@ -81,24 +81,36 @@ struct TcParams {
   unsigned long long timeout_ns;
 };
 
-template <int STAGES, bool EXACT, bool LSU>
+// BK = K per stage: 32 (A rows of 128 bytes, 128-byte swizzle) or 16 (rows of
+// 64 bytes, 64-byte swizzle). Either way a row of the A tile is one swizzle
+// span, 8-row groups are the swizzle atom, and a k-step of 8 advances the
+// descriptor by 32 bytes along the row.
+template <int BK, int STAGES, bool EXACT, bool LSU>
 struct TcConfig {
-  static constexpr int kABytes = kTM * kBK * 4;                  // 32 KiB, K-major, swizzled
-  static constexpr int kBBytes = LSU ? 0 : kBK * kTN * 4;        // 16 KiB, row-major (TMA)
+  static_assert(BK == 16 || BK == 32, "BK");
+  static constexpr int kRowBytes = BK * 4;                       // one row of the A tile
+  static constexpr int kAtomBytes = 8 * kRowBytes;               // 8-row swizzle atom (SBO)
+  static constexpr uint32_t kLayout = BK == 32 ? 2u : 4u;        // 128- or 64-byte swizzle
+  static constexpr int kABytes = kTM * BK * 4;                   // A tile, K-major, swizzled
+  static constexpr int kBBytes = LSU ? 0 : BK * kTN * 4;         // B tile, row-major (TMA)
   static constexpr int kALoBytes = EXACT ? kABytes : 0;          // 3xTF32 lo tile of A
   static constexpr int kStageBytes = kABytes + kBBytes + kALoBytes;
   static constexpr int kBOffset = kABytes;
   static constexpr int kALoOffset = kABytes + kBBytes;
   static constexpr int kTileBytes = STAGES * kStageBytes;
-  static constexpr uint32_t kBtColsPerStage = EXACT ? 2 * kBK : kBK;  // hi (+ lo)
+  static constexpr uint32_t kBtColsPerStage = EXACT ? 2 * BK : BK;  // hi (+ lo)
   static constexpr int kProdWarps = LSU ? 4 : 1;
   static constexpr int kMmaWarp = kProdWarps;
   static constexpr int kEpiWarp0 = kMmaWarp + 1;
-  static constexpr int kXformWarps = LSU ? 0 : 4;
+  // Transform warps, a multiple of 4 (whole TMEM lane quadrants). The 3xTF32
+  // split is the most work per stage: 16 warps keep it ahead of the MMAs.
+  static constexpr int kXformWarps = LSU ? 0 : (EXACT ? 16 : 8);
+  static constexpr int kXformParts = kXformWarps > 0 ? kXformWarps / 4 : 1;  // per lane quadrant
   static constexpr int kXformWarp0 = kEpiWarp0 + 4;
   static constexpr int kThreads = 32 * (kXformWarp0 + kXformWarps);
   static constexpr uint32_t kIdesc = idesc_tf32(kTN, kTM);
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(kXformWarps % 4 == 0 && BK % kXformParts == 0, "transform partition");
   static_assert(kBtCol + STAGES * kBtColsPerStage <= kTmemCols, "TMEM budget");
 };
 
@@ -124,10 +136,13 @@ __device__ __forceinline__ void tile_coords(const TcParams &p, int t, int &mb, i
   nb = r / gm;
 }
 
-// 128-byte swizzle inside 1024-byte groups of eight 128-byte rows: the
-// 16-byte chunk index is XORed with the row index mod 8.
-__device__ __forceinline__ uint32_t sw128(uint32_t linear) {
-  return linear ^ (((linear >> 7) & 7u) << 4);
+// Swizzled byte offset of a linear offset inside an A tile whose rows are
+// BK * 4 bytes: the 16-byte chunk index within a row is XORed with address
+// bits 7.. (row mod 8 for 128-byte rows, (row / 2) mod 4 for 64-byte rows),
+// the pattern the TMA unit writes and the MMA descriptor expects.
+template <int BK>
+__device__ __forceinline__ uint32_t swizzle_a(uint32_t linear) {
+  return BK == 32 ? linear ^ (((linear >> 7) & 7u) << 4) : linear ^ (((linear >> 7) & 3u) << 4);
 }
 
 // Wait with a warp-uniform outcome (every lane of the warp waits).
@@ -146,25 +161,37 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint6
   }
 }
 
-// 32 values of B^T row n (k = 0..31 of the stage) into TMEM, raw or as the
-// 3xTF32 pair hi = tf32(x), lo = tf32(x - hi).
-template <bool EXACT>
-__device__ __forceinline__ void bt_to_tmem(uint32_t t_hi, uint32_t t_lo, const float (&v)[32]) {
-  uint32_t hi[32];
+template <int W>
+__device__ __forceinline__ void tmem_store_row(uint32_t taddr, const uint32_t (&r)[W]) {
+  if constexpr (W == 32)
+    tmem_store_32cols(taddr, r);
+  else if constexpr (W == 16)
+    tmem_store_16cols(taddr, r);
+  else if constexpr (W == 8)
+    tmem_store_8cols(taddr, r);
+  else
+    tmem_store_4cols(taddr, r);
+}
+
+// W values of B^T row n (part of the stage's k range) into TMEM, raw or as
+// the 3xTF32 pair hi = tf32(x), lo = tf32(x - hi).
+template <int W, bool EXACT>
+__device__ __forceinline__ void bt_to_tmem(uint32_t t_hi, uint32_t t_lo, const float (&v)[W]) {
+  uint32_t hi[W];
   if (EXACT) {
-    uint32_t lo[32];
+    uint32_t lo[W];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < W; ++k) {
       const float h = round_tf32(v[k]);
       hi[k] = __float_as_uint(h);
       lo[k] = __float_as_uint(round_tf32(v[k] - h));
     }
-    tmem_store_32cols(t_hi, hi);
-    tmem_store_32cols(t_lo, lo);
+    tmem_store_row<W>(t_hi, hi);
+    tmem_store_row<W>(t_lo, lo);
   } else {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) hi[k] = __float_as_uint(v[k]);
-    tmem_store_32cols(t_hi, hi);
+    for (int k = 0; k < W; ++k) hi[k] = __float_as_uint(v[k]);
+    tmem_store_row<W>(t_hi, hi);
   }
 }
 
@@ -180,11 +207,11 @@ __device__ __forceinline__ void stage_a_value(uint8_t *stage, int lo_offset, uin
   }
 }
 
-template <int STAGES, bool EXACT, bool LSU>
-__global__ void __launch_bounds__(TcConfig<STAGES, EXACT, LSU>::kThreads, 1)
+template <int BK, int STAGES, bool EXACT, bool LSU>
+__global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
-  using Cfg = TcConfig<STAGES, EXACT, LSU>;
+  using Cfg = TcConfig<BK, STAGES, EXACT, LSU>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -234,9 +261,9 @@ __global__ void __launch_bounds__(TcConfig<STAGES, EXACT, LSU>::kThreads, 1)
             break;
           }
           uint8_t *st = tiles + stage * Cfg::kStageBytes;
-          mbar_arrive_expect_tx(&sh->full[stage], Cfg::kABytes + kBK * kTN * 4);
-          tma_load_2d(st, &tmap_a, &sh->full[stage], kb * kBK, mb * kTM);
-          tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], nb * kTN, kb * kBK);
+          mbar_arrive_expect_tx(&sh->full[stage], Cfg::kABytes + BK * kTN * 4);
+          tma_load_2d(st, &tmap_a, &sh->full[stage], kb * BK, mb * kTM);
+          tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], nb * kTN, kb * BK);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -269,32 +296,41 @@ __global__ void __launch_bounds__(TcConfig<STAGES, EXACT, LSU>::kThreads, 1)
         }
         tc_fence_after_sync();
         uint8_t *st = tiles + stage * Cfg::kStageBytes;
-        const int k0 = kb * kBK;
-        const int gk = k0 + lane;
+        const int k0 = kb * BK;
+        // A: one warp instruction covers 32 / BK rows of BK consecutive k; the
+        // four producer warps interleave, so kTM rows take kASteps instructions.
+        constexpr int kRowsPerInstr = 32 / BK;
+        constexpr int kASteps = kTM / (4 * kRowsPerInstr);
+        const int k_in = lane % BK;
+        const int r_in = lane / BK;
+        const int gk = k0 + k_in;
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
+        for (int chunk = 0; chunk < kASteps / 32; ++chunk) {
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int gm = m0 + warp + 4 * (half * 32 + i);
+            const int row = (chunk * 32 + i) * 4 * kRowsPerInstr + warp * kRowsPerInstr + r_in;
+            const int gm = m0 + row;
             v[i] = (gm < p.M && gk < p.K) ? __ldg(p.A + static_cast<long long>(gm) * p.lda + gk)
                                           : 0.0f;
           }
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < 32; ++i) {
+            const int row = (chunk * 32 + i) * 4 * kRowsPerInstr + warp * kRowsPerInstr + r_in;
             stage_a_value<EXACT>(st, Cfg::kALoOffset,
-                                 sw128((warp + 4 * (half * 32 + i)) * 128 + lane * 4), v[i]);
+                                 swizzle_a<BK>(row * Cfg::kRowBytes + k_in * 4), v[i]);
+          }
         }
         {
           const int gn = n0 + quad * 32 + lane;
-          float v[32];
+          float v[BK];
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
+          for (int k = 0; k < BK; ++k)
             v[k] = (gn < p.N && k0 + k < p.K)
                        ? __ldg(p.B + static_cast<long long>(k0 + k) * p.ldb + gn)
                        : 0.0f;
           const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol + stage * Cfg::kBtColsPerStage;
-          bt_to_tmem<EXACT>(col, col + kBK, v);
+          bt_to_tmem<BK, EXACT>(col, col + BK, v);
         }
         fence_proxy_async_smem();
         tmem_store_wait();
@@ -331,14 +367,15 @@ __global__ void __launch_bounds__(TcConfig<STAGES, EXACT, LSU>::kThreads, 1)
           const uint32_t a_hi = smem_addr(tiles + stage * Cfg::kStageBytes);
           const uint32_t bt_hi = tmem + kBtCol + stage * Cfg::kBtColsPerStage;
 #pragma unroll
-          for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+          for (int kk = 0; kk < BK / kUmmaK; ++kk) {
             // A tile, K-major: a k-step of 8 fp32 is 32 bytes along the swizzled row;
-            // 8-row groups are 1024 bytes apart.
-            const uint64_t da = smem_desc(a_hi + kk * 32, 16, 1024, kSw128);
+            // 8-row groups (the swizzle atom) are kAtomBytes apart.
+            const uint64_t da = smem_desc(a_hi + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
             const uint32_t accumulate = (kb | kk) != 0;
             if (EXACT) {
-              const uint64_t da_lo = smem_desc(a_hi + Cfg::kALoOffset + kk * 32, 16, 1024, kSw128);
-              mma_tf32_ts(d_tmem, bt_hi + kBK + kk * kUmmaK, da, Cfg::kIdesc, accumulate);
+              const uint64_t da_lo =
+                  smem_desc(a_hi + Cfg::kALoOffset + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
+              mma_tf32_ts(d_tmem, bt_hi + BK + kk * kUmmaK, da, Cfg::kIdesc, accumulate);
               mma_tf32_ts(d_tmem, bt_hi + kk * kUmmaK, da_lo, Cfg::kIdesc, 1);
               mma_tf32_ts(d_tmem, bt_hi + kk * kUmmaK, da, Cfg::kIdesc, 1);
             } else {
@@ -399,8 +436,11 @@ __global__ void __launch_bounds__(TcConfig<STAGES, EXACT, LSU>::kThreads, 1)
     }
   } else if (Cfg::kXformWarps > 0 && warp >= Cfg::kXformWarp0) {
     // -------------------------------------------- transform (TMA variant) --
+    // Warp (quad, part) moves k in [part * W, (part + 1) * W), W = BK / parts,
+    // of B^T rows n = 32 quad + lane into TMEM; all of them split the A tile.
     const uint32_t quad = warp & 3;
-    const int xt = threadIdx.x - Cfg::kXformWarp0 * 32;  // 0..127
+    const uint32_t part = (warp - Cfg::kXformWarp0) >> 2;
+    const int xt = threadIdx.x - Cfg::kXformWarp0 * 32;  // 0 .. 32 * kXformWarps - 1
     uint32_t stage = 0, phase = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
@@ -412,14 +452,17 @@ __global__ void __launch_bounds__(TcConfig<STAGES, EXACT, LSU>::kThreads, 1)
         tc_fence_after_sync();
         uint8_t *st = tiles + stage * Cfg::kStageBytes;
         {
-          // B tile is row-major 32 k x 128 n (512-byte rows); this thread's
+          // B tile is row-major BK k x 128 n (512-byte rows); this thread's
           // column n = 32 quad + lane becomes TMEM lane n.
-          const float *bs = reinterpret_cast<const float *>(st + Cfg::kBOffset) + quad * 32 + lane;
-          float v[32];
+          constexpr int kW = BK / Cfg::kXformParts;
+          const float *bs = reinterpret_cast<const float *>(st + Cfg::kBOffset) +
+                            part * kW * kTN + quad * 32 + lane;
+          float v[kW];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = bs[k * kTN];
-          const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol + stage * Cfg::kBtColsPerStage;
-          bt_to_tmem<EXACT>(col, col + kBK, v);
+          for (int k = 0; k < kW; ++k) v[k] = bs[k * kTN];
+          const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol +
+                               stage * Cfg::kBtColsPerStage + part * kW;
+          bt_to_tmem<kW, EXACT>(col, col + BK, v);
         }
         if (EXACT) {
           float4 *raw = reinterpret_cast<float4 *>(st);
@@ -551,10 +594,10 @@ bool get_map(const void *ptr, uint64_t d0, uint64_t d1, uint64_t pitch_bytes, ui
   return true;
 }
 
-template <int STAGES, bool EXACT, bool LSU>
+template <int BK, int STAGES, bool EXACT, bool LSU>
 int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
-  using Cfg = TcConfig<STAGES, EXACT, LSU>;
-  auto kernel = tc_gemm_kernel<STAGES, EXACT, LSU>;
+  using Cfg = TcConfig<BK, STAGES, EXACT, LSU>;
+  auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU>;
   const int smem_bytes = Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
 
   int dev = 0;
@@ -575,9 +618,9 @@ int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   std::memset(&map_a, 0, sizeof(map_a));
   std::memset(&map_b, 0, sizeof(map_b));
   if (!LSU) {
-    if (!get_map(a.A, a.K, a.M, a.lda * 4, kBK, kTM, CU_TENSOR_MAP_SWIZZLE_128B, &map_a))
-      return kErrLaunch;
-    if (!get_map(a.B, a.N, a.K, a.ldb * 4, kTN, kBK, CU_TENSOR_MAP_SWIZZLE_NONE, &map_b))
+    const CUtensorMapSwizzle sw_a = BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, kTM, sw_a, &map_a)) return kErrLaunch;
+    if (!get_map(a.B, a.N, a.K, a.ldb * 4, kTN, BK, CU_TENSOR_MAP_SWIZZLE_NONE, &map_b))
       return kErrLaunch;
   }
 
@@ -594,7 +637,7 @@ int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   p.num_m_blocks = static_cast<int>((a.M + kTM - 1) / kTM);
   p.num_n_blocks = static_cast<int>((a.N + kTN - 1) / kTN);
   p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-  p.num_k_blocks = static_cast<int>((a.K + kBK - 1) / kBK);
+  p.num_k_blocks = static_cast<int>((a.K + BK - 1) / BK);
   // Generous: a stage takes microseconds; one tile's mainloop about K * 25 ns.
   p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
 
@@ -618,12 +661,15 @@ bool tc_tma_legal(const GemmArgs &a) {
 }
 
 int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream) {
+  // Stage shapes (BK x stages, picked by timing at 4096^3): exact 16 x 5 with
+  // A 16 KiB + B 8 KiB + A_lo 16 KiB per stage; tf32 32 x 4 with A 32 KiB +
+  // B 16 KiB. The LSU variants stage no B tile in shared memory.
   if (exact) {
-    if (lsu) return launch_variant<2, true, true>(a, sm_count, stream);
-    return launch_variant<2, true, false>(a, sm_count, stream);
+    if (lsu) return launch_variant<16, 6, true, true>(a, sm_count, stream);
+    return launch_variant<16, 5, true, false>(a, sm_count, stream);
   }
-  if (lsu) return launch_variant<4, false, true>(a, sm_count, stream);
-  return launch_variant<4, false, false>(a, sm_count, stream);
+  if (lsu) return launch_variant<32, 6, false, true>(a, sm_count, stream);
+  return launch_variant<32, 4, false, false>(a, sm_count, stream);
 }
 
 int tc_poll_status(cudaStream_t stream) {
