@@ -192,6 +192,25 @@ def traffic_lookup(kernel: str, workload: str, mode: str):
     return None, sha
 
 
+# ------------------------------------------------------- rank reduction --
+
+def reduce_max(value: float, dist=None, device="cpu") -> float:
+    """Max of `value` over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gflops(max_total_ms: float, world: int, steps: int, flops_per_step: float) -> float:
+    """Aggregate throughput: every rank runs `steps` replicas of the workload;
+    the job takes as long as its slowest rank."""
+    return world * steps * flops_per_step / (max_total_ms / 1e3) / 1e9
+
+
 # -------------------------------------------------------------- CPU legs --
 
 def oracle_rows_gflops(a, b, budget_s: float, max_rows: int | None = None):
@@ -315,13 +334,9 @@ def main():
     if st != g.OK:
         raise g.GemmError(st, "device status")
 
-    total_ms = sum(times)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(sum(times), dist, "cuda")
     flops = 2.0 * M * N * K
-    value = world * args.steps * flops / (total_ms / 1e3) / 1e9
+    value = whole_job_gflops(total_ms, world, args.steps, flops)
     ms_per_step = total_ms / args.steps
 
     pk = peaks()
