@@ -78,7 +78,20 @@ struct TcParams {
   float *C;
   long long ldc;
   int num_m_blocks, num_n_blocks, num_tiles, num_k_blocks;
+  // Stream-K schedule (see UnitIter): tiles [0, dp_tiles) are whole-tile work
+  // dealt round-robin; the k-blocks of tiles [dp_tiles, num_tiles) are split
+  // into contiguous chunks of sk_share k-blocks over CTAs [0, sk_ctas).
+  int dp_tiles, sk_share, sk_ctas, sk_max_parts;
+  float *sk_partials;      // split tiles: one kTM x kTN fp32 partial per (tile, part)
+  unsigned *sk_counters;   // split tiles: parts finished so far (zeroed before launch)
   unsigned long long timeout_ns;
+};
+
+// One unit of work of a CTA: k-blocks [kb0, kb1) of output tile `tile`.
+// nparts > 1 marks a split tile: this CTA contributes part `part` of
+// `nparts`, and sk_tile indexes the tile's partial slots and counter.
+struct WorkUnit {
+  int tile, kb0, kb1, sk_tile, part, nparts;
 };
 
 // BK = K per stage: 32 (A rows of 128 bytes, 128-byte swizzle) or 16 (rows of
@@ -124,6 +137,7 @@ struct alignas(8) TcShared {
   uint64_t drain;          // every MMA of this CTA has completed
   uint32_t tmem_base;
   int abort;
+  int sk_last;             // epilogue: this CTA finished a split tile last
 };
 
 __device__ __forceinline__ void tile_coords(const TcParams &p, int t, int &mb, int &nb) {
@@ -134,6 +148,103 @@ __device__ __forceinline__ void tile_coords(const TcParams &p, int t, int &mb, i
   const int r = t - g * group_tiles;
   mb = first_m + r % gm;
   nb = r / gm;
+}
+
+// The work list of one CTA, identical for every role: first its stream-K
+// chunk (k-blocks [c * share, (c + 1) * share) of the split tiles, in order,
+// cut at tile boundaries), then the whole tiles c, c + grid, ... below
+// dp_tiles. Every CTA of the grid sees the same partition, so the number of
+// CTAs contributing to a split tile and each CTA's part index follow from the
+// chunk boundaries alone.
+struct UnitIter {
+  int sk_pos, sk_end, dp_next;
+  __device__ explicit UnitIter(const TcParams &p) {
+    const int c = blockIdx.x;
+    const int sk_total = (p.num_tiles - p.dp_tiles) * p.num_k_blocks;
+    if (c < p.sk_ctas && sk_total > 0) {
+      sk_pos = min(c * p.sk_share, sk_total);
+      sk_end = min(sk_pos + p.sk_share, sk_total);
+    } else {
+      sk_pos = sk_end = 0;
+    }
+    dp_next = c;
+  }
+  __device__ bool next(const TcParams &p, WorkUnit &u) {
+    if (sk_pos < sk_end) {
+      const int kbt = p.num_k_blocks;
+      const int s = sk_pos / kbt;
+      u.sk_tile = s;
+      u.tile = p.dp_tiles + s;
+      u.kb0 = sk_pos - s * kbt;
+      u.kb1 = min(kbt, u.kb0 + (sk_end - sk_pos));
+      const int first = (s * kbt) / p.sk_share;
+      const int last = ((s + 1) * kbt - 1) / p.sk_share;
+      u.nparts = last - first + 1;
+      u.part = static_cast<int>(blockIdx.x) - first;
+      sk_pos += u.kb1 - u.kb0;
+      return true;
+    }
+    if (dp_next < p.dp_tiles) {
+      u.tile = dp_next;
+      u.kb0 = 0;
+      u.kb1 = p.num_k_blocks;
+      u.sk_tile = -1;
+      u.part = 0;
+      u.nparts = 1;
+      dp_next += gridDim.x;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Sum the partial tiles of a split tile in part order and store the result
+// to C. Called by the 128 epilogue threads of the CTA that finished last. The
+// tile is read as float4s, eight per thread and part in flight at a time.
+__device__ __noinline__ void epilogue_fixup(const TcParams &p, const WorkUnit &u, int mb, int nb,
+                                            int tid) {
+  constexpr int kVec = kTM * kTN / 4;  // float4s per tile
+  constexpr int kRowVec = kTN / 4;     // float4s per tile row
+  constexpr int kBatch = 8;
+  const long long slot4 = static_cast<long long>(kTM) * kTN / 4;
+  const float4 *base = reinterpret_cast<const float4 *>(p.sk_partials) +
+                       static_cast<long long>(u.sk_tile) * p.sk_max_parts * slot4;
+  const bool vec_ok = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+#pragma unroll 1
+  for (int f0 = 0; f0 < kVec; f0 += 128 * kBatch) {
+    float4 acc[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) acc[j] = __ldcg(base + f0 + tid + 128 * j);
+#pragma unroll 1
+    for (int q = 1; q < u.nparts; ++q) {
+      float4 v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) v[j] = __ldcg(base + q * slot4 + f0 + tid + 128 * j);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        acc[j].x += v[j].x;
+        acc[j].y += v[j].y;
+        acc[j].z += v[j].z;
+        acc[j].w += v[j].w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int f = f0 + tid + 128 * j;
+      const int gm = mb * kTM + f / kRowVec;
+      const int gn = nb * kTN + (f % kRowVec) * 4;
+      if (gm >= p.M) continue;
+      float *dst = p.C + static_cast<long long>(gm) * p.ldc + gn;
+      if (vec_ok && gn + 3 < p.N) {
+        *reinterpret_cast<float4 *>(dst) = acc[j];
+      } else {
+        const float e[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (gn + i < p.N) dst[i] = e[i];
+      }
+    }
+  }
 }
 
 // Swizzled byte offset of a linear offset inside an A tile whose rows are
@@ -251,10 +362,12 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      UnitIter it(p);
+      WorkUnit u;
+      while (ok && it.next(p, u)) {
         int mb, nb;
-        tile_coords(p, t, mb, nb);
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        tile_coords(p, u.tile, mb, nb);
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait_bounded(&sh->empty[stage], phase ^ 1, p.timeout_ns, abort,
                                  &g_tc_status)) {
             ok = false;
@@ -284,12 +397,14 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
     // n = 32 w + lane (TMEM lanes of this warp's quadrant).
     uint32_t stage = 0, phase = 0;
     const uint32_t quad = warp & 3;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    UnitIter it(p);
+    WorkUnit u;
+    while (it.next(p, u)) {
       int mb, nb;
-      tile_coords(p, t, mb, nb);
+      tile_coords(p, u.tile, mb, nb);
       const int m0 = mb * kTM, n0 = nb * kTN;
       bool ok = true;
-      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+      for (int kb = u.kb0; kb < u.kb1; ++kb) {
         if (!warp_wait(&sh->empty[stage], phase ^ 1, p, abort)) {
           ok = false;
           break;
@@ -350,14 +465,16 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
       uint32_t stage = 0, phase = 0, acc_phase = 0;
       bool ok = true;
       const uint32_t d_tmem = tmem + kAccCol;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      UnitIter it(p);
+      WorkUnit u;
+      while (ok && it.next(p, u)) {
         if (!mbar_wait_bounded(&sh->acc_empty, acc_phase ^ 1, p.timeout_ns, abort,
                                &g_tc_status)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
           uint64_t *in_bar = LSU ? &sh->full[stage] : &sh->ready[stage];
           if (!mbar_wait_bounded(in_bar, phase, p.timeout_ns, abort, &g_tc_status)) {
             ok = false;
@@ -371,7 +488,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
             // A tile, K-major: a k-step of 8 fp32 is 32 bytes along the swizzled row;
             // 8-row groups (the swizzle atom) are kAtomBytes apart.
             const uint64_t da = smem_desc(a_hi + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
-            const uint32_t accumulate = (kb | kk) != 0;
+            const uint32_t accumulate = (kb != u.kb0 || kk != 0) ? 1u : 0u;
             if (EXACT) {
               const uint64_t da_lo =
                   smem_desc(a_hi + Cfg::kALoOffset + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
@@ -401,37 +518,76 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
     // --------------------------------------------------------- epilogue --
     const uint32_t quad = warp & 3;  // TMEM lanes (columns of C) this warp may read
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+    UnitIter it(p);
+    WorkUnit u;
+    while (it.next(p, u)) {
       int mb, nb;
-      tile_coords(p, t, mb, nb);
-      if (!warp_wait(&sh->acc_full, acc_phase, p, abort)) break;
+      tile_coords(p, u.tile, mb, nb);
+      // The four epilogue warps continue or give up together: the split-tile
+      // path below synchronises them with named barriers.
+      if (!named_barrier_and(1, 128, warp_wait(&sh->acc_full, acc_phase, p, abort))) break;
       tc_fence_after_sync();
-      const int gn = nb * kTN + quad * 32 + lane;
+      const int n_loc = quad * 32 + lane;
+      const int gn = nb * kTN + n_loc;
       const bool n_ok = gn < p.N;
       const uint32_t t_lane = tmem + ((quad * 32) << 16) + kAccCol;
+      if (u.nparts == 1) {
+        // Whole tile: straight to C.
 #pragma unroll 1
-      for (int c = 0; c < kTM / 32; ++c) {
-        const int gm0 = mb * kTM + c * 32;
-        if (gm0 >= p.M) break;
-        uint32_t r[32];
-        tmem_load_32cols(t_lane + c * 32, r);
-        tmem_load_wait();
-        float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
-        const int rows = min(32, p.M - gm0);
-        if (n_ok) {
-          if (rows == 32) {
+        for (int c = 0; c < kTM / 32; ++c) {
+          const int gm0 = mb * kTM + c * 32;
+          if (gm0 >= p.M) break;
+          uint32_t r[32];
+          tmem_load_32cols(t_lane + c * 32, r);
+          tmem_load_wait();
+          float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
+          const int rows = min(32, p.M - gm0);
+          if (n_ok) {
+            if (rows == 32) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
-          } else {
+              for (int j = 0; j < 32; ++j)
+                dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < rows) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+              for (int j = 0; j < 32; ++j)
+                if (j < rows) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+            }
           }
         }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->acc_empty);
+      } else {
+        // Split tile: write this part's partial sums ([m][n], pitch kTN) to
+        // its slot and free the accumulator; the last part to finish sums all
+        // parts in part order (a fixed order, so results are deterministic)
+        // and writes C.
+        const long long slot_elems = static_cast<long long>(kTM) * kTN;
+        float *slot = p.sk_partials +
+                      (static_cast<long long>(u.sk_tile) * p.sk_max_parts + u.part) * slot_elems;
+#pragma unroll 1
+        for (int c = 0; c < kTM / 32; ++c) {
+          uint32_t r[32];
+          tmem_load_32cols(t_lane + c * 32, r);
+          tmem_load_wait();
+          float *dst = slot + (c * 32) * kTN + n_loc;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dst[j * kTN] = __uint_as_float(r[j]);
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->acc_empty);
+        __threadfence();
+        named_barrier_sync(1, 128);
+        if (warp == Cfg::kEpiWarp0 && lane == 0)
+          sh->sk_last = atomicAdd(&p.sk_counters[u.sk_tile], 1u) == static_cast<unsigned>(u.nparts - 1);
+        named_barrier_sync(1, 128);
+        if (sh->sk_last) {
+          __threadfence();
+          epilogue_fixup(p, u, mb, nb, threadIdx.x - Cfg::kEpiWarp0 * 32);
+        }
+        named_barrier_sync(1, 128);  // sk_last is reused by the next split tile
       }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->acc_empty);
       acc_phase ^= 1;
     }
   } else if (Cfg::kXformWarps > 0 && warp >= Cfg::kXformWarp0) {
@@ -443,8 +599,10 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
     const int xt = threadIdx.x - Cfg::kXformWarp0 * 32;  // 0 .. 32 * kXformWarps - 1
     uint32_t stage = 0, phase = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-      for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+    UnitIter it(p);
+    WorkUnit u;
+    while (ok && it.next(p, u)) {
+      for (int kb = u.kb0; kb < u.kb1; ++kb) {
         if (!warp_wait(&sh->full[stage], phase, p, abort)) {
           ok = false;
           break;
@@ -594,6 +752,57 @@ bool get_map(const void *ptr, uint64_t d0, uint64_t d1, uint64_t pitch_bytes, ui
   return true;
 }
 
+// Smallest stream-K chunk, in k: shorter chunks spend more time filling the
+// pipeline and more bytes on partial tiles than they save.
+constexpr int kMinChunkK = 256;
+// Most CTAs sharing one split tile: the last of them sums every part alone.
+constexpr int kMaxSplit = 8;
+
+struct Schedule {
+  int grid, dp_tiles, sk_share, sk_ctas, sk_max_parts;
+};
+
+// Data-parallel waves plus a stream-K tail. With T tiles of KB k-blocks on
+// G SMs and T mod G != 0, all but the last full wave are dealt whole; the
+// k-blocks of the remaining G + T mod G tiles are cut into equal contiguous
+// chunks over the G CTAs. Each chunk is then at least one tile long, so a
+// split tile has at most two parts, and every SM ends up with about
+// T * KB / G k-blocks. With fewer tiles than SMs everything is stream-K,
+// with chunks of at least min_chunk k-blocks and at most kMaxSplit parts per
+// tile.
+Schedule make_schedule(int tiles, int kb, int sms, int min_chunk) {
+  Schedule s;
+  min_chunk = min_chunk < 1 ? 1 : min_chunk;
+  s.dp_tiles = (tiles >= sms && tiles % sms != 0) ? (tiles / sms - 1) * sms
+               : (tiles >= sms ? tiles : 0);
+  const int split = tiles - s.dp_tiles;
+  if (split == 0) {
+    s.grid = sms < tiles ? sms : tiles;
+    s.sk_share = 1;
+    s.sk_ctas = 0;
+    s.sk_max_parts = 1;
+    return s;
+  }
+  const long long total = static_cast<long long>(split) * kb;
+  long long ctas;
+  if (split >= sms) {
+    ctas = sms;  // one chunk per SM, each at least a tile long
+  } else {
+    ctas = total / min_chunk;
+    if (ctas > sms) ctas = sms;
+    if (ctas > static_cast<long long>(split) * kMaxSplit)
+      ctas = static_cast<long long>(split) * kMaxSplit;
+    if (ctas < split) ctas = split;  // at least one CTA per tile
+    if (ctas > total) ctas = total;
+  }
+  s.sk_share = static_cast<int>((total + ctas - 1) / ctas);
+  s.sk_ctas = static_cast<int>((total + s.sk_share - 1) / s.sk_share);
+  // Chunks that are whole multiples of a tile never split one.
+  s.sk_max_parts = s.sk_share % kb == 0 ? 1 : (kb + s.sk_share - 1) / s.sk_share + 1;
+  s.grid = split >= sms ? sms : s.sk_ctas;
+  return s;
+}
+
 template <int BK, int STAGES, bool EXACT, bool LSU>
 int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   using Cfg = TcConfig<BK, STAGES, EXACT, LSU>;
@@ -641,7 +850,32 @@ int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   // Generous: a stage takes microseconds; one tile's mainloop about K * 25 ns.
   p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
 
-  const int grid = p.num_tiles < sm_count ? p.num_tiles : sm_count;
+  const Schedule sch = make_schedule(p.num_tiles, p.num_k_blocks, sm_count, kMinChunkK / BK);
+  p.dp_tiles = sch.dp_tiles;
+  p.sk_share = sch.sk_share;
+  p.sk_ctas = sch.sk_ctas;
+  p.sk_max_parts = sch.sk_max_parts;
+  p.sk_partials = nullptr;
+  p.sk_counters = nullptr;
+  const int grid = sch.grid;
+
+  // Split tiles need a workspace: partial tiles and one counter per split
+  // tile. It comes from the device's stream-ordered pool on the caller's
+  // stream and goes back right after the kernel, so concurrent calls on other
+  // streams never share it.
+  void *ws = nullptr;
+  const int split_tiles = p.num_tiles - p.dp_tiles;
+  if (split_tiles > 0 && sch.sk_max_parts > 1) {
+    const size_t counter_bytes = (static_cast<size_t>(split_tiles) * 4 + 255) / 256 * 256;
+    const size_t partial_bytes = static_cast<size_t>(split_tiles) * sch.sk_max_parts * kTM * kTN * 4;
+    if (cudaMallocAsync(&ws, counter_bytes + partial_bytes, stream) != cudaSuccess) return kErrLaunch;
+    if (cudaMemsetAsync(ws, 0, counter_bytes, stream) != cudaSuccess) {
+      cudaFreeAsync(ws, stream);
+      return kErrLaunch;
+    }
+    p.sk_counters = static_cast<unsigned *>(ws);
+    p.sk_partials = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + counter_bytes);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
@@ -649,8 +883,9 @@ int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  if (cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p) != cudaSuccess) return kErrLaunch;
-  return kOk;
+  const bool launched = cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p) == cudaSuccess;
+  if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess) return kErrLaunch;
+  return launched ? kOk : kErrLaunch;
 }
 
 }  // namespace

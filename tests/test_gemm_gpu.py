@@ -148,6 +148,31 @@ def test_ragged_sweep(g):
             check_within_bound(c, r64, rs, k, mode, f"rand {mode}/{kernel} {m}x{n}x{k}")
 
 
+@pytest.mark.parametrize("mode,kernel", [("exact", "tc_tma"), ("tf32", "tc_tma"), ("exact", "tc_lsu"),
+                                         ("tf32", "tc_lsu")])
+@pytest.mark.parametrize("m,n,k", [
+    (256, 128, 4096),     # one tile, k split over the most CTAs
+    (200, 100, 2000),     # one ragged tile, split
+    (3328, 1536, 512),    # 156 tiles: one full wave plus 4 split tiles
+    (512, 512, 512),      # 8 tiles, each split
+])
+def test_stream_k_splits(g, mode, kernel, m, n, k):
+    # tiles whose k range is shared by several CTAs: partial sums through the
+    # workspace, summed by the last contributor in part order
+    a, b = operands(m, n, k, "normal", seed=m + 3 * n + k)
+    c, _ = run(g, a, b, mode, kernel)
+    rows = np.unique(np.concatenate([np.arange(0, m, max(1, m // 97)), [m - 1]]))
+    c64, s = oracle.gemm_rows(a, b, rows)
+    check_within_bound(c[rows], c64, s, k, mode, f"stream-K {mode}/{kernel} {m}x{n}x{k}")
+    ai = synth.small_integers((m, k), 7)
+    bi = synth.small_integers((k, n), 8)
+    ci, _ = run(g, ai, bi, mode, kernel)
+    ci64, _ = oracle.gemm_rows(ai, bi, rows)
+    assert np.array_equal(ci[rows].astype(np.float64), ci64)
+    c2, _ = run(g, a, b, mode, kernel)
+    assert np.array_equal(c.view(np.uint32), c2.view(np.uint32)), "split tiles not deterministic"
+
+
 def test_nan_prefilled_output_fully_written(g):
     for mode, kernel in VARIANTS:
         a, b = operands(385, 519, 96, "uniform", seed=9)
