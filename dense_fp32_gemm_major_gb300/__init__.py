@@ -27,6 +27,8 @@ EXACT, TF32, EXACT_SIMT = 0, 1, 2
 MODES = {"exact": EXACT, "tf32": TF32, "exact_simt": EXACT_SIMT}
 # gemm_f32_status
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_ALIAS = range(6)
+# fixed scratch of gemm_f32_noalloc
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 # gemm_f32_kernel
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC_TMA, KERNEL_TC_LSU = range(4)
 KERNELS = {"auto": KERNEL_AUTO, "simt": KERNEL_SIMT, "tc_tma": KERNEL_TC_TMA, "tc_lsu": KERNEL_TC_LSU}
@@ -60,6 +62,8 @@ def _load():
     lib.gemm_f32_select.restype = i32
     lib.gemm_f32_host.argtypes = sig + [i32]
     lib.gemm_f32_host.restype = i32
+    lib.gemm_f32_noalloc.argtypes = sig + [i32, p]
+    lib.gemm_f32_noalloc.restype = i32
     lib.gemm_f32_status_string.argtypes = [i32]
     lib.gemm_f32_status_string.restype = ctypes.c_char_p
     lib.gemm_f32_poll_device_status.argtypes = [p]
@@ -105,6 +109,12 @@ def gemm_f32_select(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel=KERNEL_AUTO) -
 
 def gemm_f32_host(M, N, K, A, lda, B, ldb, C, ldc, mode) -> int:
     return _load().gemm_f32_host(M, N, K, A, lda, B, ldb, C, ldc, mode)
+
+
+def gemm_f32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, mode, stream=0) -> int:
+    """gemm_f32 that allocates no device memory (workspace in a fixed
+    NOALLOC_SCRATCH_BYTES array; see include/gemm_f32.h)."""
+    return _load().gemm_f32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, mode, stream or None)
 
 
 def gemm_f32_status_string(status: int) -> str:

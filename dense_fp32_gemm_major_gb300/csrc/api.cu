@@ -233,6 +233,28 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
   return gemm::tc_poll_status(hs.stream);
 }
 
+int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                     const float *B, int64_t ldb, float *C, int64_t ldc, int mode, void *stream) {
+  const GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
+  bool noop = false;
+  int st = validate(a, mode, &noop);
+  if (st != gemm::kOk || noop) return st;
+  const int k = select_kernel(a, mode, GEMM_KERNEL_AUTO);
+  if (k < 0) return -k;
+  int dev = 0, sms = 0;
+  st = current_device(&dev, &sms);
+  if (st != gemm::kOk) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a.K == 0) {
+    if (cudaMemset2DAsync(a.C, static_cast<size_t>(a.ldc) * 4, 0, static_cast<size_t>(a.N) * 4,
+                          static_cast<size_t>(a.M), s) != cudaSuccess)
+      return gemm::kErrLaunch;
+    return gemm::kOk;
+  }
+  if (k == GEMM_KERNEL_SIMT) return gemm::simt_launch(a, s);  // needs no scratch
+  return gemm::tc_launch_noalloc(a, mode == GEMM_F32_EXACT, k == GEMM_KERNEL_TC_LSU, sms, s);
+}
+
 const char *gemm_f32_status_string(int status) {
   switch (status) {
     case GEMM_OK:

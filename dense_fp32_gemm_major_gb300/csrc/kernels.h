@@ -35,6 +35,11 @@ bool tc_tma_legal(const GemmArgs &a);
 // by plain loads instead of TMA. Requires K >= 1, M >= 1, N >= 1.
 int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream);
 
+// tc_launch with the stream-K workspace in the library's fixed scratch array
+// (no allocation). Returns kErrInvalidArg if the problem needs more scratch
+// than GEMM_F32_NOALLOC_SCRATCH_BYTES.
+int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream);
+
 // SIMT FP32 GEMM. Requires K >= 1, M >= 1, N >= 1.
 int simt_launch(const GemmArgs &a, cudaStream_t stream);
 

@@ -52,6 +52,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "../../include/gemm_f32.h"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -920,6 +921,141 @@ int tc_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream) {
   selftest_wait_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(timeout_ns));
   if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
   return tc_poll_status(stream);
+}
+
+}  // namespace gemm
+
+// ------------------------------------------------- allocation-free variant --
+//
+// gemm_f32_noalloc runs the same tensor-core kernel as gemm_f32 but takes the
+// stream-K workspace (split-tile partials and counters) from the fixed array
+// below instead of the device's memory pool, for callers that must not
+// allocate device memory while they run. The array is part of the library's
+// device image: every GPU that loads the library keeps these bytes until the
+// process exits, and all calls share them.
+
+static __device__ __align__(256) unsigned char g_gemm_noalloc_scratch[GEMM_F32_NOALLOC_SCRATCH_BYTES];
+
+namespace gemm {
+namespace {
+
+// Device address of the scratch array on each device. The host-side name of
+// a __device__ array is only a stand-in for it, so the address is looked up
+// once per device, with that device current.
+struct NoAllocScratch {
+  bool ready = false;
+  void *ptr = nullptr;
+};
+NoAllocScratch g_noalloc[64];
+std::mutex g_noalloc_mu;
+
+int noalloc_scratch(int dev, void **out) {
+  if (dev < 0 || dev >= 64) return kErrLaunch;
+  std::lock_guard<std::mutex> g(g_noalloc_mu);
+  NoAllocScratch &d = g_noalloc[dev];
+  if (!d.ready) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_gemm_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return kErrLaunch;
+    d.ptr = ptr;
+    d.ready = true;
+  }
+  *out = d.ptr;
+  return kOk;
+}
+
+template <int BK, int STAGES, bool EXACT, bool LSU>
+int launch_variant_noalloc(const GemmArgs &a, int sm_count, cudaStream_t stream) {
+  using Cfg = TcConfig<BK, STAGES, EXACT, LSU>;
+  auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU>;
+  const int smem_bytes = Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kErrLaunch;
+  void *scratch = nullptr;
+  const int st = noalloc_scratch(dev, &scratch);
+  if (st != kOk) return st;
+
+  TcParams p;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.A = a.A;
+  p.lda = a.lda;
+  p.B = a.B;
+  p.ldb = a.ldb;
+  p.C = a.C;
+  p.ldc = a.ldc;
+  p.num_m_blocks = static_cast<int>((a.M + kTM - 1) / kTM);
+  p.num_n_blocks = static_cast<int>((a.N + kTN - 1) / kTN);
+  p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+  p.num_k_blocks = static_cast<int>((a.K + BK - 1) / BK);
+  p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
+  const Schedule sch = make_schedule(p.num_tiles, p.num_k_blocks, sm_count, kMinChunkK / BK);
+  p.dp_tiles = sch.dp_tiles;
+  p.sk_share = sch.sk_share;
+  p.sk_ctas = sch.sk_ctas;
+  p.sk_max_parts = sch.sk_max_parts;
+  p.sk_partials = nullptr;
+  p.sk_counters = nullptr;
+
+  // The same workspace layout gemm_f32 takes from the pool, here inside the
+  // fixed array; problems that need more are refused before anything runs.
+  const int split_tiles = p.num_tiles - p.dp_tiles;
+  size_t counter_bytes = 0;
+  if (split_tiles > 0 && sch.sk_max_parts > 1) {
+    counter_bytes = (static_cast<size_t>(split_tiles) * 4 + 255) / 256 * 256;
+    const size_t partial_bytes =
+        static_cast<size_t>(split_tiles) * sch.sk_max_parts * kTM * kTN * 4;
+    if (counter_bytes + partial_bytes > GEMM_F32_NOALLOC_SCRATCH_BYTES) return kErrInvalidArg;
+    p.sk_counters = static_cast<unsigned *>(scratch);
+    p.sk_partials = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + counter_bytes);
+  }
+
+  static bool attr_set[64] = {};
+  static std::mutex attr_mu;
+  {
+    std::lock_guard<std::mutex> g(attr_mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+          cudaSuccess)
+        return kErrLaunch;
+      attr_set[dev] = true;
+    }
+  }
+  CUtensorMap map_a, map_b;
+  std::memset(&map_a, 0, sizeof(map_a));
+  std::memset(&map_b, 0, sizeof(map_b));
+  if (!LSU) {
+    const CUtensorMapSwizzle sw_a = BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, kTM, sw_a, &map_a)) return kErrLaunch;
+    if (!get_map(a.B, a.N, a.K, a.ldb * 4, kTN, BK, CU_TENSOR_MAP_SWIZZLE_NONE, &map_b))
+      return kErrLaunch;
+  }
+  // The counters must start at zero; the previous call left them counted up.
+  if (counter_bytes > 0 && cudaMemsetAsync(scratch, 0, counter_bytes, stream) != cudaSuccess)
+    return kErrLaunch;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sch.grid, 1, 1);
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p) == cudaSuccess ? kOk : kErrLaunch;
+}
+
+}  // namespace
+
+int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream) {
+  // Same kernels and stage shapes as tc_launch.
+  if (exact) {
+    if (lsu) return launch_variant_noalloc<16, 6, true, true>(a, sm_count, stream);
+    return launch_variant_noalloc<16, 5, true, false>(a, sm_count, stream);
+  }
+  if (lsu) return launch_variant_noalloc<32, 6, false, true>(a, sm_count, stream);
+  return launch_variant_noalloc<32, 4, false, false>(a, sm_count, stream);
 }
 
 }  // namespace gemm

@@ -139,6 +139,45 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K,
                   float *C, int64_t ldc,
                   int mode);
 
+/* Bytes of the fixed device array that gemm_f32_noalloc works in (64 MiB). */
+#define GEMM_F32_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * gemm_f32_noalloc -- gemm_f32 without any device memory allocation. (The
+ * pages have no counterpart: their kernels need no scratch memory.)
+ *
+ * For callers that must not allocate device memory while they run: programs
+ * that hand nearly all device memory to their own allocator at start-up (so
+ * a pool allocation on the caller's stream could fail), and latency- or
+ * budget-critical loops that must keep the process's device footprint and
+ * allocator state fixed once set up. gemm_f32 takes its stream-K workspace
+ * (partial sums of output tiles whose k range is shared between SMs) from
+ * the device's stream-ordered memory pool; this entry point runs the same
+ * kernels and schedule but keeps that workspace in a fixed array of
+ * GEMM_F32_NOALLOC_SCRATCH_BYTES that is part of the library's device image:
+ * every GPU that loads the library holds it until the process exits.
+ *
+ * Arguments, modes, layout and errors are those of gemm_f32 (device
+ * pointers owned by the caller, stream ordered, non-blocking), and results
+ * are the same. In addition it returns GEMM_ERR_INVALID_ARG, before
+ * enqueuing anything, for a problem whose workspace would not fit in the
+ * array: that happens only when the stream-K part of the schedule spans more
+ * than about 250 output tiles of 256 x 128 (it never spans more than 303 on
+ * a 152-SM GB300); a 4096^3 product uses about 52 MiB of the array.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device uses the same array and leaves its contents behind;
+ * the call itself clears what must start at zero. Calls whose work overlaps
+ * on the GPU (different streams, or different host threads) race on the
+ * array and give wrong results: serialise them.
+ */
+int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
+                     const float *A, int64_t lda,
+                     const float *B, int64_t ldb,
+                     float *C, int64_t ldc,
+                     int mode, void *stream);
+
 /* gemm_f32_status_string -- static, NUL-terminated name of a status code. */
 const char *gemm_f32_status_string(int status);
 
