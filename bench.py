@@ -30,7 +30,15 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GFLOP/s (2MNK/t) for fp32 GEMM at 4096³; % of TF32/FP32 roofline"
-WORKLOAD = "square fp32 GEMM M=N=K=4096, row-major, A,B uniform[-1,1) from seed (headline size)"
+WORKLOADS = {
+    "c1": "square fp32 GEMM M=N=K=512, row-major, A and B i.i.d. uniform[-1,1) from seed, C overwritten",
+    "c2": "square fp32 GEMM M=N=K=1024, row-major, A,B uniform[-1,1) from seed",
+    "c3": "square fp32 GEMM M=N=K=2048, row-major, A,B uniform[-1,1) from seed",
+    "c4": "square fp32 GEMM M=N=K=4096, row-major, A,B uniform[-1,1) from seed (headline size)",
+    "c5a": "ragged fp32 GEMM M=1000, K=777, N=1531, row-major, A,B normal(0,1) from seed",
+    "c5b": "transformer-projection fp32 GEMM M=8192, K=4096, N=11008, row-major, A,B normal(0,1) from seed",
+}
+WORKLOAD = WORKLOADS["c4"]
 M = N = K = 4096
 FLUSH_BYTES = 256 << 20
 TF32_PER_BF16 = 1.1 / 2.25          # nominal dense TF32 : BF16 tensor rate
@@ -47,6 +55,8 @@ def parse_args():
     ap.add_argument("--mode", default="exact", choices=["exact", "tf32", "exact_simt"],
                     help="accuracy mode of the timed steps (the headline is exact)")
     ap.add_argument("--no-extras", action="store_true", help="skip the other modes, e2e and CPU legs")
+    ap.add_argument("--config", default="c4", choices=sorted(WORKLOADS),
+                    help="workload (the benchmark is c4; the others are for the record)")
     return ap.parse_args()
 
 
@@ -272,6 +282,7 @@ def run_reference(args, rank):
 # ------------------------------------------------------------------ main --
 
 def main():
+    global M, N, K, WORKLOAD
     args = parse_args()
     rank, world, local = dist_env()
     if args.impl == "reference":
@@ -294,7 +305,9 @@ def main():
         if dist is not None:
             dist.barrier(device_ids=[local])
 
-    a, b, cfg = synth.config_operands("c4")
+    a, b, cfg = synth.config_operands(args.config)
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    WORKLOAD = WORKLOADS[args.config]
     dA = torch.from_numpy(a).cuda()
     dB = torch.from_numpy(b).cuda()
     dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
@@ -342,7 +355,7 @@ def main():
     pk = peaks()
     tf32_peak = pk["bf16"] * TF32_PER_BF16
     alu_peak = SMS * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
-    traffic, sha = traffic_lookup(kernel_name, "c4", args.mode)
+    traffic, sha = traffic_lookup(kernel_name, args.config, args.mode)
     if args.mode == "exact_simt":
         achieved = flops / (ms_per_step / 1e3) / 1e12
         roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(alu_peak, 1),
@@ -396,7 +409,7 @@ def main():
         # the oracle on the host cores, a bounded sample of the same workload
         gf, threads, rows, secs = oracle_rows_gflops(a, b, budget_s=12.0)
         cpu = {"value": round(gf, 3), "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{rows} whole rows of the 4096^3 product ({rows}x4096x4096 "
+               "sample": f"{rows} whole rows of the {M}x{N}x{K} product ({rows}x{N}x{K} "
                          f"multiply-adds in fp64), {secs:.1f} s"}
 
     if rank == 0:

@@ -139,6 +139,7 @@ struct alignas(8) TcShared {
   uint32_t tmem_base;
   int abort;
   int sk_last;             // epilogue: this CTA finished a split tile last
+  int fix_tile, fix_nparts, fix_mb, fix_nb;  // final split tile left for all warps to sum
 };
 
 __device__ __forceinline__ void tile_coords(const TcParams &p, int t, int &mb, int &nb) {
@@ -151,12 +152,13 @@ __device__ __forceinline__ void tile_coords(const TcParams &p, int t, int &mb, i
   nb = r / gm;
 }
 
-// The work list of one CTA, identical for every role: first its stream-K
-// chunk (k-blocks [c * share, (c + 1) * share) of the split tiles, in order,
-// cut at tile boundaries), then the whole tiles c, c + grid, ... below
-// dp_tiles. Every CTA of the grid sees the same partition, so the number of
-// CTAs contributing to a split tile and each CTA's part index follow from the
-// chunk boundaries alone.
+// The work list of one CTA, identical for every role: first the whole tiles
+// c, c + grid, ... below dp_tiles (raster order, so concurrent CTAs share
+// operand tiles in L2), then its stream-K chunk (k-blocks
+// [c * share, (c + 1) * share) of the remaining tiles, in order, cut at tile
+// boundaries). Every CTA of the grid sees the same partition, so the number
+// of CTAs contributing to a split tile and each CTA's part index follow from
+// the chunk boundaries alone.
 struct UnitIter {
   int sk_pos, sk_end, dp_next;
   __device__ explicit UnitIter(const TcParams &p) {
@@ -171,6 +173,16 @@ struct UnitIter {
     dp_next = c;
   }
   __device__ bool next(const TcParams &p, WorkUnit &u) {
+    if (dp_next < p.dp_tiles) {
+      u.tile = dp_next;
+      u.kb0 = 0;
+      u.kb1 = p.num_k_blocks;
+      u.sk_tile = -1;
+      u.part = 0;
+      u.nparts = 1;
+      dp_next += gridDim.x;
+      return true;
+    }
     if (sk_pos < sk_end) {
       const int kbt = p.num_k_blocks;
       const int s = sk_pos / kbt;
@@ -185,42 +197,43 @@ struct UnitIter {
       sk_pos += u.kb1 - u.kb0;
       return true;
     }
-    if (dp_next < p.dp_tiles) {
-      u.tile = dp_next;
-      u.kb0 = 0;
-      u.kb1 = p.num_k_blocks;
-      u.sk_tile = -1;
-      u.part = 0;
-      u.nparts = 1;
-      dp_next += gridDim.x;
-      return true;
-    }
     return false;
+  }
+  // True when no unit follows the one last returned by next().
+  __device__ bool done(const TcParams &p) const {
+    return dp_next >= p.dp_tiles && sk_pos >= sk_end;
   }
 };
 
-// Sum the partial tiles of a split tile in part order and store the result
-// to C. Called by the 128 epilogue threads of the CTA that finished last. The
-// tile is read as float4s, eight per thread and part in flight at a time.
-__device__ __noinline__ void epilogue_fixup(const TcParams &p, const WorkUnit &u, int mb, int nb,
-                                            int tid) {
+// Sum the partial tiles of split tile `sk_tile` in part order and store the
+// result to C. Run by `nthreads` threads of the CTA that finished last: the
+// four epilogue warps, or every warp of the CTA for its final unit. The tile
+// is read as float4s, eight per thread and part in flight at a time.
+__device__ __noinline__ void epilogue_fixup(const TcParams &p, int sk_tile, int nparts, int mb,
+                                            int nb, int tid, int nthreads) {
   constexpr int kVec = kTM * kTN / 4;  // float4s per tile
   constexpr int kRowVec = kTN / 4;     // float4s per tile row
   constexpr int kBatch = 8;
   const long long slot4 = static_cast<long long>(kTM) * kTN / 4;
   const float4 *base = reinterpret_cast<const float4 *>(p.sk_partials) +
-                       static_cast<long long>(u.sk_tile) * p.sk_max_parts * slot4;
+                       static_cast<long long>(sk_tile) * p.sk_max_parts * slot4;
   const bool vec_ok = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
 #pragma unroll 1
-  for (int f0 = 0; f0 < kVec; f0 += 128 * kBatch) {
+  for (int f0 = 0; f0 < kVec; f0 += nthreads * kBatch) {
     float4 acc[kBatch];
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) acc[j] = __ldcg(base + f0 + tid + 128 * j);
+    for (int j = 0; j < kBatch; ++j) {
+      const int f = f0 + tid + nthreads * j;
+      acc[j] = f < kVec ? __ldcg(base + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 #pragma unroll 1
-    for (int q = 1; q < u.nparts; ++q) {
+    for (int q = 1; q < nparts; ++q) {
       float4 v[kBatch];
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) v[j] = __ldcg(base + q * slot4 + f0 + tid + 128 * j);
+      for (int j = 0; j < kBatch; ++j) {
+        const int f = f0 + tid + nthreads * j;
+        v[j] = f < kVec ? __ldcg(base + q * slot4 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         acc[j].x += v[j].x;
@@ -231,7 +244,8 @@ __device__ __noinline__ void epilogue_fixup(const TcParams &p, const WorkUnit &u
     }
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
-      const int f = f0 + tid + 128 * j;
+      const int f = f0 + tid + nthreads * j;
+      if (f >= kVec) continue;
       const int gm = mb * kTM + f / kRowVec;
       const int gn = nb * kTN + (f % kRowVec) * 4;
       if (gm >= p.M) continue;
@@ -343,6 +357,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
     mbar_init(&sh->acc_empty, 4);
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
+    sh->fix_tile = -1;
     fence_barrier_init();
   }
   if (!LSU && warp == 0 && lane == 0) {
@@ -584,8 +599,18 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
           sh->sk_last = atomicAdd(&p.sk_counters[u.sk_tile], 1u) == static_cast<unsigned>(u.nparts - 1);
         named_barrier_sync(1, 128);
         if (sh->sk_last) {
-          __threadfence();
-          epilogue_fixup(p, u, mb, nb, threadIdx.x - Cfg::kEpiWarp0 * 32);
+          if (it.done(p)) {
+            // The CTA's final unit: every warp sums it after the role loops.
+            if (warp == Cfg::kEpiWarp0 && lane == 0) {
+              sh->fix_tile = u.sk_tile;
+              sh->fix_nparts = u.nparts;
+              sh->fix_mb = mb;
+              sh->fix_nb = nb;
+            }
+          } else {
+            __threadfence();
+            epilogue_fixup(p, u.sk_tile, u.nparts, mb, nb, threadIdx.x - Cfg::kEpiWarp0 * 32, 128);
+          }
         }
         named_barrier_sync(1, 128);  // sk_last is reused by the next split tile
       }
@@ -660,6 +685,11 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
   if (warp == Cfg::kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if (sh->fix_tile >= 0 && !sh->abort) {
+    __threadfence();
+    epilogue_fixup(p, sh->fix_tile, sh->fix_nparts, sh->fix_mb, sh->fix_nb, threadIdx.x,
+                   blockDim.x);
   }
 }
 
