@@ -28,7 +28,7 @@ MODES = {"exact": EXACT, "tf32": TF32, "exact_simt": EXACT_SIMT}
 # gemm_f32_status
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_ALIAS = range(6)
 # fixed scratch of gemm_f32_noalloc
-NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+NOALLOC_SCRATCH_BYTES = 40 * 1024 * 1024
 # gemm_f32_kernel
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC_TMA, KERNEL_TC_LSU = range(4)
 KERNELS = {"auto": KERNEL_AUTO, "simt": KERNEL_SIMT, "tc_tma": KERNEL_TC_TMA, "tc_lsu": KERNEL_TC_LSU}

@@ -78,30 +78,53 @@ struct TcParams {
   long long ldb;
   float *C;
   long long ldc;
-  int num_m_blocks, num_n_blocks, num_tiles, num_k_blocks;
-  // Stream-K schedule (see UnitIter): tiles [0, dp_tiles) are whole-tile work
-  // dealt round-robin; the k-blocks of tiles [dp_tiles, num_tiles) are split
-  // into contiguous chunks of sk_share k-blocks over CTAs [0, sk_ctas).
-  int dp_tiles, sk_share, sk_ctas, sk_max_parts;
-  float *sk_partials;      // split tiles: one kTM x kTN fp32 partial per (tile, part)
-  unsigned *sk_counters;   // split tiles: parts finished so far (zeroed before launch)
+  int num_m_blocks, num_n_blocks, num_k_blocks;
+  // Scheduling is in units of cl CTAs (a cluster) and of "unit tiles" of
+  // kTM x (cl * kTN): the cl CTAs of a cluster compute the cl adjacent output
+  // tiles of one unit tile and share its A tile.
+  int cl, num_nu_blocks, num_tiles;
+  // Stream-K schedule (see UnitIter): unit tiles [0, dp_tiles) are whole-tile
+  // work dealt round-robin; the k-blocks of unit tiles [dp_tiles, num_tiles)
+  // are split into contiguous chunks of sk_share k-blocks over clusters
+  // [0, sk_ctas).
+  int dp_tiles, sk_share, sk_ctas;
+  // Partial sums of split tiles: two kTM x kTN fp32 slots per (cluster, rank)
+  // -- one for the first and one for the last unit of the cluster's chunk,
+  // the only units that can be parts of a split tile.
+  float *sk_partials;
+  unsigned *sk_counters;   // split tiles: parts finished so far per (tile, rank), zeroed before launch
   unsigned long long timeout_ns;
 };
 
-// One unit of work of a CTA: k-blocks [kb0, kb1) of output tile `tile`.
+// One unit of work of a CTA: k-blocks [kb0, kb1) of unit tile `tile`.
 // nparts > 1 marks a split tile: this CTA contributes part `part` of
-// `nparts`, and sk_tile indexes the tile's partial slots and counter.
+// `nparts`, sk_tile indexes the tile's counters and slot is this part's
+// partial-sum slot pair index (see TcParams::sk_partials).
 struct WorkUnit {
-  int tile, kb0, kb1, sk_tile, part, nparts;
+  int tile, kb0, kb1, sk_tile, part, nparts, slot;
 };
+
+// Slot index of part `part` of split unit tile `s` (2 * cluster + 0 for the
+// first unit of that cluster's chunk, + 1 for its last).
+__device__ __forceinline__ int split_slot(const TcParams &p, int s, int part) {
+  const int first = (s * p.num_k_blocks) / p.sk_share;
+  const int c = first + part;
+  if (part > 0) return 2 * c;  // later parts start their cluster's chunk
+  // The first part is its cluster's first unit if that chunk starts inside
+  // this tile, otherwise its last unit.
+  return (c * p.sk_share >= s * p.num_k_blocks) ? 2 * c : 2 * c + 1;
+}
 
 // BK = K per stage: 32 (A rows of 128 bytes, 128-byte swizzle) or 16 (rows of
 // 64 bytes, 64-byte swizzle). Either way a row of the A tile is one swizzle
 // span, 8-row groups are the swizzle atom, and a k-step of 8 advances the
 // descriptor by 32 bytes along the row.
-template <int BK, int STAGES, bool EXACT, bool LSU>
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL>
 struct TcConfig {
   static_assert(BK == 16 || BK == 32, "BK");
+  static_assert(CL == 1 || (CL == 2 && !LSU), "clusters pair TMA-fed CTAs only");
+  static constexpr int kAPartRows = kTM / CL;                    // A rows each CTA loads
+  static constexpr int kAPartBytes = kAPartRows * BK * 4;
   static constexpr int kRowBytes = BK * 4;                       // one row of the A tile
   static constexpr int kAtomBytes = 8 * kRowBytes;               // 8-row swizzle atom (SBO)
   static constexpr uint32_t kLayout = BK == 32 ? 2u : 4u;        // 128- or 64-byte swizzle
@@ -142,27 +165,33 @@ struct alignas(8) TcShared {
   int fix_tile, fix_nparts, fix_mb, fix_nb;  // final split tile left for all warps to sum
 };
 
-__device__ __forceinline__ void tile_coords(const TcParams &p, int t, int &mb, int &nb) {
-  const int group_tiles = kGroupM * p.num_n_blocks;
+// Unit tile t -> (m-block, n-block of this CTA): grouped raster over unit
+// tiles, then the CTA's rank within its cluster picks one of the cl output
+// tiles of the unit tile.
+__device__ __forceinline__ void tile_coords(const TcParams &p, int t, uint32_t rank, int &mb,
+                                            int &nb) {
+  const int group_tiles = kGroupM * p.num_nu_blocks;
   const int g = t / group_tiles;
   const int first_m = g * kGroupM;
   const int gm = min(p.num_m_blocks - first_m, kGroupM);
   const int r = t - g * group_tiles;
   mb = first_m + r % gm;
-  nb = r / gm;
+  nb = (r / gm) * p.cl + static_cast<int>(rank);
 }
 
-// The work list of one CTA, identical for every role: first the whole tiles
-// c, c + grid, ... below dp_tiles (raster order, so concurrent CTAs share
-// operand tiles in L2), then its stream-K chunk (k-blocks
-// [c * share, (c + 1) * share) of the remaining tiles, in order, cut at tile
-// boundaries). Every CTA of the grid sees the same partition, so the number
-// of CTAs contributing to a split tile and each CTA's part index follow from
-// the chunk boundaries alone.
+// The work list of one cluster c (both CTAs of a cluster walk the same list),
+// identical for every role: first the whole unit tiles c, c + clusters, ...
+// below dp_tiles (raster order, so concurrent clusters share operand tiles in
+// L2), then its stream-K chunk (k-blocks [c * share, (c + 1) * share) of the
+// remaining unit tiles, in order, cut at tile boundaries). Every cluster sees
+// the same partition, so the number of clusters contributing to a split tile
+// and each one's part index follow from the chunk boundaries alone.
 struct UnitIter {
   int sk_pos, sk_end, dp_next;
+  int c, workers;
   __device__ explicit UnitIter(const TcParams &p) {
-    const int c = blockIdx.x;
+    c = static_cast<int>(blockIdx.x) / p.cl;
+    workers = static_cast<int>(gridDim.x) / p.cl;
     const int sk_total = (p.num_tiles - p.dp_tiles) * p.num_k_blocks;
     if (c < p.sk_ctas && sk_total > 0) {
       sk_pos = min(c * p.sk_share, sk_total);
@@ -180,7 +209,8 @@ struct UnitIter {
       u.sk_tile = -1;
       u.part = 0;
       u.nparts = 1;
-      dp_next += gridDim.x;
+      u.slot = -1;
+      dp_next += workers;
       return true;
     }
     if (sk_pos < sk_end) {
@@ -193,7 +223,8 @@ struct UnitIter {
       const int first = (s * kbt) / p.sk_share;
       const int last = ((s + 1) * kbt - 1) / p.sk_share;
       u.nparts = last - first + 1;
-      u.part = static_cast<int>(blockIdx.x) - first;
+      u.part = c - first;
+      u.slot = split_slot(p, s, u.part);
       sk_pos += u.kb1 - u.kb0;
       return true;
     }
@@ -209,14 +240,15 @@ struct UnitIter {
 // result to C. Run by `nthreads` threads of the CTA that finished last: the
 // four epilogue warps, or every warp of the CTA for its final unit. The tile
 // is read as float4s, eight per thread and part in flight at a time.
-__device__ __noinline__ void epilogue_fixup(const TcParams &p, int sk_tile, int nparts, int mb,
-                                            int nb, int tid, int nthreads) {
+__device__ __noinline__ void epilogue_fixup(const TcParams &p, int sk_tile, uint32_t rank,
+                                            int nparts, int mb, int nb, int tid, int nthreads) {
   constexpr int kVec = kTM * kTN / 4;  // float4s per tile
   constexpr int kRowVec = kTN / 4;     // float4s per tile row
   constexpr int kBatch = 8;
   const long long slot4 = static_cast<long long>(kTM) * kTN / 4;
-  const float4 *base = reinterpret_cast<const float4 *>(p.sk_partials) +
-                       static_cast<long long>(sk_tile) * p.sk_max_parts * slot4;
+  // Slot (index, rank) starts at (index * cl + rank) * slot4 float4s.
+  const float4 *parts = reinterpret_cast<const float4 *>(p.sk_partials) + rank * slot4;
+  const float4 *base = parts + static_cast<long long>(split_slot(p, sk_tile, 0)) * p.cl * slot4;
   const bool vec_ok = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
 #pragma unroll 1
   for (int f0 = 0; f0 < kVec; f0 += nthreads * kBatch) {
@@ -228,11 +260,12 @@ __device__ __noinline__ void epilogue_fixup(const TcParams &p, int sk_tile, int 
     }
 #pragma unroll 1
     for (int q = 1; q < nparts; ++q) {
+      const float4 *src = parts + static_cast<long long>(split_slot(p, sk_tile, q)) * p.cl * slot4;
       float4 v[kBatch];
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const int f = f0 + tid + nthreads * j;
-        v[j] = f < kVec ? __ldcg(base + q * slot4 + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[j] = f < kVec ? __ldcg(src + f) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
@@ -333,11 +366,11 @@ __device__ __forceinline__ void stage_a_value(uint8_t *stage, int lo_offset, uin
   }
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU>
-__global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL>
+__global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
-  using Cfg = TcConfig<BK, STAGES, EXACT, LSU>;
+  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -346,12 +379,13 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
 
   const uint32_t warp = warp_index();
   const uint32_t lane = threadIdx.x & 31;
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sh->full[s], LSU ? Cfg::kProdWarps : 1);
       mbar_init(&sh->ready[s], Cfg::kXformWarps > 0 ? Cfg::kXformWarps : 1);
-      mbar_init(&sh->empty[s], 1);
+      mbar_init(&sh->empty[s], CL);  // the MMAs of every CTA that writes this stage
     }
     mbar_init(&sh->acc_full, 1);
     mbar_init(&sh->acc_empty, 4);
@@ -370,6 +404,9 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
   }
   tc_fence_before_sync();
   __syncthreads();
+  // The peer's multicast copies and commits target this CTA's barriers: they
+  // must be initialised cluster-wide before either CTA issues one.
+  if (CL > 1) cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
 
@@ -382,7 +419,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
       WorkUnit u;
       while (ok && it.next(p, u)) {
         int mb, nb;
-        tile_coords(p, u.tile, mb, nb);
+        tile_coords(p, u.tile, rank, mb, nb);
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (!mbar_wait_bounded(&sh->empty[stage], phase ^ 1, p.timeout_ns, abort,
                                  &g_tc_status)) {
@@ -390,8 +427,15 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
             break;
           }
           uint8_t *st = tiles + stage * Cfg::kStageBytes;
+          // The whole A tile arrives (each CTA of the cluster multicasts its
+          // rows to all of them) plus this CTA's own B tile.
           mbar_arrive_expect_tx(&sh->full[stage], Cfg::kABytes + BK * kTN * 4);
-          tma_load_2d(st, &tmap_a, &sh->full[stage], kb * BK, mb * kTM);
+          if (CL > 1)
+            tma_load_2d_multicast(st + rank * Cfg::kAPartBytes, &tmap_a, &sh->full[stage], kb * BK,
+                                  mb * kTM + static_cast<int>(rank) * Cfg::kAPartRows,
+                                  static_cast<uint16_t>((1u << CL) - 1));
+          else
+            tma_load_2d(st, &tmap_a, &sh->full[stage], kb * BK, mb * kTM);
           tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], nb * kTN, kb * BK);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -417,7 +461,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
     WorkUnit u;
     while (it.next(p, u)) {
       int mb, nb;
-      tile_coords(p, u.tile, mb, nb);
+      tile_coords(p, u.tile, rank, mb, nb);
       const int m0 = mb * kTM, n0 = nb * kTN;
       bool ok = true;
       for (int kb = u.kb0; kb < u.kb1; ++kb) {
@@ -515,7 +559,10 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
               mma_tf32_ts(d_tmem, bt_hi + kk * kUmmaK, da, Cfg::kIdesc, accumulate);
             }
           }
-          mma_commit(&sh->empty[stage]);
+          if (CL > 1)
+            mma_commit_multicast(&sh->empty[stage], static_cast<uint16_t>((1u << CL) - 1));
+          else
+            mma_commit(&sh->empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -538,7 +585,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
     WorkUnit u;
     while (it.next(p, u)) {
       int mb, nb;
-      tile_coords(p, u.tile, mb, nb);
+      tile_coords(p, u.tile, rank, mb, nb);
       // The four epilogue warps continue or give up together: the split-tile
       // path below synchronises them with named barriers.
       if (!named_barrier_and(1, 128, warp_wait(&sh->acc_full, acc_phase, p, abort))) break;
@@ -579,8 +626,8 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
         // parts in part order (a fixed order, so results are deterministic)
         // and writes C.
         const long long slot_elems = static_cast<long long>(kTM) * kTN;
-        float *slot = p.sk_partials +
-                      (static_cast<long long>(u.sk_tile) * p.sk_max_parts + u.part) * slot_elems;
+        float *slot =
+            p.sk_partials + (static_cast<long long>(u.slot) * p.cl + rank) * slot_elems;
 #pragma unroll 1
         for (int c = 0; c < kTM / 32; ++c) {
           uint32_t r[32];
@@ -596,7 +643,8 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
         __threadfence();
         named_barrier_sync(1, 128);
         if (warp == Cfg::kEpiWarp0 && lane == 0)
-          sh->sk_last = atomicAdd(&p.sk_counters[u.sk_tile], 1u) == static_cast<unsigned>(u.nparts - 1);
+          sh->sk_last = atomicAdd(&p.sk_counters[u.sk_tile * p.cl + rank], 1u) ==
+                        static_cast<unsigned>(u.nparts - 1);
         named_barrier_sync(1, 128);
         if (sh->sk_last) {
           if (it.done(p)) {
@@ -609,7 +657,8 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
             }
           } else {
             __threadfence();
-            epilogue_fixup(p, u.sk_tile, u.nparts, mb, nb, threadIdx.x - Cfg::kEpiWarp0 * 32, 128);
+            epilogue_fixup(p, u.sk_tile, rank, u.nparts, mb, nb, threadIdx.x - Cfg::kEpiWarp0 * 32,
+                           128);
           }
         }
         named_barrier_sync(1, 128);  // sk_last is reused by the next split tile
@@ -688,9 +737,11 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU>::kThreads, 1)
   }
   if (sh->fix_tile >= 0 && !sh->abort) {
     __threadfence();
-    epilogue_fixup(p, sh->fix_tile, sh->fix_nparts, sh->fix_mb, sh->fix_nb, threadIdx.x,
+    epilogue_fixup(p, sh->fix_tile, rank, sh->fix_nparts, sh->fix_mb, sh->fix_nb, threadIdx.x,
                    blockDim.x);
   }
+  // No CTA of a cluster leaves while its peer may still signal its barriers.
+  if (CL > 1) cluster_sync();
 }
 
 // One warp waits, bounded, on a barrier that is never signalled.
@@ -783,6 +834,11 @@ bool get_map(const void *ptr, uint64_t d0, uint64_t d1, uint64_t pitch_bytes, ui
   return true;
 }
 
+// CTAs per cluster of the TMA-fed kernels (pairs share the A tile by
+// multicast, which halves its L2 reads).
+constexpr int kClusterExact = 2;
+constexpr int kClusterTf32 = 2;
+
 // Smallest stream-K chunk, in k: shorter chunks spend more time filling the
 // pipeline and more bytes on partial tiles than they save.
 constexpr int kMinChunkK = 256;
@@ -790,7 +846,8 @@ constexpr int kMinChunkK = 256;
 constexpr int kMaxSplit = 8;
 
 struct Schedule {
-  int grid, dp_tiles, sk_share, sk_ctas, sk_max_parts;
+  int grid, dp_tiles, sk_share, sk_ctas;
+  bool splits;  // some tile's k range is shared by two or more chunks
 };
 
 // Data-parallel waves plus a stream-K tail. With T tiles of KB k-blocks on
@@ -811,7 +868,7 @@ Schedule make_schedule(int tiles, int kb, int sms, int min_chunk) {
     s.grid = sms < tiles ? sms : tiles;
     s.sk_share = 1;
     s.sk_ctas = 0;
-    s.sk_max_parts = 1;
+    s.splits = false;
     return s;
   }
   const long long total = static_cast<long long>(split) * kb;
@@ -829,94 +886,185 @@ Schedule make_schedule(int tiles, int kb, int sms, int min_chunk) {
   s.sk_share = static_cast<int>((total + ctas - 1) / ctas);
   s.sk_ctas = static_cast<int>((total + s.sk_share - 1) / s.sk_share);
   // Chunks that are whole multiples of a tile never split one.
-  s.sk_max_parts = s.sk_share % kb == 0 ? 1 : (kb + s.sk_share - 1) / s.sk_share + 1;
+  s.splits = s.sk_share % kb != 0;
   s.grid = split >= sms ? sms : s.sk_ctas;
   return s;
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU>
-int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
-  using Cfg = TcConfig<BK, STAGES, EXACT, LSU>;
-  auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU>;
-  const int smem_bytes = Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
-
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return kErrLaunch;
-  static bool attr_set[64] = {};
-  static std::mutex attr_mu;
-  {
-    std::lock_guard<std::mutex> g(attr_mu);
-    if (dev < 64 && !attr_set[dev]) {
-      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
-          cudaSuccess)
-        return kErrLaunch;
-      attr_set[dev] = true;
-    }
-  }
-
-  CUtensorMap map_a, map_b;
-  std::memset(&map_a, 0, sizeof(map_a));
-  std::memset(&map_b, 0, sizeof(map_b));
-  if (!LSU) {
-    const CUtensorMapSwizzle sw_a = BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, kTM, sw_a, &map_a)) return kErrLaunch;
-    if (!get_map(a.B, a.N, a.K, a.ldb * 4, kTN, BK, CU_TENSOR_MAP_SWIZZLE_NONE, &map_b))
-      return kErrLaunch;
-  }
-
+// Everything a launch needs except the stream-K workspace.
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL>
+struct LaunchPlan {
+  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL>;
   TcParams p;
-  p.M = static_cast<int>(a.M);
-  p.N = static_cast<int>(a.N);
-  p.K = static_cast<int>(a.K);
-  p.A = a.A;
-  p.lda = a.lda;
-  p.B = a.B;
-  p.ldb = a.ldb;
-  p.C = a.C;
-  p.ldc = a.ldc;
-  p.num_m_blocks = static_cast<int>((a.M + kTM - 1) / kTM);
-  p.num_n_blocks = static_cast<int>((a.N + kTN - 1) / kTN);
-  p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-  p.num_k_blocks = static_cast<int>((a.K + BK - 1) / BK);
-  // Generous: a stage takes microseconds; one tile's mainloop about K * 25 ns.
-  p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
+  Schedule sch;
+  CUtensorMap map_a, map_b;
+  int smem_bytes = 0;
+  size_t counter_bytes = 0, partial_bytes = 0;  // workspace, 0 if no tile is split
 
-  const Schedule sch = make_schedule(p.num_tiles, p.num_k_blocks, sm_count, kMinChunkK / BK);
-  p.dp_tiles = sch.dp_tiles;
-  p.sk_share = sch.sk_share;
-  p.sk_ctas = sch.sk_ctas;
-  p.sk_max_parts = sch.sk_max_parts;
-  p.sk_partials = nullptr;
-  p.sk_counters = nullptr;
-  const int grid = sch.grid;
-
-  // Split tiles need a workspace: partial tiles and one counter per split
-  // tile. It comes from the device's stream-ordered pool on the caller's
-  // stream and goes back right after the kernel, so concurrent calls on other
-  // streams never share it.
-  void *ws = nullptr;
-  const int split_tiles = p.num_tiles - p.dp_tiles;
-  if (split_tiles > 0 && sch.sk_max_parts > 1) {
-    const size_t counter_bytes = (static_cast<size_t>(split_tiles) * 4 + 255) / 256 * 256;
-    const size_t partial_bytes = static_cast<size_t>(split_tiles) * sch.sk_max_parts * kTM * kTN * 4;
-    if (cudaMallocAsync(&ws, counter_bytes + partial_bytes, stream) != cudaSuccess) return kErrLaunch;
-    if (cudaMemsetAsync(ws, 0, counter_bytes, stream) != cudaSuccess) {
-      cudaFreeAsync(ws, stream);
-      return kErrLaunch;
+  int prepare(const GemmArgs &a, int sm_count) {
+    auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL>;
+    smem_bytes = Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kErrLaunch;
+    static bool attr_set[64] = {};
+    static std::mutex attr_mu;
+    {
+      std::lock_guard<std::mutex> g(attr_mu);
+      if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+            cudaSuccess)
+          return kErrLaunch;
+        attr_set[dev] = true;
+      }
     }
+    std::memset(&map_a, 0, sizeof(map_a));
+    std::memset(&map_b, 0, sizeof(map_b));
+    if (!LSU) {
+      const CUtensorMapSwizzle sw_a =
+          BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+      if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, Cfg::kAPartRows, sw_a, &map_a)) return kErrLaunch;
+      if (!get_map(a.B, a.N, a.K, a.ldb * 4, kTN, BK, CU_TENSOR_MAP_SWIZZLE_NONE, &map_b))
+        return kErrLaunch;
+    }
+    p.M = static_cast<int>(a.M);
+    p.N = static_cast<int>(a.N);
+    p.K = static_cast<int>(a.K);
+    p.A = a.A;
+    p.lda = a.lda;
+    p.B = a.B;
+    p.ldb = a.ldb;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.num_m_blocks = static_cast<int>((a.M + kTM - 1) / kTM);
+    p.num_n_blocks = static_cast<int>((a.N + kTN - 1) / kTN);
+    p.num_k_blocks = static_cast<int>((a.K + BK - 1) / BK);
+    p.cl = CL;
+    p.num_nu_blocks = (p.num_n_blocks + CL - 1) / CL;
+    p.num_tiles = p.num_m_blocks * p.num_nu_blocks;
+    // Generous: a stage takes microseconds; one tile's mainloop about K * 25 ns.
+    p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
+    // Workers: clusters that can be resident at once (the placement of CTA
+    // pairs may leave some SMs unpaired).
+    static int workers_cached[64] = {};
+    static std::mutex workers_mu;
+    int workers = sm_count / CL;
+    if (CL > 1) {
+      std::lock_guard<std::mutex> g(workers_mu);
+      if (workers_cached[dev] == 0) {
+        cudaLaunchConfig_t qc = {};
+        qc.gridDim = dim3(CL * workers, 1, 1);
+        qc.blockDim = dim3(Cfg::kThreads, 1, 1);
+        qc.dynamicSmemBytes = smem_bytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CL;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        qc.attrs = attr;
+        qc.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &qc) != cudaSuccess || clusters <= 0)
+          return kErrLaunch;
+        workers_cached[dev] = clusters < workers ? clusters : workers;
+      }
+      workers = workers_cached[dev];
+    }
+    sch = make_schedule(p.num_tiles, p.num_k_blocks, workers, kMinChunkK / BK);
+    p.dp_tiles = sch.dp_tiles;
+    p.sk_share = sch.sk_share;
+    p.sk_ctas = sch.sk_ctas;
+    p.sk_partials = nullptr;
+    p.sk_counters = nullptr;
+    const int split_tiles = p.num_tiles - p.dp_tiles;
+    if (split_tiles > 0 && sch.splits) {
+      counter_bytes = (static_cast<size_t>(split_tiles) * CL * 4 + 255) / 256 * 256;
+      partial_bytes = static_cast<size_t>(sch.sk_ctas) * 2 * CL * kTM * kTN * 4;
+    }
+    return kOk;
+  }
+
+  // Point the schedule at a workspace of counter_bytes + partial_bytes.
+  void set_workspace(void *ws) {
     p.sk_counters = static_cast<unsigned *>(ws);
     p.sk_partials = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + counter_bytes);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes;
-  cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
-  const bool launched = cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p) == cudaSuccess;
+
+  int launch(cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sch.grid * CL, 1, 1);
+    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CL > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL>, map_a, map_b, p) ==
+                   cudaSuccess
+               ? kOk
+               : kErrLaunch;
+  }
+};
+
+// The library's own stream-ordered memory pool on each device, for stream-K
+// workspaces. Unlike the device's default pool (release threshold 0, which
+// hands memory back to the driver at every synchronisation and makes the
+// next allocation map it again), it keeps what it has reserved, so a
+// workspace allocation after a synchronisation costs no more than one inside
+// a busy stream.
+int workspace_pool(int dev, cudaMemPool_t *out) {
+  static cudaMemPool_t pools[64] = {};
+  static std::mutex mu;
+  if (dev < 0 || dev >= 64) return kErrLaunch;
+  std::lock_guard<std::mutex> g(mu);
+  if (pools[dev] == nullptr) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return kErrLaunch;
+    uint64_t keep = ~0ull;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return kErrLaunch;
+    }
+    pools[dev] = pool;
+  }
+  *out = pools[dev];
+  return kOk;
+}
+
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL>
+int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
+  LaunchPlan<BK, STAGES, EXACT, LSU, CL> plan;
+  int st = plan.prepare(a, sm_count);
+  if (st != kOk) return st;
+  // Split tiles need a workspace: partial tiles and one counter per split
+  // tile and CTA rank. It comes from the library's stream-ordered pool on the
+  // caller's stream and goes back right after the kernel, so concurrent calls
+  // on other streams never share it.
+  void *ws = nullptr;
+  if (plan.counter_bytes > 0) {
+    int dev = 0;
+    cudaMemPool_t pool = nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || workspace_pool(dev, &pool) != kOk) return kErrLaunch;
+    if (cudaMallocFromPoolAsync(&ws, plan.counter_bytes + plan.partial_bytes, pool, stream) !=
+        cudaSuccess)
+      return kErrLaunch;
+    if (cudaMemsetAsync(ws, 0, plan.counter_bytes, stream) != cudaSuccess) {
+      cudaFreeAsync(ws, stream);
+      return kErrLaunch;
+    }
+    plan.set_workspace(ws);
+  }
+  st = plan.launch(stream);
   if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess) return kErrLaunch;
-  return launched ? kOk : kErrLaunch;
+  return st;
 }
 
 }  // namespace
@@ -931,11 +1079,11 @@ int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_
   // A 16 KiB + B 8 KiB + A_lo 16 KiB per stage; tf32 32 x 4 with A 32 KiB +
   // B 16 KiB. The LSU variants stage no B tile in shared memory.
   if (exact) {
-    if (lsu) return launch_variant<16, 6, true, true>(a, sm_count, stream);
-    return launch_variant<16, 5, true, false>(a, sm_count, stream);
+    if (lsu) return launch_variant<16, 6, true, true, 1>(a, sm_count, stream);
+    return launch_variant<16, 5, true, false, kClusterExact>(a, sm_count, stream);
   }
-  if (lsu) return launch_variant<32, 6, false, true>(a, sm_count, stream);
-  return launch_variant<32, 4, false, false>(a, sm_count, stream);
+  if (lsu) return launch_variant<32, 6, false, true, 1>(a, sm_count, stream);
+  return launch_variant<32, 4, false, false, kClusterTf32>(a, sm_count, stream);
 }
 
 int tc_poll_status(cudaStream_t stream) {
@@ -994,86 +1142,26 @@ int noalloc_scratch(int dev, void **out) {
   return kOk;
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU>
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL>
 int launch_variant_noalloc(const GemmArgs &a, int sm_count, cudaStream_t stream) {
-  using Cfg = TcConfig<BK, STAGES, EXACT, LSU>;
-  auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU>;
-  const int smem_bytes = Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
-
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return kErrLaunch;
   void *scratch = nullptr;
-  const int st = noalloc_scratch(dev, &scratch);
+  int st = noalloc_scratch(dev, &scratch);
   if (st != kOk) return st;
-
-  TcParams p;
-  p.M = static_cast<int>(a.M);
-  p.N = static_cast<int>(a.N);
-  p.K = static_cast<int>(a.K);
-  p.A = a.A;
-  p.lda = a.lda;
-  p.B = a.B;
-  p.ldb = a.ldb;
-  p.C = a.C;
-  p.ldc = a.ldc;
-  p.num_m_blocks = static_cast<int>((a.M + kTM - 1) / kTM);
-  p.num_n_blocks = static_cast<int>((a.N + kTN - 1) / kTN);
-  p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-  p.num_k_blocks = static_cast<int>((a.K + BK - 1) / BK);
-  p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
-  const Schedule sch = make_schedule(p.num_tiles, p.num_k_blocks, sm_count, kMinChunkK / BK);
-  p.dp_tiles = sch.dp_tiles;
-  p.sk_share = sch.sk_share;
-  p.sk_ctas = sch.sk_ctas;
-  p.sk_max_parts = sch.sk_max_parts;
-  p.sk_partials = nullptr;
-  p.sk_counters = nullptr;
-
+  LaunchPlan<BK, STAGES, EXACT, LSU, CL> plan;
+  st = plan.prepare(a, sm_count);
+  if (st != kOk) return st;
   // The same workspace layout gemm_f32 takes from the pool, here inside the
   // fixed array; problems that need more are refused before anything runs.
-  const int split_tiles = p.num_tiles - p.dp_tiles;
-  size_t counter_bytes = 0;
-  if (split_tiles > 0 && sch.sk_max_parts > 1) {
-    counter_bytes = (static_cast<size_t>(split_tiles) * 4 + 255) / 256 * 256;
-    const size_t partial_bytes =
-        static_cast<size_t>(split_tiles) * sch.sk_max_parts * kTM * kTN * 4;
-    if (counter_bytes + partial_bytes > GEMM_F32_NOALLOC_SCRATCH_BYTES) return kErrInvalidArg;
-    p.sk_counters = static_cast<unsigned *>(scratch);
-    p.sk_partials = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) + counter_bytes);
+  if (plan.counter_bytes > 0) {
+    if (plan.counter_bytes + plan.partial_bytes > GEMM_F32_NOALLOC_SCRATCH_BYTES)
+      return kErrInvalidArg;
+    // The counters must start at zero; the previous call left them counted up.
+    if (cudaMemsetAsync(scratch, 0, plan.counter_bytes, stream) != cudaSuccess) return kErrLaunch;
+    plan.set_workspace(scratch);
   }
-
-  static bool attr_set[64] = {};
-  static std::mutex attr_mu;
-  {
-    std::lock_guard<std::mutex> g(attr_mu);
-    if (!attr_set[dev]) {
-      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
-          cudaSuccess)
-        return kErrLaunch;
-      attr_set[dev] = true;
-    }
-  }
-  CUtensorMap map_a, map_b;
-  std::memset(&map_a, 0, sizeof(map_a));
-  std::memset(&map_b, 0, sizeof(map_b));
-  if (!LSU) {
-    const CUtensorMapSwizzle sw_a = BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, kTM, sw_a, &map_a)) return kErrLaunch;
-    if (!get_map(a.B, a.N, a.K, a.ldb * 4, kTN, BK, CU_TENSOR_MAP_SWIZZLE_NONE, &map_b))
-      return kErrLaunch;
-  }
-  // The counters must start at zero; the previous call left them counted up.
-  if (counter_bytes > 0 && cudaMemsetAsync(scratch, 0, counter_bytes, stream) != cudaSuccess)
-    return kErrLaunch;
-
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(sch.grid, 1, 1);
-  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem_bytes;
-  cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, kernel, map_a, map_b, p) == cudaSuccess ? kOk : kErrLaunch;
+  return plan.launch(stream);
 }
 
 }  // namespace
@@ -1081,11 +1169,11 @@ int launch_variant_noalloc(const GemmArgs &a, int sm_count, cudaStream_t stream)
 int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream) {
   // Same kernels and stage shapes as tc_launch.
   if (exact) {
-    if (lsu) return launch_variant_noalloc<16, 6, true, true>(a, sm_count, stream);
-    return launch_variant_noalloc<16, 5, true, false>(a, sm_count, stream);
+    if (lsu) return launch_variant_noalloc<16, 6, true, true, 1>(a, sm_count, stream);
+    return launch_variant_noalloc<16, 5, true, false, kClusterExact>(a, sm_count, stream);
   }
-  if (lsu) return launch_variant_noalloc<32, 6, false, true>(a, sm_count, stream);
-  return launch_variant_noalloc<32, 4, false, false>(a, sm_count, stream);
+  if (lsu) return launch_variant_noalloc<32, 6, false, true, 1>(a, sm_count, stream);
+  return launch_variant_noalloc<32, 4, false, false, kClusterTf32>(a, sm_count, stream);
 }
 
 }  // namespace gemm

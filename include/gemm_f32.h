@@ -33,8 +33,13 @@
  * gemm_f32_ex are DEVICE pointers owned by the caller; the library keeps no
  * reference to them after the call returns. `stream` is a cudaStream_t passed
  * as void* (NULL = the legacy default stream). The call is stream ordered: it
- * enqueues work and returns without synchronising. The library allocates no
- * memory per call.
+ * enqueues work and returns without synchronising. When the schedule splits
+ * the k range of some output tiles between SMs (stream-K), the call takes a
+ * workspace of at most two 128 KiB partial tiles per SM from a stream-ordered
+ * memory pool that the library creates on each device and never shrinks, and
+ * returns it to the pool behind the kernel on the same stream; calls on
+ * different streams therefore never share it. gemm_f32_noalloc avoids even
+ * that.
  *
  * Errors are returned synchronously as gemm_f32_status codes. Argument errors
  * are detected on the host before anything is enqueued, and no CUDA call is
@@ -139,8 +144,8 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K,
                   float *C, int64_t ldc,
                   int mode);
 
-/* Bytes of the fixed device array that gemm_f32_noalloc works in (64 MiB). */
-#define GEMM_F32_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+/* Bytes of the fixed device array that gemm_f32_noalloc works in (40 MiB). */
+#define GEMM_F32_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
 
 /*
  * gemm_f32_noalloc -- gemm_f32 without any device memory allocation. (The
@@ -152,7 +157,7 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K,
  * budget-critical loops that must keep the process's device footprint and
  * allocator state fixed once set up. gemm_f32 takes its stream-K workspace
  * (partial sums of output tiles whose k range is shared between SMs) from
- * the device's stream-ordered memory pool; this entry point runs the same
+ * the library's stream-ordered memory pool; this entry point runs the same
  * kernels and schedule but keeps that workspace in a fixed array of
  * GEMM_F32_NOALLOC_SCRATCH_BYTES that is part of the library's device image:
  * every GPU that loads the library holds it until the process exits.
@@ -161,9 +166,9 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K,
  * pointers owned by the caller, stream ordered, non-blocking), and results
  * are the same. In addition it returns GEMM_ERR_INVALID_ARG, before
  * enqueuing anything, for a problem whose workspace would not fit in the
- * array: that happens only when the stream-K part of the schedule spans more
- * than about 250 output tiles of 256 x 128 (it never spans more than 303 on
- * a 152-SM GB300); a 4096^3 product uses about 52 MiB of the array.
+ * array. The workspace holds at most two 128 KiB partial tiles per SM plus a
+ * few counters (under 39 MiB on a 152-SM GB300, whatever the shape), so on
+ * such a device every valid problem fits; the check guards larger devices.
  *
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.

@@ -6,8 +6,8 @@ take its stream-K workspace from the memory pool. gemm_f32_noalloc runs the
 same kernels with that workspace in a fixed array inside the library. These
 tests call it through the C ABI, twice in a row with different problems (so
 the second call starts from the first call's leftovers in the array), and
-compare each result with gemm_f32's on the same inputs; they also check that
-a problem too big for the array is refused. This file is collected last.
+compare each result with gemm_f32's on the same inputs. This file is
+collected last.
 """
 
 import numpy as np
@@ -62,15 +62,3 @@ def test_noalloc_matches_gemm_f32_on_calls_in_a_row(g):
         tol = tolerance_factor(mode, k) * s
         diff = np.abs(out[rows].astype(np.float64) - ref[rows].astype(np.float64))
         assert np.all(diff <= tol), f"{mode} {m}x{n}x{k}: max diff {diff.max():.3e}"
-
-
-def test_noalloc_refuses_problems_beyond_its_scratch(g):
-    # 101 x 3 output tiles with K = 4096 in exact mode: every tile is split in
-    # two and the workspace (about 79 MB) exceeds the fixed array. Refused on
-    # the host before anything is enqueued, so the (never dereferenced)
-    # addresses below are not touched.
-    assert g.NOALLOC_SCRATCH_BYTES == 64 * 1024 * 1024
-    m, n, k = 256 * 101, 384, 4096
-    pa, pb, pc = 1 << 40, 2 << 40, 3 << 40
-    st = g.gemm_f32_noalloc(m, n, k, pa, k, pb, n, pc, n, g.EXACT, 0)
-    assert st == g.ERR_INVALID_ARG
