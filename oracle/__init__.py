@@ -63,6 +63,10 @@ def _load():
             lib.oracle_gemm_rows_f64.restype = None
             lib.oracle_gemm_entries_f64.argtypes = [i64, p, p, i64, p, i64, p, i64, p, p]
             lib.oracle_gemm_entries_f64.restype = None
+            d = ctypes.c_double
+            lib.oracle_gemm_general_rows_f64.argtypes = [ctypes.c_int, i64, p, i64, i64, d, p, i64,
+                                                         p, i64, d, p, i64, p, p]
+            lib.oracle_gemm_general_rows_f64.restype = None
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -144,6 +148,38 @@ def gemm_entries(a: np.ndarray, b: np.ndarray, ii, jj):
         _load().oracle_gemm_entries_f64(ii.size, _ptr(ii), _ptr(jj), k, _ptr(a), _ld(a),
                                         _ptr(b), _ld(b), _ptr(c64), _ptr(s))
     return c64, s
+
+
+def gemm_general(a: np.ndarray, b: np.ndarray, opb: int = 0, alpha: float = 1.0,
+                 beta: float = 0.0, c: np.ndarray | None = None, rows=None):
+    """Cout = alpha * a @ op(b) + beta * c in fp64, and S = |a| @ |op(b)|.
+
+    op(b) = b (K x N) when opb == 0, or b.T when opb == 1 (b then stored N x K).
+    ``c`` (M x N fp32) is read only when beta != 0. ``rows`` selects output rows
+    (default: all). Returns (Cout, S), each len(rows) x N.
+    """
+    a = _as_f32_2d(a, "a")
+    b = _as_f32_2d(b, "b")
+    m, k = a.shape
+    n, kb = (b.shape[1], b.shape[0]) if opb == 0 else (b.shape[0], b.shape[1])
+    if k != kb:
+        raise ValueError("inner dimensions differ")
+    rows = np.arange(m, dtype=np.int64) if rows is None else np.asarray(rows, dtype=np.int64)
+    rows = np.ascontiguousarray(rows)
+    if beta != 0.0:
+        if c is None or c.shape != (m, n):
+            raise ValueError("beta != 0 needs c of shape (M, N)")
+        c = _as_f32_2d(c, "c")
+        cptr, ldc = _ptr(c), _ld(c)
+    else:
+        cptr, ldc = None, max(n, 1)
+    out = np.zeros((rows.size, n), dtype=np.float64)
+    s = np.zeros((rows.size, n), dtype=np.float64)
+    if rows.size and n:
+        _load().oracle_gemm_general_rows_f64(int(opb), rows.size, _ptr(rows), n, k, float(alpha),
+                                             _ptr(a), _ld(a), _ptr(b), _ld(b), float(beta), cptr,
+                                             ldc, _ptr(out), _ptr(s))
+    return out, s
 
 
 def num_threads() -> int:

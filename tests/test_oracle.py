@@ -249,3 +249,47 @@ def test_input_generators_are_deterministic_and_in_range():
 
 def test_num_threads_reported():
     assert oracle.num_threads() >= 1
+
+
+# --- the general form: alpha * A op(B) + beta * C -----------------------------
+
+@pytest.mark.parametrize("m,n,k", [(1, 1, 1), (7, 5, 3), (33, 65, 17)])
+def test_general_reduces_to_the_plain_product(m, n, k):
+    a = synth.normal((m, k), 51)
+    b = synth.normal((k, n), 52)
+    c64, s = oracle.gemm(a, b)
+    g64, gs = oracle.gemm_general(a, b)
+    assert np.array_equal(g64, c64) and np.array_equal(gs, s)
+    # B supplied transposed: same products, same k order, so bitwise equal
+    t64, ts = oracle.gemm_general(a, np.ascontiguousarray(b.T), opb=1)
+    assert np.array_equal(t64, c64) and np.array_equal(ts, s)
+
+
+def test_general_scaling_and_accumulation():
+    m, n, k = 9, 11, 13
+    a = synth.small_integers((m, k), 53)
+    b = synth.small_integers((k, n), 54)
+    c = synth.small_integers((m, n), 55)
+    c64, _ = oracle.gemm(a, b)
+    # exact for small integers and dyadic scales
+    out, _ = oracle.gemm_general(a, b, alpha=2.0, beta=-0.5, c=c)
+    assert np.array_equal(out, 2.0 * c64 - 0.5 * c.astype(np.float64))
+    out, _ = oracle.gemm_general(a, b, alpha=0.0, beta=1.0, c=c)
+    assert np.array_equal(out, c.astype(np.float64))
+    # beta == 0 never reads C (NaN there does not propagate)
+    nanc = np.full((m, n), np.nan, np.float32)
+    out, _ = oracle.gemm_general(a, b, alpha=1.0, beta=0.0, c=nanc)
+    assert np.array_equal(out, c64)
+    # hand-worked: the 2x2 fixture with alpha = 1, beta = 1, C = [[1, 1], [1, 1]]
+    g = _read_golden("hand_2x2.txt")
+    out, _ = oracle.gemm_general(g["A"].astype(np.float32), g["B"].astype(np.float32), alpha=1.0,
+                                 beta=1.0, c=np.ones((2, 2), np.float32))
+    assert np.array_equal(out, g["C"] + 1)
+
+
+def test_general_rows_select():
+    a = synth.normal((20, 7), 56)
+    b = synth.normal((7, 9), 57)
+    full, s = oracle.gemm_general(a, b)
+    part, ps = oracle.gemm_general(a, b, rows=[19, 0, 5])
+    assert np.array_equal(part, full[[19, 0, 5]]) and np.array_equal(ps, s[[19, 0, 5]])
