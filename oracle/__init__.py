@@ -64,8 +64,8 @@ def _load():
             lib.oracle_gemm_entries_f64.argtypes = [i64, p, p, i64, p, i64, p, i64, p, p]
             lib.oracle_gemm_entries_f64.restype = None
             d = ctypes.c_double
-            lib.oracle_gemm_general_rows_f64.argtypes = [ctypes.c_int, i64, p, i64, i64, d, p, i64,
-                                                         p, i64, d, p, i64, p, p]
+            lib.oracle_gemm_general_rows_f64.argtypes = [ctypes.c_int, ctypes.c_int, i64, p, i64, i64,
+                                                         d, p, i64, p, i64, d, p, i64, p, p]
             lib.oracle_gemm_general_rows_f64.restype = None
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
@@ -151,16 +151,17 @@ def gemm_entries(a: np.ndarray, b: np.ndarray, ii, jj):
 
 
 def gemm_general(a: np.ndarray, b: np.ndarray, opb: int = 0, alpha: float = 1.0,
-                 beta: float = 0.0, c: np.ndarray | None = None, rows=None):
-    """Cout = alpha * a @ op(b) + beta * c in fp64, and S = |a| @ |op(b)|.
+                 beta: float = 0.0, c: np.ndarray | None = None, rows=None, opa: int = 0):
+    """Cout = alpha * op(a) @ op(b) + beta * c in fp64, and S = |op(a)| @ |op(b)|.
 
+    op(a) = a (M x K) when opa == 0, or a.T when opa == 1 (a then stored K x M);
     op(b) = b (K x N) when opb == 0, or b.T when opb == 1 (b then stored N x K).
     ``c`` (M x N fp32) is read only when beta != 0. ``rows`` selects output rows
     (default: all). Returns (Cout, S), each len(rows) x N.
     """
     a = _as_f32_2d(a, "a")
     b = _as_f32_2d(b, "b")
-    m, k = a.shape
+    m, k = (a.shape[1], a.shape[0]) if opa else a.shape
     n, kb = (b.shape[1], b.shape[0]) if opb == 0 else (b.shape[0], b.shape[1])
     if k != kb:
         raise ValueError("inner dimensions differ")
@@ -176,7 +177,8 @@ def gemm_general(a: np.ndarray, b: np.ndarray, opb: int = 0, alpha: float = 1.0,
     out = np.zeros((rows.size, n), dtype=np.float64)
     s = np.zeros((rows.size, n), dtype=np.float64)
     if rows.size and n:
-        _load().oracle_gemm_general_rows_f64(int(opb), rows.size, _ptr(rows), n, k, float(alpha),
+        _load().oracle_gemm_general_rows_f64(int(opa), int(opb), rows.size, _ptr(rows), n, k,
+                                             float(alpha),
                                              _ptr(a), _ld(a), _ptr(b), _ld(b), float(beta), cptr,
                                              ldc, _ptr(out), _ptr(s))
     return out, s

@@ -120,15 +120,20 @@ void oracle_gemm_entries_f64(int64_t n, const int64_t *ii, const int64_t *jj,
     }
 }
 
-/* General form: Cout[i][j] = alpha * sum_k A[i][k] * op(B)[k][j] + beta * Cin[i][j]
- * (beta == 0: Cin is not read), all in fp64, with op(B)[k][j] = B[k * ldb + j]
- * (opb == 0) or B[j * ldb + k] (opb == 1: the caller stores B transposed,
- * N x K). The scale S[i][j] = sum_k |A[i][k]| * |op(B)[k][j]|. This is the
+/* General form: Cout[i][j] = alpha * sum_k op(A)[i][k] * op(B)[k][j] + beta * Cin[i][j]
+ * (beta == 0: Cin is not read), all in fp64, row-major storage, with
+ *   op(A)[i][k] = A[i * lda + k] (opa == 0) or A[k * lda + i] (opa == 1: the
+ *                 caller stores A transposed, K x M),
+ *   op(B)[k][j] = B[k * ldb + j] (opb == 0) or B[j * ldb + k] (opb == 1: B
+ *                 stored transposed, N x K).
+ * The scale S[i][j] = sum_k |op(A)[i][k]| * |op(B)[k][j]|. This is the
  * product of oracle_gemm_f64 with the transposed-B storage of "Optimizing a
- * WebGPU Matmul Kernel using Subgroups", section 7 "Vectorized Buffers", and
- * the usual scale-and-add of an existing C. Rows of the output are selected
- * by rows[] (nrows of them; output row r is row rows[r]). */
-void oracle_gemm_general_rows_f64(int opb, int64_t nrows, const int64_t *rows,
+ * WebGPU Matmul Kernel using Subgroups", section 7 "Vectorized Buffers", the
+ * transposed (column-major) storage that "WebGPU 计算着色器矩阵乘法优化：从
+ * Naive 到 Tiled 深度实战" mentions under "工程实践建议", and the usual
+ * scale-and-add of an existing C. Rows of the output are selected by rows[]
+ * (nrows of them; output row r is row rows[r]). */
+void oracle_gemm_general_rows_f64(int opa, int opb, int64_t nrows, const int64_t *rows,
                                   int64_t N, int64_t K, double alpha,
                                   const float *A, int64_t lda,
                                   const float *B, int64_t ldb,
@@ -146,7 +151,7 @@ void oracle_gemm_general_rows_f64(int opb, int64_t nrows, const int64_t *rows,
         for (int64_t j = 0; j < N; ++j) {
             double acc = 0.0, scale = 0.0;
             for (int64_t k = 0; k < K; ++k) {
-                const double a = (double)A[i * lda + k];
+                const double a = (double)(opa ? A[k * lda + i] : A[i * lda + k]);
                 const double b = (double)(opb ? B[j * ldb + k] : B[k * ldb + j]);
                 acc += a * b;
                 scale += fabs(a) * fabs(b);

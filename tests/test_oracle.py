@@ -263,6 +263,27 @@ def test_general_reduces_to_the_plain_product(m, n, k):
     # B supplied transposed: same products, same k order, so bitwise equal
     t64, ts = oracle.gemm_general(a, np.ascontiguousarray(b.T), opb=1)
     assert np.array_equal(t64, c64) and np.array_equal(ts, s)
+    # A supplied transposed (K x M), and both
+    t64, ts = oracle.gemm_general(np.ascontiguousarray(a.T), b, opa=1)
+    assert np.array_equal(t64, c64) and np.array_equal(ts, s)
+    t64, ts = oracle.gemm_general(np.ascontiguousarray(a.T), np.ascontiguousarray(b.T), opa=1,
+                                  opb=1)
+    assert np.array_equal(t64, c64) and np.array_equal(ts, s)
+
+
+@pytest.mark.parametrize("name", ["hand_2x2.txt", "hand_3x2x4.txt"])
+@pytest.mark.parametrize("opa,opb", [(0, 1), (1, 0), (1, 1)])
+def test_general_transposed_storage_hand_worked(name, opa, opb):
+    # The hand-worked fixtures, with the operands handed over in transposed
+    # storage (the transposed B of the subgroups page, section 7; A likewise).
+    g = _read_golden(name)
+    a = g["A"].astype(np.float32)
+    b = g["B"].astype(np.float32)
+    a_st = np.ascontiguousarray(a.T) if opa else a
+    b_st = np.ascontiguousarray(b.T) if opb else b
+    out, s = oracle.gemm_general(a_st, b_st, opa=opa, opb=opb)
+    assert np.array_equal(out, g["C"])
+    assert np.array_equal(s, g["S"])
 
 
 def test_general_scaling_and_accumulation():
