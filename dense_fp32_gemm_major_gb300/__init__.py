@@ -8,8 +8,9 @@ missing the import fails loudly (build it with ``__graft_entry__.build()`` or
 
 The entry points mirror include/gemm_f32.h one to one (same names, same
 argument order; pointers are plain integers, streams are ``cudaStream_t``
-values as integers, 0 = the legacy default stream). ``matmul`` is a
-convenience wrapper over ``gemm_f32`` for torch CUDA tensors.
+values as integers, 0 = the legacy default stream). ``matmul`` and ``gemm``
+are convenience wrappers over ``gemm_f32_ex`` and ``gemm_f32_general`` for
+torch CUDA tensors.
 """
 
 from __future__ import annotations
@@ -32,6 +33,9 @@ NOALLOC_SCRATCH_BYTES = 40 * 1024 * 1024
 # gemm_f32_kernel
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC_TMA, KERNEL_TC_LSU = range(4)
 KERNELS = {"auto": KERNEL_AUTO, "simt": KERNEL_SIMT, "tc_tma": KERNEL_TC_TMA, "tc_lsu": KERNEL_TC_LSU}
+# gemm_f32_order, gemm_f32_op
+ROW_MAJOR, COL_MAJOR = 0, 1
+OP_N, OP_T = 0, 1
 
 
 class GemmError(RuntimeError):
@@ -64,6 +68,10 @@ def _load():
     lib.gemm_f32_host.restype = i32
     lib.gemm_f32_noalloc.argtypes = sig + [i32, p]
     lib.gemm_f32_noalloc.restype = i32
+    f32 = ctypes.c_float
+    lib.gemm_f32_general.argtypes = [i32, i32, i32, i64, i64, i64, f32, p, i64, p, i64, f32, p,
+                                     i64, i32, i32, p]
+    lib.gemm_f32_general.restype = i32
     lib.gemm_f32_status_string.argtypes = [i32]
     lib.gemm_f32_status_string.restype = ctypes.c_char_p
     lib.gemm_f32_poll_device_status.argtypes = [p]
@@ -101,6 +109,13 @@ def gemm_f32(M, N, K, A, lda, B, ldb, C, ldc, mode, stream=0) -> int:
 
 def gemm_f32_ex(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel, stream=0) -> int:
     return _load().gemm_f32_ex(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel, stream or None)
+
+
+def gemm_f32_general(order, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, mode,
+                     kernel=KERNEL_AUTO, stream=0) -> int:
+    """C = alpha * op(A) op(B) + beta * C (see include/gemm_f32.h)."""
+    return _load().gemm_f32_general(order, transa, transb, M, N, K, alpha, A, lda, B, ldb, beta,
+                                    C, ldc, mode, kernel, stream or None)
 
 
 def gemm_f32_select(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel=KERNEL_AUTO) -> int:
@@ -180,6 +195,43 @@ def matmul(a, b, mode="exact", out=None, kernel="auto", stream=None):
                          _ld(out), _mode(mode), _kernel(kernel), stream)
     if st != OK:
         raise GemmError(st)
+    return out
+
+
+def gemm(a, b, out=None, alpha=1.0, beta=0.0, transa=False, transb=False, mode="exact",
+         kernel="auto", stream=None):
+    """out = alpha * op(a) op(b) + beta * out for row-major float32 CUDA tensors.
+
+    ``a`` is stored M x K, or K x M with ``transa``; ``b`` K x N, or N x K
+    with ``transb``. ``out`` (M x N) is read only when beta != 0 and is
+    required then. Stream ordered on ``stream`` (default: torch's current
+    stream); returns ``out``.
+    """
+    import torch
+
+    _check_operand(a, "a")
+    _check_operand(b, "b")
+    m, k = (a.shape[1], a.shape[0]) if transa else tuple(a.shape)
+    k2, n = (b.shape[1], b.shape[0]) if transb else tuple(b.shape)
+    if k != k2:
+        raise ValueError(f"inner dimensions differ: op(a) is {m} x {k}, op(b) is {k2} x {n}")
+    if out is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs out")
+        out = torch.empty((m, n), dtype=torch.float32, device=a.device)
+    else:
+        _check_operand(out, "out")
+        if tuple(out.shape) != (m, n):
+            raise ValueError("out has the wrong shape")
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device).cuda_stream
+    with torch.cuda.device(a.device):
+        st = gemm_f32_general(ROW_MAJOR, OP_T if transa else OP_N, OP_T if transb else OP_N, m, n,
+                              k, float(alpha), a.data_ptr(), _ld(a), b.data_ptr(), _ld(b),
+                              float(beta), out.data_ptr(), _ld(out), _mode(mode), _kernel(kernel),
+                              stream)
+    if st != OK:
+        raise GemmError(st, "gemm_f32_general")
     return out
 
 

@@ -73,9 +73,15 @@ int validate(const GemmArgs &a, int mode, bool *noop) {
   *noop = false;
   if (mode != GEMM_F32_EXACT && mode != GEMM_F32_TF32 && mode != GEMM_F32_EXACT_SIMT)
     return gemm::kErrInvalidArg;
+  if ((a.opa != GEMM_OP_N && a.opa != GEMM_OP_T) || (a.opb != GEMM_OP_N && a.opb != GEMM_OP_T))
+    return gemm::kErrInvalidArg;
   if (a.M < 0 || a.N < 0 || a.K < 0) return gemm::kErrInvalidArg;
   if (a.M > kMaxDim || a.N > kMaxDim || a.K > kMaxDim) return gemm::kErrInvalidArg;
-  if (a.lda < (a.K > 1 ? a.K : 1) || a.ldb < (a.N > 1 ? a.N : 1) || a.ldc < (a.N > 1 ? a.N : 1))
+  // A is M x K (op N) or stored transposed, K x M (op T); B is K x N or N x K.
+  const int64_t a_rows = a.opa ? a.K : a.M, a_cols = a.opa ? a.M : a.K;
+  const int64_t b_rows = a.opb ? a.N : a.K, b_cols = a.opb ? a.K : a.N;
+  if (a.lda < (a_cols > 1 ? a_cols : 1) || a.ldb < (b_cols > 1 ? b_cols : 1) ||
+      a.ldc < (a.N > 1 ? a.N : 1))
     return gemm::kErrInvalidArg;
   if (a.lda > kMaxDim || a.ldb > kMaxDim || a.ldc > kMaxDim) return gemm::kErrInvalidArg;
   if (a.M == 0 || a.N == 0) {
@@ -89,9 +95,9 @@ int validate(const GemmArgs &a, int mode, bool *noop) {
       return gemm::kErrInvalidArg;
     uintptr_t c0, c1, x0, x1;
     matrix_range(a.C, a.M, a.N, a.ldc, &c0, &c1);
-    matrix_range(a.A, a.M, a.K, a.lda, &x0, &x1);
+    matrix_range(a.A, a_rows, a_cols, a.lda, &x0, &x1);
     if (ranges_overlap(c0, c1, x0, x1)) return gemm::kErrAlias;
-    matrix_range(a.B, a.K, a.N, a.ldb, &x0, &x1);
+    matrix_range(a.B, b_rows, b_cols, a.ldb, &x0, &x1);
     if (ranges_overlap(c0, c1, x0, x1)) return gemm::kErrAlias;
   }
   return gemm::kOk;
@@ -130,12 +136,19 @@ int run(const GemmArgs &a, int mode, int kernel, cudaStream_t stream) {
   int dev = 0, sms = 0;
   st = current_device(&dev, &sms);
   if (st != gemm::kOk) return st;
-  if (a.K == 0) {
-    // The empty sum: C = 0.
-    if (cudaMemset2DAsync(a.C, static_cast<size_t>(a.ldc) * 4, 0, static_cast<size_t>(a.N) * 4,
-                          static_cast<size_t>(a.M), stream) != cudaSuccess)
-      return gemm::kErrLaunch;
-    return gemm::kOk;
+  if (a.K == 0 || a.alpha == 0.0f) {
+    // No product term: C = beta * C, and C = 0 when beta == 0 (C not read).
+    if (a.beta == 0.0f) {
+      if (cudaMemset2DAsync(a.C, static_cast<size_t>(a.ldc) * 4, 0, static_cast<size_t>(a.N) * 4,
+                            static_cast<size_t>(a.M), stream) != cudaSuccess)
+        return gemm::kErrLaunch;
+      return gemm::kOk;
+    }
+    // The FP32 kernel over an empty k range stores 0 * 0 + beta * C.
+    GemmArgs s = a;
+    s.K = 0;
+    s.alpha = 0.0f;
+    return gemm::simt_launch(s, stream);
   }
   switch (k) {
     case GEMM_KERNEL_SIMT:
@@ -165,6 +178,28 @@ extern "C" {
 int gemm_f32_ex(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
                 int64_t ldb, float *C, int64_t ldc, int mode, int kernel, void *stream) {
   const GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
+  return run(a, mode, kernel, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_f32_general(int order, int transa, int transb, int64_t M, int64_t N, int64_t K,
+                     float alpha, const float *A, int64_t lda, const float *B, int64_t ldb,
+                     float beta, float *C, int64_t ldc, int mode, int kernel, void *stream) {
+  GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
+  if (order == GEMM_ROW_MAJOR) {
+    a.opa = transa;
+    a.opb = transb;
+  } else if (order == GEMM_COL_MAJOR) {
+    // A column-major matrix is the row-major storage of its transpose, so
+    // C = op(A) op(B) in column-major order is C^T = op(B)^T op(A)^T in
+    // row-major order: swap the operands and their flags and exchange M, N.
+    a = GemmArgs{N, M, K, B, ldb, A, lda, C, ldc};
+    a.opa = transb;
+    a.opb = transa;
+  } else {
+    return GEMM_ERR_INVALID_ARG;
+  }
+  a.alpha = alpha;
+  a.beta = beta;
   return run(a, mode, kernel, static_cast<cudaStream_t>(stream));
 }
 

@@ -7,6 +7,9 @@
 
 namespace gemm {
 
+// C = alpha * op(A) op(B) + beta * C, row-major. opa = 0: A is M x K (pitch
+// lda); opa = 1: A is stored transposed, K x M. opb = 0: B is K x N (pitch
+// ldb); opb = 1: B is stored transposed, N x K.
 struct GemmArgs {
   int64_t M, N, K;
   const float *A;
@@ -15,6 +18,10 @@ struct GemmArgs {
   int64_t ldb;
   float *C;
   int64_t ldc;
+  int opb = 0;
+  int opa = 0;
+  float alpha = 1.0f;
+  float beta = 0.0f;
 };
 
 // Status codes (values of gemm_f32_status).

@@ -20,7 +20,12 @@
 //     Optimization Guide".
 //
 // Each output is accumulated by fused multiply-adds over k in increasing
-// order in fp32, so |C - AB| <= K 2^-24 |A||B| element-wise.
+// order in fp32, so |C - AB| <= K 2^-24 |A||B| element-wise. The general form
+// C = alpha * A op(B) + beta * C scales the sum once at the store (C is read
+// only when beta != 0). op(B) = B, or B stored transposed (N x K, the vec4
+// transposed-B storage of the subgroups page, section 7), which is staged
+// through the same transposing stores as A; op(A) = A, or A stored
+// transposed (K x M), whose rows of m are stored into the k-major tile as is.
 
 #include <cuda_runtime.h>
 
@@ -45,13 +50,14 @@ struct SimtParams {
   long long ldb;
   float *C;
   long long ldc;
+  float alpha, beta;
   int tiles_m, tiles_n;
 };
 
-template <bool VEC>
+template <bool VEC, bool OPB, bool OPA>
 __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams p) {
   __shared__ __align__(16) float As[2][kSliceK][kApad];
-  __shared__ __align__(16) float Bs[2][kSliceK][kTile];
+  __shared__ __align__(16) float Bs[2][kSliceK][kApad];
 
   // Grouped raster: kGroup tile-rows sweep all tile-columns before moving on.
   const int bid = blockIdx.x;
@@ -66,10 +72,14 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
   const int tid = threadIdx.x;
   const int tx = tid & 15, ty = tid >> 4;
 
-  // Load assignment: A row (tid / 2), k-offset (tid % 2) * 4;
-  // B k-row (tid / 32), column (tid % 32) * 4.
-  const int a_row = tid >> 1, a_k = (tid & 1) * 4;
-  const int b_k = tid >> 5, b_col = (tid & 31) * 4;
+  // Load assignment: A row (tid / 2), k-offset (tid % 2) * 4 (A stored
+  // transposed: k-row tid / 32, rows (tid % 32) * 4 ...); B k-row (tid / 32),
+  // column (tid % 32) * 4, or for B stored transposed, like A: n-row
+  // (tid / 2), k-offset (tid % 2) * 4.
+  const int a_row = OPA ? (tid & 31) * 4 : tid >> 1;
+  const int a_k = OPA ? tid >> 5 : (tid & 1) * 4;
+  const int b_k = OPB ? (tid & 1) * 4 : tid >> 5;
+  const int b_col = OPB ? tid >> 1 : (tid & 31) * 4;
   const int ga_row = m0 + a_row;
   const int gb_col = n0 + b_col;
 
@@ -85,31 +95,60 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
     const int ka = k0 + a_k;
     const int kb = k0 + b_k;
     if (VEC) {
-      // K % 4 == 0 and N % 4 == 0: a 4-wide group is wholly inside or outside.
+      // Contiguous extents are multiples of 4: a 4-wide group is wholly
+      // inside or outside.
       float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
-      if (ga_row < p.M && ka < p.K)
+      if (OPA) {
+        if (ka < p.K && ga_row < p.M)
+          va = __ldg(reinterpret_cast<const float4 *>(p.A + static_cast<long long>(ka) * p.lda + ga_row));
+      } else if (ga_row < p.M && ka < p.K) {
         va = __ldg(reinterpret_cast<const float4 *>(p.A + static_cast<long long>(ga_row) * p.lda + ka));
-      if (kb < p.K && gb_col < p.N)
+      }
+      if (OPB) {
+        if (gb_col < p.N && kb < p.K)
+          vb = __ldg(reinterpret_cast<const float4 *>(p.B + static_cast<long long>(gb_col) * p.ldb + kb));
+      } else if (kb < p.K && gb_col < p.N) {
         vb = __ldg(reinterpret_cast<const float4 *>(p.B + static_cast<long long>(kb) * p.ldb + gb_col));
+      }
       a_reg[0] = va.x; a_reg[1] = va.y; a_reg[2] = va.z; a_reg[3] = va.w;
       b_reg[0] = vb.x; b_reg[1] = vb.y; b_reg[2] = vb.z; b_reg[3] = vb.w;
     } else {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        a_reg[j] = (ga_row < p.M && ka + j < p.K)
-                       ? __ldg(p.A + static_cast<long long>(ga_row) * p.lda + ka + j)
-                       : 0.0f;
-        b_reg[j] = (kb < p.K && gb_col + j < p.N)
-                       ? __ldg(p.B + static_cast<long long>(kb) * p.ldb + gb_col + j)
-                       : 0.0f;
+        if (OPA)
+          a_reg[j] = (ka < p.K && ga_row + j < p.M)
+                         ? __ldg(p.A + static_cast<long long>(ka) * p.lda + ga_row + j)
+                         : 0.0f;
+        else
+          a_reg[j] = (ga_row < p.M && ka + j < p.K)
+                         ? __ldg(p.A + static_cast<long long>(ga_row) * p.lda + ka + j)
+                         : 0.0f;
+        if (OPB)
+          b_reg[j] = (gb_col < p.N && kb + j < p.K)
+                         ? __ldg(p.B + static_cast<long long>(gb_col) * p.ldb + kb + j)
+                         : 0.0f;
+        else
+          b_reg[j] = (kb < p.K && gb_col + j < p.N)
+                         ? __ldg(p.B + static_cast<long long>(kb) * p.ldb + gb_col + j)
+                         : 0.0f;
       }
     }
   };
   auto store_slice = [&](int buf) {
+    if (OPA) {
+      *reinterpret_cast<float4 *>(&As[buf][a_k][a_row]) =
+          make_float4(a_reg[0], a_reg[1], a_reg[2], a_reg[3]);
+    } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) As[buf][a_k + j][a_row] = a_reg[j];
-    *reinterpret_cast<float4 *>(&Bs[buf][b_k][b_col]) =
-        make_float4(b_reg[0], b_reg[1], b_reg[2], b_reg[3]);
+      for (int j = 0; j < 4; ++j) As[buf][a_k + j][a_row] = a_reg[j];
+    }
+    if (OPB) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) Bs[buf][b_k + j][b_col] = b_reg[j];
+    } else {
+      *reinterpret_cast<float4 *>(&Bs[buf][b_k][b_col]) =
+          make_float4(b_reg[0], b_reg[1], b_reg[2], b_reg[3]);
+    }
   };
 
   const int num_slices = (p.K + kSliceK - 1) / kSliceK;
@@ -146,14 +185,28 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int col = n0 + h * 64 + tx * 4;
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = p.alpha * acc[i][h * 4 + j];
       if (VEC) {
-        if (col < p.N)
-          *reinterpret_cast<float4 *>(crow + col) =
-              make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
+        if (col < p.N) {
+          float4 *dst = reinterpret_cast<float4 *>(crow + col);
+          if (p.beta != 0.0f) {
+            const float4 c = *dst;
+            v[0] += p.beta * c.x;
+            v[1] += p.beta * c.y;
+            v[2] += p.beta * c.z;
+            v[3] += p.beta * c.w;
+          }
+          *dst = make_float4(v[0], v[1], v[2], v[3]);
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (col + j < p.N) crow[col + j] = acc[i][h * 4 + j];
+          if (col + j < p.N) {
+            if (p.beta != 0.0f) v[j] += p.beta * crow[col + j];
+            crow[col + j] = v[j];
+          }
       }
     }
   }
@@ -172,18 +225,33 @@ int simt_launch(const GemmArgs &a, cudaStream_t stream) {
   p.ldb = a.ldb;
   p.C = a.C;
   p.ldc = a.ldc;
+  p.alpha = a.alpha;
+  p.beta = a.beta;
   p.tiles_m = static_cast<int>((a.M + kTile - 1) / kTile);
   p.tiles_n = static_cast<int>((a.N + kTile - 1) / kTile);
   const long long blocks = static_cast<long long>(p.tiles_m) * p.tiles_n;
   if (blocks > 0x7fffffffLL) return kErrInvalidArg;
+  // 128-bit accesses: every pointer 16-byte aligned, every pitch and every
+  // contiguous extent (A: K, or M when stored transposed; B: N, or K; C: N) a
+  // multiple of 4, so a 4-wide group is wholly inside or outside.
+  const int64_t a_inner = a.opa ? a.M : a.K, b_inner = a.opb ? a.K : a.N;
   const bool vec = reinterpret_cast<uintptr_t>(a.A) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(a.B) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(a.C) % 16 == 0 && a.lda % 4 == 0 &&
-                   a.ldb % 4 == 0 && a.ldc % 4 == 0 && a.K % 4 == 0 && a.N % 4 == 0;
-  if (vec)
-    simt_gemm_kernel<true><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
-  else
-    simt_gemm_kernel<false><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(p);
+                   a.ldb % 4 == 0 && a.ldc % 4 == 0 && a_inner % 4 == 0 && b_inner % 4 == 0 &&
+                   a.N % 4 == 0;
+  const dim3 grid(static_cast<unsigned>(blocks));
+  const int variant = (vec ? 4 : 0) | (a.opb ? 2 : 0) | (a.opa ? 1 : 0);
+  switch (variant) {
+    case 0: simt_gemm_kernel<false, false, false><<<grid, kThreads, 0, stream>>>(p); break;
+    case 1: simt_gemm_kernel<false, false, true><<<grid, kThreads, 0, stream>>>(p); break;
+    case 2: simt_gemm_kernel<false, true, false><<<grid, kThreads, 0, stream>>>(p); break;
+    case 3: simt_gemm_kernel<false, true, true><<<grid, kThreads, 0, stream>>>(p); break;
+    case 4: simt_gemm_kernel<true, false, false><<<grid, kThreads, 0, stream>>>(p); break;
+    case 5: simt_gemm_kernel<true, false, true><<<grid, kThreads, 0, stream>>>(p); break;
+    case 6: simt_gemm_kernel<true, true, false><<<grid, kThreads, 0, stream>>>(p); break;
+    default: simt_gemm_kernel<true, true, true><<<grid, kThreads, 0, stream>>>(p); break;
+  }
   return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 

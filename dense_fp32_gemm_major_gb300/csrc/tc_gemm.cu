@@ -67,8 +67,8 @@ constexpr int kTN = 128;        // columns of C per tile (MMA M = TMEM lanes)
 constexpr int kUmmaK = 8;       // K per tcgen05.mma of kind::tf32
 constexpr int kGroupM = 8;      // m-blocks per raster group
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 0;    // D: columns [0, 256)
-constexpr uint32_t kBtCol = 256;   // B^T stage buffers from column 256
+constexpr uint32_t kAccCol = 0;    // D: columns [0, 256) (and [256, 512) when double-buffered)
+constexpr uint32_t kBtCol = 256;   // B^T stage buffers from column 256 (B stored K x N)
 
 struct TcParams {
   int M, N, K;
@@ -93,6 +93,7 @@ struct TcParams {
   // the only units that can be parts of a split tile.
   float *sk_partials;
   unsigned *sk_counters;   // split tiles: parts finished so far per (tile, rank), zeroed before launch
+  float alpha, beta;       // C = alpha * A op(B) + beta * C (beta == 0: C is not read)
   unsigned long long timeout_ns;
 };
 
@@ -119,36 +120,49 @@ __device__ __forceinline__ int split_slot(const TcParams &p, int s, int part) {
 // 64 bytes, 64-byte swizzle). Either way a row of the A tile is one swizzle
 // span, 8-row groups are the swizzle atom, and a k-step of 8 advances the
 // descriptor by 32 bytes along the row.
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL>
+// OPB = false: B is stored K x N (N contiguous); its tile goes through
+// registers into TMEM as B^T. OPB = true: B is stored transposed, N x K (K
+// contiguous), so its tile is K-major like A's and feeds the MMA from shared
+// memory directly; TMEM then holds only accumulators, two of them.
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB>
 struct TcConfig {
   static_assert(BK == 16 || BK == 32, "BK");
   static_assert(CL == 1 || (CL == 2 && !LSU), "clusters pair TMA-fed CTAs only");
   static constexpr int kAPartRows = kTM / CL;                    // A rows each CTA loads
   static constexpr int kAPartBytes = kAPartRows * BK * 4;
-  static constexpr int kRowBytes = BK * 4;                       // one row of the A tile
+  static constexpr int kRowBytes = BK * 4;                       // one K-major tile row
   static constexpr int kAtomBytes = 8 * kRowBytes;               // 8-row swizzle atom (SBO)
   static constexpr uint32_t kLayout = BK == 32 ? 2u : 4u;        // 128- or 64-byte swizzle
   static constexpr int kABytes = kTM * BK * 4;                   // A tile, K-major, swizzled
-  static constexpr int kBBytes = LSU ? 0 : BK * kTN * 4;         // B tile, row-major (TMA)
-  static constexpr int kALoBytes = EXACT ? kABytes : 0;          // 3xTF32 lo tile of A
-  static constexpr int kStageBytes = kABytes + kBBytes + kALoBytes;
+  // B tile: row-major BK x 128 for TMA (OPB = false; LSU keeps none), or
+  // K-major 128 x BK like A (OPB = true).
+  static constexpr int kBBytes = (LSU && !OPB) ? 0 : BK * kTN * 4;
+  // 3xTF32 lo tiles follow the hi (or raw) tiles at kLoOffset, same layout.
+  static constexpr int kLoOffset = kABytes + kBBytes;
+  static constexpr int kLoBytes = EXACT ? (OPB ? kABytes + kBBytes : kABytes) : 0;
+  static constexpr int kStageBytes = kABytes + kBBytes + kLoBytes;
   static constexpr int kBOffset = kABytes;
-  static constexpr int kALoOffset = kABytes + kBBytes;
+  static constexpr int kALoOffset = kLoOffset;
+  static constexpr int kBLoOffset = kLoOffset + kABytes;         // OPB && EXACT
   static constexpr int kTileBytes = STAGES * kStageBytes;
-  static constexpr uint32_t kBtColsPerStage = EXACT ? 2 * BK : BK;  // hi (+ lo)
+  static constexpr uint32_t kBtColsPerStage = OPB ? 0 : (EXACT ? 2 * BK : BK);  // hi (+ lo)
+  static constexpr int kAccBufs = OPB ? 2 : 1;                   // TMEM accumulators
   static constexpr int kProdWarps = LSU ? 4 : 1;
   static constexpr int kMmaWarp = kProdWarps;
   static constexpr int kEpiWarp0 = kMmaWarp + 1;
   // Transform warps, a multiple of 4 (whole TMEM lane quadrants). The 3xTF32
   // split is the most work per stage: 16 warps keep it ahead of the MMAs.
-  static constexpr int kXformWarps = LSU ? 0 : (EXACT ? 16 : 8);
+  // With B transposed and one TF32 pass there is nothing to transform.
+  static constexpr int kXformWarps = LSU ? 0 : (OPB ? (EXACT ? 16 : 0) : (EXACT ? 16 : 8));
   static constexpr int kXformParts = kXformWarps > 0 ? kXformWarps / 4 : 1;  // per lane quadrant
   static constexpr int kXformWarp0 = kEpiWarp0 + 4;
   static constexpr int kThreads = 32 * (kXformWarp0 + kXformWarps);
   static constexpr uint32_t kIdesc = idesc_tf32(kTN, kTM);
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(kXformWarps % 4 == 0 && BK % kXformParts == 0, "transform partition");
-  static_assert(kBtCol + STAGES * kBtColsPerStage <= kTmemCols, "TMEM budget");
+  static_assert(OPB ? kAccBufs * kTM <= static_cast<int>(kTmemCols)
+                    : kBtCol + STAGES * kBtColsPerStage <= kTmemCols,
+                "TMEM budget");
 };
 
 template <int STAGES>
@@ -156,8 +170,8 @@ struct alignas(8) TcShared {
   uint64_t full[STAGES];   // stage loaded (TMA bytes, or the LSU producer warps)
   uint64_t ready[STAGES];  // B^T in TMEM (and A split) by the transform warps
   uint64_t empty[STAGES];  // stage consumed by the MMAs (tcgen05.commit)
-  uint64_t acc_full;       // accumulator complete (tcgen05.commit)
-  uint64_t acc_empty;      // accumulator drained by the epilogue warps
+  uint64_t acc_full[2];    // accumulator complete (tcgen05.commit)
+  uint64_t acc_empty[2];   // accumulator drained by the epilogue warps
   uint64_t drain;          // every MMA of this CTA has completed
   uint32_t tmem_base;
   int abort;
@@ -236,6 +250,12 @@ struct UnitIter {
   }
 };
 
+// alpha * acc + beta * C (C read only when beta != 0).
+__device__ __forceinline__ float scale_out(const TcParams &p, float acc, const float *c) {
+  const float v = p.alpha * acc;
+  return p.beta != 0.0f ? v + p.beta * *c : v;
+}
+
 // Sum the partial tiles of split tile `sk_tile` in part order and store the
 // result to C. Run by `nthreads` threads of the CTA that finished last: the
 // four epilogue warps, or every warp of the CTA for its final unit. The tile
@@ -284,12 +304,21 @@ __device__ __noinline__ void epilogue_fixup(const TcParams &p, int sk_tile, uint
       if (gm >= p.M) continue;
       float *dst = p.C + static_cast<long long>(gm) * p.ldc + gn;
       if (vec_ok && gn + 3 < p.N) {
-        *reinterpret_cast<float4 *>(dst) = acc[j];
+        float4 v = make_float4(p.alpha * acc[j].x, p.alpha * acc[j].y, p.alpha * acc[j].z,
+                               p.alpha * acc[j].w);
+        if (p.beta != 0.0f) {
+          const float4 c = *reinterpret_cast<const float4 *>(dst);
+          v.x += p.beta * c.x;
+          v.y += p.beta * c.y;
+          v.z += p.beta * c.z;
+          v.w += p.beta * c.w;
+        }
+        *reinterpret_cast<float4 *>(dst) = v;
       } else {
         const float e[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          if (gn + i < p.N) dst[i] = e[i];
+          if (gn + i < p.N) dst[i] = scale_out(p, e[i], dst + i);
       }
     }
   }
@@ -366,11 +395,83 @@ __device__ __forceinline__ void stage_a_value(uint8_t *stage, int lo_offset, uin
   }
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL>
-__global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads, 1)
+// Plain-load staging of `rows` rows (r0 + row, row < rows) x BK k (k0 + k) of
+// a row-major matrix with leading dimension ld into a K-major swizzled tile
+// (zero outside [0, limit_r) x [0, K)); with EXACT the hi part goes to the
+// tile and the lo part lo_offset bytes further. Four producer warps, warp w
+// taking rows w * (32 / BK) + ..., one BK-wide row segment per 32 / BK lanes.
+template <int BK, bool EXACT, int ROWS>
+__device__ __forceinline__ void stage_rows_lsu(uint8_t *tile, int lo_offset, const float *src,
+                                               long long ld, int r0, int limit_r, int k0, int K,
+                                               uint32_t warp, uint32_t lane, int row_bytes) {
+  constexpr int kRowsPerInstr = 32 / BK;
+  constexpr int kSteps = ROWS / (4 * kRowsPerInstr);
+  constexpr int kChunk = kSteps < 32 ? kSteps : 32;  // loads in flight per lane
+  static_assert(kSteps % kChunk == 0, "rows per producer pass");
+  const int k_in = lane % BK;
+  const int r_in = lane / BK;
+  const int gk = k0 + k_in;
+#pragma unroll 1
+  for (int chunk = 0; chunk < kSteps / kChunk; ++chunk) {
+    float v[kChunk];
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const int row = (chunk * kChunk + i) * 4 * kRowsPerInstr + warp * kRowsPerInstr + r_in;
+      const int gr = r0 + row;
+      v[i] = (gr < limit_r && gk < K) ? __ldg(src + static_cast<long long>(gr) * ld + gk) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const int row = (chunk * kChunk + i) * 4 * kRowsPerInstr + warp * kRowsPerInstr + r_in;
+      stage_a_value<EXACT>(tile, lo_offset, swizzle_a<BK>(row * row_bytes + k_in * 4), v[i]);
+    }
+  }
+}
+
+// Plain-load staging of the same tile from a matrix stored transposed: element
+// (row r, k) at src[k * ld + r] (rows contiguous). Lane l covers rows
+// 8g + l % 8 and k 4h + l / 8 of an 8 x 4 block, so one load instruction
+// reads four fully used 32-byte segments and one store instruction hits 32
+// distinct banks of the swizzled tile (eight rows give eight distinct XOR
+// patterns, four k the four words of a 16-byte chunk). Four producer warps
+// take the blocks in turn.
+template <int BK, bool EXACT, int ROWS>
+__device__ __forceinline__ void stage_cols_lsu(uint8_t *tile, int lo_offset, const float *src,
+                                               long long ld, int r0, int limit_r, int k0, int K,
+                                               uint32_t warp, uint32_t lane, int row_bytes) {
+  constexpr int kRowGroups = ROWS / 8;
+  constexpr int kPerWarp = kRowGroups * (BK / 4) / 4;
+  constexpr int kChunk = kPerWarp < 16 ? kPerWarp : 16;  // loads in flight per lane
+  static_assert(kPerWarp % kChunk == 0, "blocks per producer pass");
+  const int r_in = static_cast<int>(lane & 7u);
+  const int k_in = static_cast<int>(lane >> 3);
+#pragma unroll 1
+  for (int chunk = 0; chunk < kPerWarp / kChunk; ++chunk) {
+    float v[kChunk];
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const int g = (chunk * kChunk + i) * 4 + static_cast<int>(warp);
+      const int row = (g % kRowGroups) * 8 + r_in;
+      const int k = (g / kRowGroups) * 4 + k_in;
+      const int gr = r0 + row, gk = k0 + k;
+      v[i] = (gr < limit_r && gk < K) ? __ldg(src + static_cast<long long>(gk) * ld + gr) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const int g = (chunk * kChunk + i) * 4 + static_cast<int>(warp);
+      const int row = (g % kRowGroups) * 8 + r_in;
+      const int k = (g / kRowGroups) * 4 + k_in;
+      stage_a_value<EXACT>(tile, lo_offset, swizzle_a<BK>(row * row_bytes + k * 4), v[i]);
+    }
+  }
+}
+
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA>
+__global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
-  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL>;
+  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>;
+  static_assert(!OPA || LSU, "A stored transposed is staged by the LSU producer");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -387,8 +488,10 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
       mbar_init(&sh->ready[s], Cfg::kXformWarps > 0 ? Cfg::kXformWarps : 1);
       mbar_init(&sh->empty[s], CL);  // the MMAs of every CTA that writes this stage
     }
-    mbar_init(&sh->acc_full, 1);
-    mbar_init(&sh->acc_empty, 4);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh->acc_full[a], 1);
+      mbar_init(&sh->acc_empty[a], 4);
+    }
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     sh->fix_tile = -1;
@@ -436,7 +539,10 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
                                   static_cast<uint16_t>((1u << CL) - 1));
           else
             tma_load_2d(st, &tmap_a, &sh->full[stage], kb * BK, mb * kTM);
-          tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], nb * kTN, kb * BK);
+          if (OPB)
+            tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], kb * BK, nb * kTN);
+          else
+            tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], nb * kTN, kb * BK);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -472,31 +578,17 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
         tc_fence_after_sync();
         uint8_t *st = tiles + stage * Cfg::kStageBytes;
         const int k0 = kb * BK;
-        // A: one warp instruction covers 32 / BK rows of BK consecutive k; the
-        // four producer warps interleave, so kTM rows take kASteps instructions.
-        constexpr int kRowsPerInstr = 32 / BK;
-        constexpr int kASteps = kTM / (4 * kRowsPerInstr);
-        const int k_in = lane % BK;
-        const int r_in = lane / BK;
-        const int gk = k0 + k_in;
-#pragma unroll 1
-        for (int chunk = 0; chunk < kASteps / 32; ++chunk) {
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int row = (chunk * 32 + i) * 4 * kRowsPerInstr + warp * kRowsPerInstr + r_in;
-            const int gm = m0 + row;
-            v[i] = (gm < p.M && gk < p.K) ? __ldg(p.A + static_cast<long long>(gm) * p.lda + gk)
-                                          : 0.0f;
-          }
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int row = (chunk * 32 + i) * 4 * kRowsPerInstr + warp * kRowsPerInstr + r_in;
-            stage_a_value<EXACT>(st, Cfg::kALoOffset,
-                                 swizzle_a<BK>(row * Cfg::kRowBytes + k_in * 4), v[i]);
-          }
-        }
-        {
+        if (OPA)
+          stage_cols_lsu<BK, EXACT, kTM>(st, Cfg::kALoOffset, p.A, p.lda, m0, p.M, k0, p.K, warp,
+                                         lane, Cfg::kRowBytes);
+        else
+          stage_rows_lsu<BK, EXACT, kTM>(st, Cfg::kALoOffset, p.A, p.lda, m0, p.M, k0, p.K, warp,
+                                         lane, Cfg::kRowBytes);
+        if (OPB) {
+          // B stored N x K: its tile is staged K-major, like A's.
+          stage_rows_lsu<BK, EXACT, kTN>(st + Cfg::kBOffset, Cfg::kBLoOffset - Cfg::kBOffset, p.B,
+                                         p.ldb, n0, p.N, k0, p.K, warp, lane, Cfg::kRowBytes);
+        } else {
           const int gn = n0 + quad * 32 + lane;
           float v[BK];
 #pragma unroll
@@ -522,20 +614,20 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
   } else if (warp == Cfg::kMmaWarp) {
     // -------------------------------------------------------------- MMA --
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, acc_phase = 0;
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      const uint32_t d_tmem = tmem + kAccCol;
       UnitIter it(p);
       WorkUnit u;
       while (ok && it.next(p, u)) {
-        if (!mbar_wait_bounded(&sh->acc_empty, acc_phase ^ 1, p.timeout_ns, abort,
+        if (!mbar_wait_bounded(&sh->acc_empty[acc], acc_phase ^ 1, p.timeout_ns, abort,
                                &g_tc_status)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + kAccCol + acc * kTM;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          uint64_t *in_bar = LSU ? &sh->full[stage] : &sh->ready[stage];
+          uint64_t *in_bar = Cfg::kXformWarps > 0 ? &sh->ready[stage] : &sh->full[stage];
           if (!mbar_wait_bounded(in_bar, phase, p.timeout_ns, abort, &g_tc_status)) {
             ok = false;
             break;
@@ -549,7 +641,22 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
             // 8-row groups (the swizzle atom) are kAtomBytes apart.
             const uint64_t da = smem_desc(a_hi + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
             const uint32_t accumulate = (kb != u.kb0 || kk != 0) ? 1u : 0u;
-            if (EXACT) {
+            if (OPB) {
+              // B^T rows straight from the K-major B tile in shared memory.
+              const uint64_t db = smem_desc(a_hi + Cfg::kBOffset + kk * 32, 16, Cfg::kAtomBytes,
+                                            Cfg::kLayout);
+              if (EXACT) {
+                const uint64_t da_lo = smem_desc(a_hi + Cfg::kALoOffset + kk * 32, 16,
+                                                 Cfg::kAtomBytes, Cfg::kLayout);
+                const uint64_t db_lo = smem_desc(a_hi + Cfg::kBLoOffset + kk * 32, 16,
+                                                 Cfg::kAtomBytes, Cfg::kLayout);
+                mma_tf32(d_tmem, db_lo, da, Cfg::kIdesc, accumulate);
+                mma_tf32(d_tmem, db, da_lo, Cfg::kIdesc, 1);
+                mma_tf32(d_tmem, db, da, Cfg::kIdesc, 1);
+              } else {
+                mma_tf32(d_tmem, db, da, Cfg::kIdesc, accumulate);
+              }
+            } else if (EXACT) {
               const uint64_t da_lo =
                   smem_desc(a_hi + Cfg::kALoOffset + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
               mma_tf32_ts(d_tmem, bt_hi + BK + kk * kUmmaK, da, Cfg::kIdesc, accumulate);
@@ -569,8 +676,11 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
           }
         }
         if (!ok) break;
-        mma_commit(&sh->acc_full);
-        acc_phase ^= 1;
+        mma_commit(&sh->acc_full[acc]);
+        if (++acc == Cfg::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
       // Every MMA this thread issued completes before TMEM is released.
       mma_commit(&sh->drain);
@@ -580,7 +690,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
   } else if (warp >= Cfg::kEpiWarp0 && warp < Cfg::kEpiWarp0 + 4) {
     // --------------------------------------------------------- epilogue --
     const uint32_t quad = warp & 3;  // TMEM lanes (columns of C) this warp may read
-    uint32_t acc_phase = 0;
+    uint32_t acc = 0, acc_phase = 0;
     UnitIter it(p);
     WorkUnit u;
     while (it.next(p, u)) {
@@ -588,12 +698,12 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
       tile_coords(p, u.tile, rank, mb, nb);
       // The four epilogue warps continue or give up together: the split-tile
       // path below synchronises them with named barriers.
-      if (!named_barrier_and(1, 128, warp_wait(&sh->acc_full, acc_phase, p, abort))) break;
+      if (!named_barrier_and(1, 128, warp_wait(&sh->acc_full[acc], acc_phase, p, abort))) break;
       tc_fence_after_sync();
       const int n_loc = quad * 32 + lane;
       const int gn = nb * kTN + n_loc;
       const bool n_ok = gn < p.N;
-      const uint32_t t_lane = tmem + ((quad * 32) << 16) + kAccCol;
+      const uint32_t t_lane = tmem + ((quad * 32) << 16) + kAccCol + acc * kTM;
       if (u.nparts == 1) {
         // Whole tile: straight to C.
 #pragma unroll 1
@@ -606,20 +716,29 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
           float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
           const int rows = min(32, p.M - gm0);
           if (n_ok) {
-            if (rows == 32) {
+            if (p.alpha == 1.0f && p.beta == 0.0f) {
+              if (rows == 32) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+                for (int j = 0; j < 32; ++j)
+                  dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j < rows) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+              }
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (j < rows) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+                if (j < rows) {
+                  float *d = dst + static_cast<long long>(j) * p.ldc;
+                  *d = scale_out(p, __uint_as_float(r[j]), d);
+                }
             }
           }
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->acc_empty);
+        if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
       } else {
         // Split tile: write this part's partial sums ([m][n], pitch kTN) to
         // its slot and free the accumulator; the last part to finish sums all
@@ -639,7 +758,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->acc_empty);
+        if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
         __threadfence();
         named_barrier_sync(1, 128);
         if (warp == Cfg::kEpiWarp0 && lane == 0)
@@ -663,7 +782,10 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
         }
         named_barrier_sync(1, 128);  // sk_last is reused by the next split tile
       }
-      acc_phase ^= 1;
+      if (++acc == Cfg::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
     }
   } else if (Cfg::kXformWarps > 0 && warp >= Cfg::kXformWarp0) {
     // -------------------------------------------- transform (TMA variant) --
@@ -684,7 +806,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
         }
         tc_fence_after_sync();
         uint8_t *st = tiles + stage * Cfg::kStageBytes;
-        {
+        if (!OPB) {
           // B tile is row-major BK k x 128 n (512-byte rows); this thread's
           // column n = 32 quad + lane becomes TMEM lane n.
           constexpr int kW = BK / Cfg::kXformParts;
@@ -698,10 +820,13 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL>::kThreads
           bt_to_tmem<kW, EXACT>(col, col + BK, v);
         }
         if (EXACT) {
+          // Split the K-major tiles (A, and B when it is stored transposed):
+          // hi in place, lo kLoOffset bytes further.
+          constexpr int kSplitVecs = (OPB ? Cfg::kABytes + Cfg::kBBytes : Cfg::kABytes) / 16;
           float4 *raw = reinterpret_cast<float4 *>(st);
-          float4 *lo = reinterpret_cast<float4 *>(st + Cfg::kALoOffset);
+          float4 *lo = reinterpret_cast<float4 *>(st + Cfg::kLoOffset);
 #pragma unroll 4
-          for (int i = xt; i < Cfg::kABytes / 16; i += 32 * Cfg::kXformWarps) {
+          for (int i = xt; i < kSplitVecs; i += 32 * Cfg::kXformWarps) {
             const float4 x = raw[i];
             float4 h, l;
             h.x = round_tf32(x.x);
@@ -892,9 +1017,9 @@ Schedule make_schedule(int tiles, int kb, int sms, int min_chunk) {
 }
 
 // Everything a launch needs except the stream-K workspace.
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL>
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false>
 struct LaunchPlan {
-  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL>;
+  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>;
   TcParams p;
   Schedule sch;
   CUtensorMap map_a, map_b;
@@ -902,7 +1027,7 @@ struct LaunchPlan {
   size_t counter_bytes = 0, partial_bytes = 0;  // workspace, 0 if no tile is split
 
   int prepare(const GemmArgs &a, int sm_count) {
-    auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL>;
+    auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA>;
     smem_bytes = Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kErrLaunch;
@@ -923,8 +1048,12 @@ struct LaunchPlan {
       const CUtensorMapSwizzle sw_a =
           BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
       if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, Cfg::kAPartRows, sw_a, &map_a)) return kErrLaunch;
-      if (!get_map(a.B, a.N, a.K, a.ldb * 4, kTN, BK, CU_TENSOR_MAP_SWIZZLE_NONE, &map_b))
+      if (OPB) {
+        // B stored N x K: a K-major BK x 128 box with A's swizzle.
+        if (!get_map(a.B, a.K, a.N, a.ldb * 4, BK, kTN, sw_a, &map_b)) return kErrLaunch;
+      } else if (!get_map(a.B, a.N, a.K, a.ldb * 4, kTN, BK, CU_TENSOR_MAP_SWIZZLE_NONE, &map_b)) {
         return kErrLaunch;
+      }
     }
     p.M = static_cast<int>(a.M);
     p.N = static_cast<int>(a.N);
@@ -935,6 +1064,8 @@ struct LaunchPlan {
     p.ldb = a.ldb;
     p.C = a.C;
     p.ldc = a.ldc;
+    p.alpha = a.alpha;
+    p.beta = a.beta;
     p.num_m_blocks = static_cast<int>((a.M + kTM - 1) / kTM);
     p.num_n_blocks = static_cast<int>((a.N + kTN - 1) / kTN);
     p.num_k_blocks = static_cast<int>((a.K + BK - 1) / BK);
@@ -1002,7 +1133,8 @@ struct LaunchPlan {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = CL > 1 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL>, map_a, map_b, p) ==
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA>, map_a,
+                              map_b, p) ==
                    cudaSuccess
                ? kOk
                : kErrLaunch;
@@ -1039,9 +1171,9 @@ int workspace_pool(int dev, cudaMemPool_t *out) {
   return kOk;
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL>
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false>
 int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
-  LaunchPlan<BK, STAGES, EXACT, LSU, CL> plan;
+  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA> plan;
   int st = plan.prepare(a, sm_count);
   if (st != kOk) return st;
   // Split tiles need a workspace: partial tiles and one counter per split
@@ -1070,20 +1202,41 @@ int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
 }  // namespace
 
 bool tc_tma_legal(const GemmArgs &a) {
-  return reinterpret_cast<uintptr_t>(a.A) % 16 == 0 && reinterpret_cast<uintptr_t>(a.B) % 16 == 0 &&
-         a.lda % 4 == 0 && a.ldb % 4 == 0;
+  // A stored transposed (K x M) is only staged by the LSU producer.
+  return !a.opa && reinterpret_cast<uintptr_t>(a.A) % 16 == 0 &&
+         reinterpret_cast<uintptr_t>(a.B) % 16 == 0 && a.lda % 4 == 0 && a.ldb % 4 == 0;
 }
 
 int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream) {
   // Stage shapes (BK x stages, picked by timing at 4096^3): exact 16 x 5 with
   // A 16 KiB + B 8 KiB + A_lo 16 KiB per stage; tf32 32 x 4 with A 32 KiB +
   // B 16 KiB. The LSU variants stage no B tile in shared memory.
-  if (exact) {
-    if (lsu) return launch_variant<16, 6, true, true, 1>(a, sm_count, stream);
-    return launch_variant<16, 5, true, false, kClusterExact>(a, sm_count, stream);
+  if (a.opa) {
+    // A stored transposed (K x M): the LSU producer transposes its tile on
+    // the way into shared memory; B as for A stored row-major.
+    if (a.opb) {
+      if (exact) return launch_variant<16, 4, true, true, 1, true, true>(a, sm_count, stream);
+      return launch_variant<32, 4, false, true, 1, true, true>(a, sm_count, stream);
+    }
+    if (exact) return launch_variant<16, 6, true, true, 1, false, true>(a, sm_count, stream);
+    return launch_variant<32, 6, false, true, 1, false, true>(a, sm_count, stream);
   }
-  if (lsu) return launch_variant<32, 6, false, true, 1>(a, sm_count, stream);
-  return launch_variant<32, 4, false, false, kClusterTf32>(a, sm_count, stream);
+  if (a.opb) {
+    // B stored transposed: both tiles K-major in shared memory. Stages of
+    // 48 KiB (exact: A, B and their lo tiles at BK = 16; tf32: A and B at 32).
+    if (exact) {
+      if (lsu) return launch_variant<16, 4, true, true, 1, true>(a, sm_count, stream);
+      return launch_variant<16, 4, true, false, kClusterExact, true>(a, sm_count, stream);
+    }
+    if (lsu) return launch_variant<32, 4, false, true, 1, true>(a, sm_count, stream);
+    return launch_variant<32, 4, false, false, kClusterTf32, true>(a, sm_count, stream);
+  }
+  if (exact) {
+    if (lsu) return launch_variant<16, 6, true, true, 1, false>(a, sm_count, stream);
+    return launch_variant<16, 5, true, false, kClusterExact, false>(a, sm_count, stream);
+  }
+  if (lsu) return launch_variant<32, 6, false, true, 1, false>(a, sm_count, stream);
+  return launch_variant<32, 4, false, false, kClusterTf32, false>(a, sm_count, stream);
 }
 
 int tc_poll_status(cudaStream_t stream) {
@@ -1142,14 +1295,14 @@ int noalloc_scratch(int dev, void **out) {
   return kOk;
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL>
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB>
 int launch_variant_noalloc(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return kErrLaunch;
   void *scratch = nullptr;
   int st = noalloc_scratch(dev, &scratch);
   if (st != kOk) return st;
-  LaunchPlan<BK, STAGES, EXACT, LSU, CL> plan;
+  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB> plan;
   st = plan.prepare(a, sm_count);
   if (st != kOk) return st;
   // The same workspace layout gemm_f32 takes from the pool, here inside the
@@ -1169,11 +1322,11 @@ int launch_variant_noalloc(const GemmArgs &a, int sm_count, cudaStream_t stream)
 int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream) {
   // Same kernels and stage shapes as tc_launch.
   if (exact) {
-    if (lsu) return launch_variant_noalloc<16, 6, true, true, 1>(a, sm_count, stream);
-    return launch_variant_noalloc<16, 5, true, false, kClusterExact>(a, sm_count, stream);
+    if (lsu) return launch_variant_noalloc<16, 6, true, true, 1, false>(a, sm_count, stream);
+    return launch_variant_noalloc<16, 5, true, false, kClusterExact, false>(a, sm_count, stream);
   }
-  if (lsu) return launch_variant_noalloc<32, 6, false, true, 1>(a, sm_count, stream);
-  return launch_variant_noalloc<32, 4, false, false, kClusterTf32>(a, sm_count, stream);
+  if (lsu) return launch_variant_noalloc<32, 6, false, true, 1, false>(a, sm_count, stream);
+  return launch_variant_noalloc<32, 4, false, false, kClusterTf32, false>(a, sm_count, stream);
 }
 
 }  // namespace gemm

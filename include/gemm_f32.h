@@ -116,6 +116,61 @@ int gemm_f32_ex(int64_t M, int64_t N, int64_t K,
                 float *C, int64_t ldc,
                 int mode, int kernel, void *stream);
 
+/* Storage order and operand transposition for gemm_f32_general. */
+typedef enum {
+    GEMM_ROW_MAJOR = 0,  /* element (i, j) of a matrix with pitch ld at [i * ld + j] */
+    GEMM_COL_MAJOR = 1   /* element (i, j) at [j * ld + i] (BLAS / LAPACK storage) */
+} gemm_f32_order;
+
+typedef enum {
+    GEMM_OP_N = 0,  /* op(X) = X */
+    GEMM_OP_T = 1   /* op(X) = X^T: the operand is supplied transposed */
+} gemm_f32_op;
+
+/*
+ * gemm_f32_general -- C = alpha * op(A) op(B) + beta * C, stream ordered.
+ *
+ * The general form of gemm_f32: op(A) is M x K, op(B) is K x N, C is M x N.
+ * Transposed operands are the layouts of "Optimizing a WebGPU Matmul Kernel
+ * using Subgroups", section 7 (B supplied transposed, N x K, so that both
+ * operands are read along k) and of the column-major (BLAS) storage that
+ * "WebGPU 计算着色器矩阵乘法优化：从 Naive 到 Tiled 深度实战" ("工程实践建议")
+ * advises adapting the indexing to. alpha and beta are not on the pages,
+ * whose kernels overwrite C; they are the usual scale of the product and of
+ * the previous C.
+ *   order     a gemm_f32_order; it applies to A, B and C alike.
+ *   transa    a gemm_f32_op. Stored A: M x K for GEMM_OP_N, K x M for
+ *             GEMM_OP_T, with lda >= max(1, columns of the stored A in
+ *             row-major order / rows in column-major order).
+ *   transb    a gemm_f32_op. Stored B: K x N for GEMM_OP_N, N x K for
+ *             GEMM_OP_T, with ldb likewise.
+ *   alpha     scale of the product. alpha == 0 or K == 0: A and B are not
+ *             read and C = beta * C.
+ *   beta      scale of the previous C. beta == 0: C is not read, so its
+ *             previous contents (NaN included) do not matter.
+ *   C, ldc    ldc >= max(1, N) (row-major) or max(1, M) (column-major).
+ *   mode, kernel, stream   as for gemm_f32_ex.
+ * A column-major call is the row-major call on the transposes (C^T =
+ * op(B)^T op(A)^T): the library swaps the operands and their flags. Row-major
+ * calls with transa == GEMM_OP_T (column-major: transb == GEMM_OP_T) are
+ * served by the tensor-core kernel fed by plain loads (GEMM_KERNEL_TC_LSU;
+ * GEMM_KERNEL_TC_TMA returns GEMM_ERR_INVALID_ARG for them) or the SIMT
+ * kernel. Accuracy classes apply to alpha * op(A) op(B) with S = |op(A)|
+ * |op(B)| scaled by |alpha|, plus one rounding of the scale-and-add.
+ * gemm_f32(...) is gemm_f32_general(GEMM_ROW_MAJOR, GEMM_OP_N, GEMM_OP_N,
+ * M, N, K, 1, A, lda, B, ldb, 0, C, ldc, mode, GEMM_KERNEL_AUTO, stream).
+ * Returns a gemm_f32_status; errors as for gemm_f32 (an unknown order or op
+ * is GEMM_ERR_INVALID_ARG).
+ */
+int gemm_f32_general(int order, int transa, int transb,
+                     int64_t M, int64_t N, int64_t K,
+                     float alpha,
+                     const float *A, int64_t lda,
+                     const float *B, int64_t ldb,
+                     float beta,
+                     float *C, int64_t ldc,
+                     int mode, int kernel, void *stream);
+
 /*
  * gemm_f32_select -- the kernel gemm_f32_ex would run for these arguments (a
  * gemm_f32_kernel value, never AUTO), or a negative gemm_f32_status if the

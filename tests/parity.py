@@ -30,12 +30,17 @@ def tf32_arithmetic_factor(k: int) -> float:
     return 2.0 ** -9 + k * 2.0 ** -23
 
 
-def check_within_bound(c, c64, s, k, mode, what=""):
+def check_within_bound(c, c64, s, k, mode, what="", extra=0.0):
+    """Element-wise acceptance of C against the oracle's C64 with scale S.
+
+    ``extra`` (scalar or array) is added to both bounds: the rounding of a
+    scale-and-add epilogue in the general form (see ``general_slack``).
+    """
     c = np.asarray(c, dtype=np.float32)
     assert c.shape == c64.shape, (c.shape, c64.shape)
     finite = np.isfinite(c)
     assert finite.all(), f"{what}: {int((~finite).sum())} non-finite outputs"
-    tol = tolerance_factor(mode, k) * s
+    tol = tolerance_factor(mode, k) * s + extra
     err = np.abs(c.astype(np.float64) - c64)
     bad = err > tol
     if bad.any():
@@ -45,7 +50,7 @@ def check_within_bound(c, c64, s, k, mode, what=""):
             f"{what}: {int(bad.sum())} of {bad.size} outputs outside the {mode} bound; "
             f"first at {i}: C={c[i]!r} C64={c64[i]!r} err={err[i]:.3e} tol={tol[i]:.3e}")
     if mode == "tf32":
-        tight = tf32_arithmetic_factor(k) * s
+        tight = tf32_arithmetic_factor(k) * s + extra
         bad = err > tight
         if bad.any():
             i = tuple(int(v) for v in np.argwhere(bad)[0])
@@ -56,3 +61,14 @@ def check_within_bound(c, c64, s, k, mode, what=""):
     with np.errstate(divide="ignore", invalid="ignore"):
         used = np.where(tol > 0, err / tol, 0.0)
     return float(used.max()) if used.size else 0.0
+
+
+def general_slack(s, alpha, beta, c0=None):
+    """Rounding allowance of C = alpha * P + beta * C0 computed in fp32 on top
+    of the product P (scale S): alpha * P and beta * C0 are each rounded once
+    and added once (or fused), so at most 2**-22 * (|alpha| S + |beta| |C0|)
+    beyond |alpha| times the product's own bound."""
+    extra = 2.0 ** -22 * abs(alpha) * s
+    if beta != 0.0:
+        extra = extra + 2.0 ** -22 * abs(beta) * np.abs(np.asarray(c0, dtype=np.float64))
+    return extra

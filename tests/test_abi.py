@@ -9,6 +9,7 @@ import pytest
 EXPECTED = {
     "gemm_f32", "gemm_f32_ex", "gemm_f32_select", "gemm_f32_host", "gemm_f32_status_string",
     "gemm_f32_poll_device_status", "gemm_f32_selftest_wait_timeout", "gemm_f32_noalloc",
+    "gemm_f32_general",
 }
 
 # Fake, never dereferenced, 256-byte aligned "device" addresses for host-only paths.
@@ -87,6 +88,60 @@ def test_kernel_selection(gemm_lib):
     assert sel(64, 64, 64, PA, 64, PB, 64, PC, 64, E, 9) == -gemm_lib.ERR_INVALID_ARG
     # invalid arguments are reported as negative status codes
     assert sel(-1, 64, 64, PA, 64, PB, 64, PC, 64, E, 0) == -gemm_lib.ERR_INVALID_ARG
+
+
+def _general(gemm_lib, **kw):
+    a = dict(order=0, transa=0, transb=0, M=16, N=32, K=64, alpha=1.0, A=PA, lda=64, B=PB, ldb=32,
+             beta=0.0, C=PC, ldc=32, mode=0, kernel=0)
+    a.update(kw)
+    return gemm_lib.gemm_f32_general(a["order"], a["transa"], a["transb"], a["M"], a["N"], a["K"],
+                                     a["alpha"], a["A"], a["lda"], a["B"], a["ldb"], a["beta"],
+                                     a["C"], a["ldc"], a["mode"], a["kernel"], 0)
+
+
+@pytest.mark.parametrize("args", [
+    dict(order=2), dict(order=-1), dict(transa=2), dict(transb=-1),
+    # row-major, A stored K x M: lda >= M; B stored N x K: ldb >= K
+    dict(transa=1, lda=15), dict(transb=1, ldb=63), dict(transb=1, ldb=32),
+    # column-major: lda >= M (A is M x K), ldb >= K (B is K x N), ldc >= M
+    dict(order=1, lda=15), dict(order=1, lda=16, ldb=63), dict(order=1, lda=16, ldb=64, ldc=15),
+    dict(order=1, transa=1, lda=63, ldb=64, ldc=16),   # A stored K x M column-major: lda >= K
+    dict(mode=3), dict(kernel=9), dict(M=-1),
+    dict(transa=1, lda=16, kernel=2),                  # TMA cannot feed A stored transposed
+    dict(transa=1, lda=16, mode=1, kernel=1),          # SIMT cannot serve TF32
+])
+def test_general_invalid_arguments_rejected(gemm_lib, args):
+    assert _general(gemm_lib, **args) == gemm_lib.ERR_INVALID_ARG
+
+
+def test_general_alias_uses_stored_extents(gemm_lib):
+    # B stored N x K (transb) with pitch ldb spans (N - 1) * ldb + K elements:
+    # C on its last element overlaps.
+    n, k = 32, 64
+    last = (n - 1) * k + k - 1
+    assert _general(gemm_lib, transb=1, N=n, K=k, ldb=k, C=PB + 4 * last, ldc=n,
+                    M=1) == gemm_lib.ERR_ALIAS
+    # A stored K x M (transa), pitch lda = M: (K - 1) * M + M elements.
+    assert _general(gemm_lib, transa=1, M=16, K=64, A=PA, lda=16, C=PA + 4 * 1023,
+                    ldc=32) == gemm_lib.ERR_ALIAS
+
+
+def test_general_valid_layouts_pass_validation_without_gpu(gemm_lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    fine = (gemm_lib.ERR_LAUNCH, gemm_lib.ERR_UNSUPPORTED_DEVICE)
+    assert _general(gemm_lib, transa=1, lda=16) in fine
+    assert _general(gemm_lib, transb=1, ldb=64) in fine
+    assert _general(gemm_lib, order=1, lda=16, ldb=64, ldc=16) in fine
+    assert _general(gemm_lib, order=1, transa=1, transb=1, lda=64, ldb=32, ldc=16) in fine
+    assert _general(gemm_lib, alpha=0.0, beta=2.0) in fine
+    # just past the stored N x K extent of B (inside a K x N reading of it)
+    assert _general(gemm_lib, transb=1, N=32, K=64, ldb=64, C=PB + 4 * 32 * 64, ldc=32,
+                    M=1) in fine
+    assert _general(gemm_lib, transa=1, M=16, K=64, A=PA, lda=16, C=PA + 4 * 1024,
+                    ldc=32) in fine
 
 
 def test_valid_call_without_gpu_fails_cleanly(gemm_lib):
