@@ -57,6 +57,9 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true", help="skip the other modes, e2e and CPU legs")
     ap.add_argument("--config", default="c4", choices=sorted(WORKLOADS),
                     help="workload (the benchmark is c4; the others are for the record)")
+    ap.add_argument("--layout", default="nn", choices=["nn", "nt", "tn", "tt"],
+                    help="operand storage (n: as is, t: transposed) through gemm_f32_general; "
+                         "the benchmark is nn through gemm_f32")
     return ap.parse_args()
 
 
@@ -308,14 +311,27 @@ def main():
     a, b, cfg = synth.config_operands(args.config)
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     WORKLOAD = WORKLOADS[args.config]
-    dA = torch.from_numpy(a).cuda()
-    dB = torch.from_numpy(b).cuda()
+    transa, transb = (1 if args.layout[0] == "t" else 0), (1 if args.layout[1] == "t" else 0)
+    if args.layout != "nn":
+        WORKLOAD += f"; A stored {'K x M' if transa else 'M x K'}, B stored {'N x K' if transb else 'K x N'}"
+    dA = torch.from_numpy(np.ascontiguousarray(a.T) if transa else a).cuda()
+    dB = torch.from_numpy(np.ascontiguousarray(b.T) if transb else b).cuda()
+    lda, ldb = dA.shape[1], dB.shape[1]
     dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
 
     def gemm_call(mode):
+        if args.layout != "nn":
+            def fn():
+                st = g.gemm_f32_general(g.ROW_MAJOR, transa, transb, M, N, K, 1.0, dA.data_ptr(),
+                                        lda, dB.data_ptr(), ldb, 0.0, dC.data_ptr(), N, mode,
+                                        g.KERNEL_AUTO, sptr)
+                if st != g.OK:
+                    raise g.GemmError(st, "gemm_f32_general")
+            return fn
+
         def fn():
             st = g.gemm_f32(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N, mode, sptr)
             if st != g.OK:
@@ -355,6 +371,10 @@ def main():
     pk = peaks()
     tf32_peak = pk["bf16"] * TF32_PER_BF16
     alu_peak = SMS * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+    if args.layout != "nn" and kernel != g.KERNEL_SIMT:
+        # A stored transposed reaches the TMA-fed kernel through a transposed copy
+        kernel_name += "_" + args.layout + ("_after_transpose" if transa and kernel == g.KERNEL_TC_TMA
+                                            else "")
     traffic, sha = traffic_lookup(kernel_name, args.config, args.mode)
     if args.mode == "exact_simt":
         achieved = flops / (ms_per_step / 1e3) / 1e12
@@ -419,7 +439,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "mode": args.mode,
-                       "kernel": kernel_name, "l2": "flushed (256 MiB write) between timed steps",
+                       "layout": args.layout, "kernel": kernel_name, "l2": "flushed (256 MiB write) between timed steps",
                        "replicas": world, "parallelism": "replicas" if world > 1 else "single"},
             "roofline": roofline,
             "cpu_baseline": cpu,

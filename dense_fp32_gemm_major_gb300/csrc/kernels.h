@@ -35,7 +35,9 @@ enum : int {
 };
 
 // True when A and B can be described by TMA tensor maps: 16-byte aligned
-// base addresses and row pitches that are multiples of 16 bytes.
+// base addresses and row pitches that are multiples of 16 bytes. A stored
+// transposed (opa) qualifies whatever its layout: tc_launch first copies it
+// into a row-major workspace that does.
 bool tc_tma_legal(const GemmArgs &a);
 
 // tcgen05 GEMM: exact = 3xTF32, else single-pass TF32; lsu = operands staged
@@ -46,6 +48,11 @@ int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_
 // (no allocation). Returns kErrInvalidArg if the problem needs more scratch
 // than GEMM_F32_NOALLOC_SCRATCH_BYTES.
 int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream);
+
+// dst (cols x rows, pitch ldd) = src^T for src rows x cols (pitch lds), on
+// `stream`. Sizes below 2^31.
+int transpose_launch(const float *src, int64_t lds, int64_t rows, int64_t cols, float *dst,
+                     int64_t ldd, int sm_count, cudaStream_t stream);
 
 // SIMT FP32 GEMM. Requires K >= 1, M >= 1, N >= 1.
 int simt_launch(const GemmArgs &a, cudaStream_t stream);

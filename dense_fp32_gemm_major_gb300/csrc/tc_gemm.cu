@@ -122,12 +122,17 @@ __device__ __forceinline__ int split_slot(const TcParams &p, int s, int part) {
 // descriptor by 32 bytes along the row.
 // OPB = false: B is stored K x N (N contiguous); its tile goes through
 // registers into TMEM as B^T. OPB = true: B is stored transposed, N x K (K
-// contiguous), so its tile is K-major like A's and feeds the MMA from shared
-// memory directly; TMEM then holds only accumulators, two of them.
+// contiguous), so its tile is K-major like A's. One TF32 pass (and the LSU
+// variants) feed it to the MMA from shared memory directly, and TMEM then
+// holds only accumulators, two of them. The TMA-fed 3xTF32 variant still
+// moves it into TMEM (hi and lo), as for B stored K x N: reading both hi/lo
+// operand pairs from shared memory would exceed the shared-memory bandwidth
+// that the split and the copies leave to the MMAs.
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB>
 struct TcConfig {
   static_assert(BK == 16 || BK == 32, "BK");
   static_assert(CL == 1 || (CL == 2 && !LSU), "clusters pair TMA-fed CTAs only");
+  static constexpr bool kBtTmem = !OPB || (EXACT && !LSU);       // B^T operand in TMEM
   static constexpr int kAPartRows = kTM / CL;                    // A rows each CTA loads
   static constexpr int kAPartBytes = kAPartRows * BK * 4;
   static constexpr int kRowBytes = BK * 4;                       // one K-major tile row
@@ -139,29 +144,29 @@ struct TcConfig {
   static constexpr int kBBytes = (LSU && !OPB) ? 0 : BK * kTN * 4;
   // 3xTF32 lo tiles follow the hi (or raw) tiles at kLoOffset, same layout.
   static constexpr int kLoOffset = kABytes + kBBytes;
-  static constexpr int kLoBytes = EXACT ? (OPB ? kABytes + kBBytes : kABytes) : 0;
+  static constexpr int kLoBytes = EXACT ? (kBtTmem ? kABytes : kABytes + kBBytes) : 0;
   static constexpr int kStageBytes = kABytes + kBBytes + kLoBytes;
   static constexpr int kBOffset = kABytes;
   static constexpr int kALoOffset = kLoOffset;
   static constexpr int kBLoOffset = kLoOffset + kABytes;         // OPB && EXACT
   static constexpr int kTileBytes = STAGES * kStageBytes;
-  static constexpr uint32_t kBtColsPerStage = OPB ? 0 : (EXACT ? 2 * BK : BK);  // hi (+ lo)
-  static constexpr int kAccBufs = OPB ? 2 : 1;                   // TMEM accumulators
+  static constexpr uint32_t kBtColsPerStage = kBtTmem ? (EXACT ? 2 * BK : BK) : 0;  // hi (+ lo)
+  static constexpr int kAccBufs = kBtTmem ? 1 : 2;               // TMEM accumulators
   static constexpr int kProdWarps = LSU ? 4 : 1;
   static constexpr int kMmaWarp = kProdWarps;
   static constexpr int kEpiWarp0 = kMmaWarp + 1;
   // Transform warps, a multiple of 4 (whole TMEM lane quadrants). The 3xTF32
   // split is the most work per stage: 16 warps keep it ahead of the MMAs.
   // With B transposed and one TF32 pass there is nothing to transform.
-  static constexpr int kXformWarps = LSU ? 0 : (OPB ? (EXACT ? 16 : 0) : (EXACT ? 16 : 8));
+  static constexpr int kXformWarps = LSU ? 0 : (kBtTmem ? (EXACT ? 16 : 8) : 0);
   static constexpr int kXformParts = kXformWarps > 0 ? kXformWarps / 4 : 1;  // per lane quadrant
   static constexpr int kXformWarp0 = kEpiWarp0 + 4;
   static constexpr int kThreads = 32 * (kXformWarp0 + kXformWarps);
   static constexpr uint32_t kIdesc = idesc_tf32(kTN, kTM);
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(kXformWarps % 4 == 0 && BK % kXformParts == 0, "transform partition");
-  static_assert(OPB ? kAccBufs * kTM <= static_cast<int>(kTmemCols)
-                    : kBtCol + STAGES * kBtColsPerStage <= kTmemCols,
+  static_assert(kBtTmem ? kBtCol + STAGES * kBtColsPerStage <= kTmemCols
+                        : kAccBufs * kTM <= static_cast<int>(kTmemCols),
                 "TMEM budget");
 };
 
@@ -641,7 +646,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kTh
             // 8-row groups (the swizzle atom) are kAtomBytes apart.
             const uint64_t da = smem_desc(a_hi + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
             const uint32_t accumulate = (kb != u.kb0 || kk != 0) ? 1u : 0u;
-            if (OPB) {
+            if (!Cfg::kBtTmem) {
               // B^T rows straight from the K-major B tile in shared memory.
               const uint64_t db = smem_desc(a_hi + Cfg::kBOffset + kk * 32, 16, Cfg::kAtomBytes,
                                             Cfg::kLayout);
@@ -818,11 +823,32 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kTh
           const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol +
                                stage * Cfg::kBtColsPerStage + part * kW;
           bt_to_tmem<kW, EXACT>(col, col + BK, v);
+        } else if (Cfg::kBtTmem) {
+          // B tile is K-major 128 n x BK k (swizzled rows of BK * 4 bytes):
+          // row n = 32 quad + lane holds this thread's TMEM lane, and part
+          // `part` reads its kW consecutive k as 16-byte chunks.
+          constexpr int kW = BK / Cfg::kXformParts;
+          static_assert(kW % 4 == 0, "whole 16-byte chunks per part");
+          const int n = quad * 32 + lane;
+          float v[kW];
+#pragma unroll
+          for (int c = 0; c < kW / 4; ++c) {
+            const float4 x = *reinterpret_cast<const float4 *>(
+                st + Cfg::kBOffset + swizzle_a<BK>(n * Cfg::kRowBytes + (part * kW + c * 4) * 4));
+            v[c * 4 + 0] = x.x;
+            v[c * 4 + 1] = x.y;
+            v[c * 4 + 2] = x.z;
+            v[c * 4 + 3] = x.w;
+          }
+          const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol +
+                               stage * Cfg::kBtColsPerStage + part * kW;
+          bt_to_tmem<kW, EXACT>(col, col + BK, v);
         }
         if (EXACT) {
-          // Split the K-major tiles (A, and B when it is stored transposed):
-          // hi in place, lo kLoOffset bytes further.
-          constexpr int kSplitVecs = (OPB ? Cfg::kABytes + Cfg::kBBytes : Cfg::kABytes) / 16;
+          // Split the K-major tiles held in shared memory as MMA operands (A,
+          // and B when it is not moved into TMEM): hi in place, lo kLoOffset
+          // bytes further.
+          constexpr int kSplitVecs = (Cfg::kBtTmem ? Cfg::kABytes : Cfg::kABytes + Cfg::kBBytes) / 16;
           float4 *raw = reinterpret_cast<float4 *>(st);
           float4 *lo = reinterpret_cast<float4 *>(st + Cfg::kLoOffset);
 #pragma unroll 4
@@ -1202,18 +1228,40 @@ int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
 }  // namespace
 
 bool tc_tma_legal(const GemmArgs &a) {
-  // A stored transposed (K x M) is only staged by the LSU producer.
-  return !a.opa && reinterpret_cast<uintptr_t>(a.A) % 16 == 0 &&
-         reinterpret_cast<uintptr_t>(a.B) % 16 == 0 && a.lda % 4 == 0 && a.ldb % 4 == 0;
+  const bool a_ok = a.opa || (reinterpret_cast<uintptr_t>(a.A) % 16 == 0 && a.lda % 4 == 0);
+  return a_ok && reinterpret_cast<uintptr_t>(a.B) % 16 == 0 && a.ldb % 4 == 0;
 }
 
 int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream) {
   // Stage shapes (BK x stages, picked by timing at 4096^3): exact 16 x 5 with
   // A 16 KiB + B 8 KiB + A_lo 16 KiB per stage; tf32 32 x 4 with A 32 KiB +
   // B 16 KiB. The LSU variants stage no B tile in shared memory.
+  if (a.opa && !lsu) {
+    // A stored transposed (K x M) for the TMA-fed kernel: rewrite it as a
+    // row-major M x K copy (16-byte pitch) in a workspace from the library's
+    // pool, ordered on the stream before the GEMM and released after it.
+    const int64_t ldt = (a.K + 3) / 4 * 4;
+    int dev = 0;
+    cudaMemPool_t pool = nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || workspace_pool(dev, &pool) != kOk) return kErrLaunch;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a.M) * ldt * 4, pool, stream) !=
+        cudaSuccess)
+      return kErrLaunch;
+    GemmArgs t = a;
+    t.A = static_cast<const float *>(ws);
+    t.lda = ldt;
+    t.opa = 0;
+    int st = transpose_launch(a.A, a.lda, a.K, a.M, static_cast<float *>(ws), ldt, sm_count,
+                              stream);
+    if (st == kOk) st = tc_launch(t, exact, false, sm_count, stream);
+    if (cudaFreeAsync(ws, stream) != cudaSuccess && st == kOk) st = kErrLaunch;
+    return st;
+  }
   if (a.opa) {
-    // A stored transposed (K x M): the LSU producer transposes its tile on
-    // the way into shared memory; B as for A stored row-major.
+    // A stored transposed (K x M) for the LSU variant: the producer
+    // transposes each tile on its way into shared memory; B as for A stored
+    // row-major.
     if (a.opb) {
       if (exact) return launch_variant<16, 4, true, true, 1, true, true>(a, sm_count, stream);
       return launch_variant<32, 4, false, true, 1, true, true>(a, sm_count, stream);
@@ -1223,10 +1271,12 @@ int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_
   }
   if (a.opb) {
     // B stored transposed: both tiles K-major in shared memory. Stages of
-    // 48 KiB (exact: A, B and their lo tiles at BK = 16; tf32: A and B at 32).
+    // 48 KiB (LSU exact: A, B and their lo tiles at BK = 16; tf32: A and B
+    // at 32) or 40 KiB (TMA exact: B^T hi and lo go to TMEM, as for B
+    // stored K x N).
     if (exact) {
       if (lsu) return launch_variant<16, 4, true, true, 1, true>(a, sm_count, stream);
-      return launch_variant<16, 4, true, false, kClusterExact, true>(a, sm_count, stream);
+      return launch_variant<16, 5, true, false, kClusterExact, true>(a, sm_count, stream);
     }
     if (lsu) return launch_variant<32, 4, false, true, 1, true>(a, sm_count, stream);
     return launch_variant<32, 4, false, false, kClusterTf32, true>(a, sm_count, stream);

@@ -1,0 +1,64 @@
+// transpose.cu -- out-of-place fp32 matrix transpose, dst = src^T.
+//
+// Feeds the TMA-fed tensor-core kernel when A is supplied transposed (stored
+// K x M): TMA can only hand the tcgen05 TF32 MMA K-major tiles, so A^T is
+// first rewritten as a row-major M x K copy with a 16-byte pitch. The copy is
+// bound by HBM bandwidth (one read and one write of the matrix).
+//
+// A CTA of 256 threads moves 32 x 32 tiles through shared memory (a padded
+// 32 x 33 array, so that the column reads of the transposed store do not
+// conflict): loads and stores are each one coalesced 128-byte row segment
+// per warp. CTAs are persistent and walk the tiles in steps of the grid.
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kernels.h"
+
+namespace gemm {
+namespace {
+
+constexpr int kT = 32;
+constexpr int kRowsPerPass = 8;  // 256 threads = 8 rows of 32
+constexpr int kBlocksPerSm = 8;
+
+__global__ void __launch_bounds__(kT * kRowsPerPass)
+    transpose_kernel(const float *__restrict__ src, long long lds, int rows, int cols,
+                     float *__restrict__ dst, long long ldd, int tiles_c, long long tiles) {
+  __shared__ float t[kT][kT + 1];
+  const int tx = threadIdx.x % kT, ty = threadIdx.x / kT;
+  for (long long tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int r0 = static_cast<int>(tile / tiles_c) * kT;
+    const int c0 = static_cast<int>(tile % tiles_c) * kT;
+#pragma unroll
+    for (int i = ty; i < kT; i += kRowsPerPass) {
+      const int r = r0 + i, c = c0 + tx;
+      if (r < rows && c < cols) t[i][tx] = __ldg(src + static_cast<long long>(r) * lds + c);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = ty; i < kT; i += kRowsPerPass) {
+      const int c = c0 + i, r = r0 + tx;  // dst row c, column r
+      if (c < cols && r < rows) dst[static_cast<long long>(c) * ldd + r] = t[tx][i];
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+int transpose_launch(const float *src, int64_t lds, int64_t rows, int64_t cols, float *dst,
+                     int64_t ldd, int sm_count, cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return kOk;
+  const long long tiles_r = (rows + kT - 1) / kT, tiles_c = (cols + kT - 1) / kT;
+  const long long tiles = tiles_r * tiles_c;
+  const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * kBlocksPerSm;
+  const unsigned grid = static_cast<unsigned>(tiles < cap ? tiles : cap);
+  transpose_kernel<<<grid, kT * kRowsPerPass, 0, stream>>>(
+      src, lds, static_cast<int>(rows), static_cast<int>(cols), dst, ldd,
+      static_cast<int>(tiles_c), tiles);
+  return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+}
+
+}  // namespace gemm

@@ -151,12 +151,15 @@ typedef enum {
  *   C, ldc    ldc >= max(1, N) (row-major) or max(1, M) (column-major).
  *   mode, kernel, stream   as for gemm_f32_ex.
  * A column-major call is the row-major call on the transposes (C^T =
- * op(B)^T op(A)^T): the library swaps the operands and their flags. Row-major
- * calls with transa == GEMM_OP_T (column-major: transb == GEMM_OP_T) are
- * served by the tensor-core kernel fed by plain loads (GEMM_KERNEL_TC_LSU;
- * GEMM_KERNEL_TC_TMA returns GEMM_ERR_INVALID_ARG for them) or the SIMT
- * kernel. Accuracy classes apply to alpha * op(A) op(B) with S = |op(A)|
- * |op(B)| scaled by |alpha|, plus one rounding of the scale-and-add.
+ * op(B)^T op(A)^T): the library swaps the operands and their flags. When a
+ * row-major call has transa == GEMM_OP_T (column-major: transb ==
+ * GEMM_OP_T), the TMA-fed tensor-core kernel (GEMM_KERNEL_TC_TMA, which AUTO
+ * picks when B allows it) runs on a row-major copy of op(A) that a transpose
+ * kernel writes first into a workspace of M x K floats (pitch rounded up to
+ * 4) from the library's stream-ordered pool; GEMM_KERNEL_TC_LSU instead
+ * transposes each tile of A as it stages it, with no workspace. Accuracy
+ * classes apply to alpha * op(A) op(B) with S = |op(A)| |op(B)| scaled by
+ * |alpha|, plus one rounding of the scale-and-add.
  * gemm_f32(...) is gemm_f32_general(GEMM_ROW_MAJOR, GEMM_OP_N, GEMM_OP_N,
  * M, N, K, 1, A, lda, B, ldb, 0, C, ldc, mode, GEMM_KERNEL_AUTO, stream).
  * Returns a gemm_f32_status; errors as for gemm_f32 (an unknown order or op

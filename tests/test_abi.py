@@ -107,7 +107,7 @@ def _general(gemm_lib, **kw):
     dict(order=1, lda=15), dict(order=1, lda=16, ldb=63), dict(order=1, lda=16, ldb=64, ldc=15),
     dict(order=1, transa=1, lda=63, ldb=64, ldc=16),   # A stored K x M column-major: lda >= K
     dict(mode=3), dict(kernel=9), dict(M=-1),
-    dict(transa=1, lda=16, kernel=2),                  # TMA cannot feed A stored transposed
+    dict(transa=1, lda=16, kernel=2, B=PB + 4),        # TMA needs a 16-byte aligned B
     dict(transa=1, lda=16, mode=1, kernel=1),          # SIMT cannot serve TF32
 ])
 def test_general_invalid_arguments_rejected(gemm_lib, args):
@@ -133,6 +133,7 @@ def test_general_valid_layouts_pass_validation_without_gpu(gemm_lib):
         pytest.skip("a GPU is present")
     fine = (gemm_lib.ERR_LAUNCH, gemm_lib.ERR_UNSUPPORTED_DEVICE)
     assert _general(gemm_lib, transa=1, lda=16) in fine
+    assert _general(gemm_lib, transa=1, lda=17, kernel=2) in fine  # A copied for the TMA kernel
     assert _general(gemm_lib, transb=1, ldb=64) in fine
     assert _general(gemm_lib, order=1, lda=16, ldb=64, ldc=16) in fine
     assert _general(gemm_lib, order=1, transa=1, transb=1, lda=64, ldb=32, ldc=16) in fine
