@@ -1,12 +1,14 @@
-"""fp64 oracle for C = A x B (row-major fp32 operands).
+"""fp64 oracle for C = A x B (row-major fp32 operands) and for the sum of a
+fp32 vector.
 
 TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg may import this package. The CUDA library never
 calls it, and it never calls the CUDA library: the two share nothing but the
 seeded inputs from ``synth``.
 
-The arithmetic lives in ``gemm_oracle.c`` (plain C, fp64, no blocking); this
-file compiles it on first use and wraps it with ctypes. Every function returns
+The arithmetic lives in ``gemm_oracle.c`` and ``reduce_oracle.c`` (plain C,
+fp64, no blocking); this file compiles them on first use and wraps them with
+ctypes. Every function returns
 ``(C64, S)`` where ``C64[i, j] = sum_k A[i, k] * B[k, j]`` in fp64 and
 ``S[i, j] = sum_k |A[i, k]| * |B[k, j]|``: the product that
 "Optimizing a WebGPU Matmul Kernel using Subgroups", section 1 "Naive", and the
@@ -28,7 +30,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_SRCS = [os.path.join(_HERE, "gemm_oracle.c"), os.path.join(_HERE, "reduce_oracle.c")]
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_OUT_DIR, "liboracle.so")
 _lock = threading.Lock()
@@ -36,17 +38,20 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile gemm_oracle.c into oracle/_build/liboracle.so (OpenMP if available)."""
+    """Compile the oracle's C sources into oracle/_build/liboracle.so (OpenMP if
+    available)."""
     os.makedirs(_OUT_DIR, exist_ok=True)
-    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+    if (not force and os.path.exists(_LIB)
+            and all(os.path.getmtime(_LIB) >= os.path.getmtime(f) for f in _SRCS)):
         return _LIB
     base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
     tmp = _LIB + f".tmp{os.getpid()}"
     try:
-        subprocess.run(base + ["-fopenmp", "-o", tmp, _SRC, "-lm"], check=True,
+        subprocess.run(base + ["-fopenmp", "-o", tmp] + _SRCS + ["-lm"], check=True,
                        capture_output=True, text=True)
     except subprocess.CalledProcessError:
-        subprocess.run(base + ["-o", tmp, _SRC, "-lm"], check=True, capture_output=True, text=True)
+        subprocess.run(base + ["-o", tmp] + _SRCS + ["-lm"], check=True, capture_output=True,
+                       text=True)
     os.replace(tmp, _LIB)
     return _LIB
 
@@ -67,6 +72,8 @@ def _load():
             lib.oracle_gemm_general_rows_f64.argtypes = [ctypes.c_int, ctypes.c_int, i64, p, i64, i64,
                                                          d, p, i64, p, i64, d, p, i64, p, p]
             lib.oracle_gemm_general_rows_f64.restype = None
+            lib.oracle_sum_f64.argtypes = [i64, p, p, p]
+            lib.oracle_sum_f64.restype = None
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -182,6 +189,19 @@ def gemm_general(a: np.ndarray, b: np.ndarray, opb: int = 0, alpha: float = 1.0,
                                              _ptr(a), _ld(a), _ptr(b), _ld(b), float(beta), cptr,
                                              ldc, _ptr(out), _ptr(s))
     return out, s
+
+
+def vector_sum(x: np.ndarray):
+    """Sum of a 1-D float32 array in fp64, in index order: returns (s64, S)
+    with S = sum |x|. The quantity the per-group tree reduction of "GPU
+    compute shaders" computes."""
+    if not isinstance(x, np.ndarray) or x.dtype != np.float32 or x.ndim != 1:
+        raise TypeError("x must be a 1-D float32 array")
+    x = np.ascontiguousarray(x)
+    s64 = ctypes.c_double(0.0)
+    scale = ctypes.c_double(0.0)
+    _load().oracle_sum_f64(x.size, _ptr(x), ctypes.addressof(s64), ctypes.addressof(scale))
+    return s64.value, scale.value
 
 
 def num_threads() -> int:
