@@ -412,6 +412,29 @@ def main():
                              "roofline": {"bound": bound, "achieved": round(ach, 2),
                                           "peak": round(peak, 1), "unit": "TFLOP/s",
                                           "frac": round(ach / peak, 4)}}
+        # the pages' second workload: the per-group tree reduction of 2^26 fp32
+        # values (two dispatches), HBM-bound; the vector (256 MiB) exceeds L2
+        rn = 1 << 26
+        xr = torch.from_numpy(synth.uniform_pm1((rn,), 1026).reshape(-1)).cuda()
+        rout = torch.empty(1, dtype=torch.float32, device="cuda")
+
+        def reduce_fn():
+            st = g.reduce_f32_sum(rn, xr.data_ptr(), rout.data_ptr(), 0, sptr)
+            if st != g.OK:
+                raise g.GemmError(st, "reduce_f32_sum")
+
+        rts, _ = time_steps(torch, reduce_fn, 200, 10, flush, stream)
+        rms = statistics.mean(rts)
+        rgbs = 4.0 * rn / (rms / 1e3) / 1e9
+        extras["reduce_sum"] = {
+            "workload": "sum of 2^26 fp32 values, uniform[-1,1) from seed (reduce_f32_sum: "
+                        "per-group partials, then a second dispatch)",
+            "value": round(rgbs, 1), "unit": "GB/s", "ms_per_step": round(rms, 4), "steps": 200,
+            "gpu_launches_per_step": 2,
+            "roofline": {"bound": "hbm", "achieved": round(rgbs, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(rgbs / pk["hbm"], 4),
+                         "algorithmic_bytes": 4 * rn}}
+        del xr
         # end to end through the host-buffer entry point (pinned host memory)
         ha = torch.from_numpy(a).pin_memory().numpy()
         hb = torch.from_numpy(b).pin_memory().numpy()

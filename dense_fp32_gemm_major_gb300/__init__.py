@@ -21,7 +21,9 @@ import re
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgemm_f32.so")
-HEADER_PATH = os.path.join(os.path.dirname(_PKG), "include", "gemm_f32.h")
+INCLUDE_DIR = os.path.join(os.path.dirname(_PKG), "include")
+HEADER_PATH = os.path.join(INCLUDE_DIR, "gemm_f32.h")
+HEADERS = [HEADER_PATH, os.path.join(INCLUDE_DIR, "reduce_f32.h")]
 
 # gemm_f32_mode
 EXACT, TF32, EXACT_SIMT = 0, 1, 2
@@ -72,6 +74,8 @@ def _load():
     lib.gemm_f32_general.argtypes = [i32, i32, i32, i64, i64, i64, f32, p, i64, p, i64, f32, p,
                                      i64, i32, i32, p]
     lib.gemm_f32_general.restype = i32
+    lib.reduce_f32_sum.argtypes = [i64, p, p, i32, p]
+    lib.reduce_f32_sum.restype = i32
     lib.gemm_f32_status_string.argtypes = [i32]
     lib.gemm_f32_status_string.restype = ctypes.c_char_p
     lib.gemm_f32_poll_device_status.argtypes = [p]
@@ -94,11 +98,15 @@ def library():
 
 
 def declared_symbols() -> list[str]:
-    """Function names declared in include/gemm_f32.h."""
-    with open(HEADER_PATH) as f:
-        text = f.read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gemm_f32\w*)\s*\(", text, flags=re.M)))
+    """Function names declared in the public headers (include/*.h)."""
+    names = set()
+    for path in HEADERS:
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:gemm|reduce)_f32\w*)\s*\(",
+                                text, flags=re.M))
+    return sorted(names)
 
 
 # ------------------------------------------------------------ raw C ABI --
@@ -130,6 +138,11 @@ def gemm_f32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, mode, stream=0) -> int:
     """gemm_f32 that allocates no device memory (workspace in a fixed
     NOALLOC_SCRATCH_BYTES array; see include/gemm_f32.h)."""
     return _load().gemm_f32_noalloc(M, N, K, A, lda, B, ldb, C, ldc, mode, stream or None)
+
+
+def reduce_f32_sum(n, x, out, groups=0, stream=0) -> int:
+    """*out = sum of x[0, n) (device pointers; see include/reduce_f32.h)."""
+    return _load().reduce_f32_sum(n, x, out, groups, stream or None)
 
 
 def gemm_f32_status_string(status: int) -> str:
@@ -232,6 +245,25 @@ def gemm(a, b, out=None, alpha=1.0, beta=0.0, transa=False, transb=False, mode="
                               stream)
     if st != OK:
         raise GemmError(st, "gemm_f32_general")
+    return out
+
+
+def vector_sum(x, groups=0, out=None, stream=None):
+    """Sum of a 1-D float32 CUDA tensor through reduce_f32_sum; returns a
+    one-element float32 CUDA tensor (stream ordered)."""
+    import torch
+
+    if (not isinstance(x, torch.Tensor) or x.dtype != torch.float32 or not x.is_cuda
+            or x.dim() != 1 or (x.numel() > 1 and x.stride(0) != 1)):
+        raise TypeError("x must be a contiguous 1-D float32 CUDA tensor")
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    with torch.cuda.device(x.device):
+        st = reduce_f32_sum(x.numel(), x.data_ptr(), out.data_ptr(), int(groups), stream)
+    if st != OK:
+        raise GemmError(st, "reduce_f32_sum")
     return out
 
 

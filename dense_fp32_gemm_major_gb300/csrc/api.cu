@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "../../include/gemm_f32.h"
+#include "../../include/reduce_f32.h"
 #include "kernels.h"
 
 namespace {
@@ -288,6 +289,29 @@ int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t ld
   }
   if (k == GEMM_KERNEL_SIMT) return gemm::simt_launch(a, s);  // needs no scratch
   return gemm::tc_launch_noalloc(a, mode == GEMM_F32_EXACT, k == GEMM_KERNEL_TC_LSU, sms, s);
+}
+
+int reduce_f32_sum(int64_t n, const float *x, float *out, int groups, void *stream) {
+  if (n < 0 || n > (int64_t{1} << 40) || groups < 0 || groups > 65535) return GEMM_ERR_INVALID_ARG;
+  if (out == nullptr || reinterpret_cast<uintptr_t>(out) % 4 != 0) return GEMM_ERR_INVALID_ARG;
+  if (n > 0) {
+    if (x == nullptr || reinterpret_cast<uintptr_t>(x) % 4 != 0) return GEMM_ERR_INVALID_ARG;
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(x), x1 = x0 + static_cast<uintptr_t>(n) * 4;
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(out);
+    if (ranges_overlap(o0, o0 + 4, x0, x1)) return GEMM_ERR_ALIAS;
+  }
+  int dev = 0, sms = 0;
+  int st = current_device(&dev, &sms);
+  if (st != gemm::kOk) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n == 0) return gemm::reduce_launch(0, x, out, 1, nullptr, s);
+  const int g = groups > 0 ? groups : gemm::reduce_default_groups(sms);
+  void *partials = nullptr;
+  st = gemm::pool_alloc(&partials, static_cast<size_t>(g) * sizeof(float), s);
+  if (st != gemm::kOk) return st;
+  st = gemm::reduce_launch(n, x, out, g, static_cast<float *>(partials), s);
+  const int fst = gemm::pool_free(partials, s);
+  return st != gemm::kOk ? st : fst;
 }
 
 const char *gemm_f32_status_string(int status) {

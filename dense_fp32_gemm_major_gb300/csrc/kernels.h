@@ -54,6 +54,18 @@ int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cud
 int transpose_launch(const float *src, int64_t lds, int64_t rows, int64_t cols, float *dst,
                      int64_t ldd, int sm_count, cudaStream_t stream);
 
+// Stream-ordered workspace from the library's memory pool on the current
+// device (kept reserved by the pool once used, never shrunk).
+int pool_alloc(void **ptr, size_t bytes, cudaStream_t stream);
+int pool_free(void *ptr, cudaStream_t stream);
+
+// Sum of x[0, n) into *out (device pointers): `groups` partial sums written to
+// `partials` (groups floats), then a second kernel adds them. n == 0 sets
+// *out = 0.
+int reduce_launch(int64_t n, const float *x, float *out, int groups, float *partials,
+                  cudaStream_t stream);
+int reduce_default_groups(int sm_count);
+
 // SIMT FP32 GEMM. Requires K >= 1, M >= 1, N >= 1.
 int simt_launch(const GemmArgs &a, cudaStream_t stream);
 

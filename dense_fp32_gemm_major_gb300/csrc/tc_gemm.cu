@@ -1227,6 +1227,17 @@ int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
 
 }  // namespace
 
+int pool_alloc(void **ptr, size_t bytes, cudaStream_t stream) {
+  int dev = 0;
+  cudaMemPool_t pool = nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || workspace_pool(dev, &pool) != kOk) return kErrLaunch;
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, stream) == cudaSuccess ? kOk : kErrLaunch;
+}
+
+int pool_free(void *ptr, cudaStream_t stream) {
+  return cudaFreeAsync(ptr, stream) == cudaSuccess ? kOk : kErrLaunch;
+}
+
 bool tc_tma_legal(const GemmArgs &a) {
   const bool a_ok = a.opa || (reinterpret_cast<uintptr_t>(a.A) % 16 == 0 && a.lda % 4 == 0);
   return a_ok && reinterpret_cast<uintptr_t>(a.B) % 16 == 0 && a.ldb % 4 == 0;

@@ -9,7 +9,7 @@ import pytest
 EXPECTED = {
     "gemm_f32", "gemm_f32_ex", "gemm_f32_select", "gemm_f32_host", "gemm_f32_status_string",
     "gemm_f32_poll_device_status", "gemm_f32_selftest_wait_timeout", "gemm_f32_noalloc",
-    "gemm_f32_general",
+    "gemm_f32_general", "reduce_f32_sum",
 }
 
 # Fake, never dereferenced, 256-byte aligned "device" addresses for host-only paths.
@@ -143,6 +143,31 @@ def test_general_valid_layouts_pass_validation_without_gpu(gemm_lib):
                     M=1) in fine
     assert _general(gemm_lib, transa=1, M=16, K=64, A=PA, lda=16, C=PA + 4 * 1024,
                     ldc=32) in fine
+
+
+@pytest.mark.parametrize("args", [
+    dict(n=-1), dict(n=(1 << 40) + 1), dict(groups=-1), dict(groups=65536),
+    dict(out=0), dict(out=PC + 2), dict(x=0), dict(x=PA + 1),
+])
+def test_reduce_invalid_arguments_rejected(gemm_lib, args):
+    a = dict(n=1000, x=PA, out=PC, groups=0)
+    a.update(args)
+    assert gemm_lib.reduce_f32_sum(a["n"], a["x"], a["out"], a["groups"]) == gemm_lib.ERR_INVALID_ARG
+
+
+def test_reduce_alias_rejected(gemm_lib):
+    assert gemm_lib.reduce_f32_sum(1000, PA, PA + 4 * 999, 0) == gemm_lib.ERR_ALIAS
+    assert gemm_lib.reduce_f32_sum(1000, PA, PA + 4 * 500, 7) == gemm_lib.ERR_ALIAS
+
+
+def test_reduce_valid_call_without_gpu_fails_cleanly(gemm_lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    fine = (gemm_lib.ERR_LAUNCH, gemm_lib.ERR_UNSUPPORTED_DEVICE)
+    assert gemm_lib.reduce_f32_sum(1000, PA, PA + 4 * 1000, 0) in fine
+    assert gemm_lib.reduce_f32_sum(0, 0, PC, 0) in fine
 
 
 def test_valid_call_without_gpu_fails_cleanly(gemm_lib):
