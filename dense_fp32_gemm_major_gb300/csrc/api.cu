@@ -104,9 +104,12 @@ int validate(const GemmArgs &a, int mode, bool *noop) {
   return gemm::kOk;
 }
 
-// Kernel for (validated, non-empty) arguments, or -kErrInvalidArg.
-int select_kernel(const GemmArgs &a, int mode, int kernel) {
-  const bool tma_ok = gemm::tc_tma_legal(a);
+// Kernel for (validated, non-empty) arguments, or -kErrInvalidArg. With
+// can_pack the TMA-fed kernel serves any operands (those TMA cannot describe
+// are copied into a workspace first); without it (no allocation allowed)
+// only operands it can read as given.
+int select_kernel(const GemmArgs &a, int mode, int kernel, bool can_pack = true) {
+  const bool tma_ok = can_pack || gemm::tc_tma_direct(a);
   switch (kernel) {
     case GEMM_KERNEL_AUTO:
       if (mode == GEMM_F32_EXACT_SIMT) return GEMM_KERNEL_SIMT;
@@ -275,7 +278,7 @@ int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t ld
   bool noop = false;
   int st = validate(a, mode, &noop);
   if (st != gemm::kOk || noop) return st;
-  const int k = select_kernel(a, mode, GEMM_KERNEL_AUTO);
+  const int k = select_kernel(a, mode, GEMM_KERNEL_AUTO, /*can_pack=*/false);
   if (k < 0) return -k;
   int dev = 0, sms = 0;
   st = current_device(&dev, &sms);

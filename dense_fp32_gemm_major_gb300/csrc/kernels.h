@@ -34,18 +34,21 @@ enum : int {
   kErrAlias = 5,
 };
 
-// True when A and B can be described by TMA tensor maps: 16-byte aligned
-// base addresses and row pitches that are multiples of 16 bytes. A stored
-// transposed (opa) qualifies whatever its layout: tc_launch first copies it
-// into a row-major workspace that does.
-bool tc_tma_legal(const GemmArgs &a);
+// True when A and B as given can be described by TMA tensor maps: A not
+// stored transposed, 16-byte aligned base addresses and row pitches that are
+// multiples of 16 bytes.
+bool tc_tma_direct(const GemmArgs &a);
 
 // tcgen05 GEMM: exact = 3xTF32, else single-pass TF32; lsu = operands staged
-// by plain loads instead of TMA. Requires K >= 1, M >= 1, N >= 1.
+// by plain loads instead of TMA. The TMA-fed kernel takes any operands: those
+// that are not tc_tma_direct are first copied (A stored transposed:
+// transposed) into a workspace from the library's pool that is. Requires
+// K >= 1, M >= 1, N >= 1.
 int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream);
 
 // tc_launch with the stream-K workspace in the library's fixed scratch array
-// (no allocation). Returns kErrInvalidArg if the problem needs more scratch
+// (no allocation, so no operand copies: with lsu = false the operands must
+// be tc_tma_direct). Returns kErrInvalidArg if the problem needs more scratch
 // than GEMM_F32_NOALLOC_SCRATCH_BYTES.
 int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream);
 
@@ -65,6 +68,10 @@ int pool_free(void *ptr, cudaStream_t stream);
 int reduce_launch(int64_t n, const float *x, float *out, int groups, float *partials,
                   cudaStream_t stream);
 int reduce_default_groups(int sm_count);
+
+// dst (rows x cols, pitch ldd) = src (pitch lds), on `stream`. Sizes below 2^31.
+int pack_rows_launch(const float *src, int64_t lds, int64_t rows, int64_t cols, float *dst,
+                     int64_t ldd, int sm_count, cudaStream_t stream);
 
 // SIMT FP32 GEMM. Requires K >= 1, M >= 1, N >= 1.
 int simt_launch(const GemmArgs &a, cudaStream_t stream);

@@ -13,7 +13,9 @@
 // thread keeps four independent fp32 accumulators (the components of its
 // 128-bit loads) and has four 128-bit loads in flight, 16 KiB per CTA, which
 // covers the memory latency at full bandwidth. The tree runs on warp shuffles
-// (5 levels) and one shared-memory step across the 8 warps.
+// (5 levels) and one shared-memory step across the 8 warps. The second
+// dispatch is a programmatic dependent launch, so its start-up overlaps the
+// first grid's tail.
 //
 // Error: every element reaches the result through at most
 // h = ceil(n / (4 * 256 * G)) + ceil(G / 256) + 24 roundings (its
@@ -63,6 +65,9 @@ __device__ __forceinline__ float block_sum(float v) {
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
     reduce_partials_kernel(const float *__restrict__ x, long long n, float *__restrict__ partials) {
+  // Let the second dispatch be scheduled now; it waits for this grid to
+  // finish (and its writes to land) before it reads the partials.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long T = static_cast<long long>(gridDim.x) * kThreads;
   const long long t = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
   float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
@@ -110,6 +115,9 @@ __global__ void __launch_bounds__(kThreads)
 // g mod 256, then the tree) into *out.
 __global__ void __launch_bounds__(kThreads)
     reduce_final_kernel(const float *__restrict__ partials, int groups, float *__restrict__ out) {
+  // Launched as a programmatic dependent of the partial-sum grid: wait until
+  // that grid has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   float a = 0.0f;
   for (int g = threadIdx.x; g < groups; g += kThreads) a += partials[g];
   const float s = block_sum(a);
@@ -130,8 +138,21 @@ int reduce_launch(int64_t n, const float *x, float *out, int groups, float *part
   else
     reduce_partials_kernel<false><<<groups, kThreads, 0, stream>>>(x, n, partials);
   if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
-  reduce_final_kernel<<<1, kThreads, 0, stream>>>(partials, groups, out);
-  return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+  // The second dispatch as a programmatic dependent launch: its launch
+  // overlaps the tail of the first grid instead of following its completion.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, reduce_final_kernel, static_cast<const float *>(partials),
+                            groups, out) == cudaSuccess
+             ? kOk
+             : kErrLaunch;
 }
 
 }  // namespace gemm

@@ -1238,36 +1238,46 @@ int pool_free(void *ptr, cudaStream_t stream) {
   return cudaFreeAsync(ptr, stream) == cudaSuccess ? kOk : kErrLaunch;
 }
 
-bool tc_tma_legal(const GemmArgs &a) {
-  const bool a_ok = a.opa || (reinterpret_cast<uintptr_t>(a.A) % 16 == 0 && a.lda % 4 == 0);
-  return a_ok && reinterpret_cast<uintptr_t>(a.B) % 16 == 0 && a.ldb % 4 == 0;
+bool tc_tma_direct(const GemmArgs &a) {
+  return !a.opa && reinterpret_cast<uintptr_t>(a.A) % 16 == 0 && a.lda % 4 == 0 &&
+         reinterpret_cast<uintptr_t>(a.B) % 16 == 0 && a.ldb % 4 == 0;
 }
 
 int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream) {
-  // Stage shapes (BK x stages, picked by timing at 4096^3): exact 16 x 5 with
-  // A 16 KiB + B 8 KiB + A_lo 16 KiB per stage; tf32 32 x 4 with A 32 KiB +
-  // B 16 KiB. The LSU variants stage no B tile in shared memory.
-  if (a.opa && !lsu) {
-    // A stored transposed (K x M) for the TMA-fed kernel: rewrite it as a
-    // row-major M x K copy (16-byte pitch) in a workspace from the library's
-    // pool, ordered on the stream before the GEMM and released after it.
-    const int64_t ldt = (a.K + 3) / 4 * 4;
-    int dev = 0;
-    cudaMemPool_t pool = nullptr;
-    if (cudaGetDevice(&dev) != cudaSuccess || workspace_pool(dev, &pool) != kOk) return kErrLaunch;
+  if (!lsu && !tc_tma_direct(a)) {
+    // Operands TMA cannot describe as given: copy them into one workspace
+    // from the library's pool with 16-byte row pitches (A stored transposed,
+    // K x M, becomes a row-major M x K copy), ordered on the stream before
+    // the GEMM and released after it.
+    const bool a_ok = !a.opa && reinterpret_cast<uintptr_t>(a.A) % 16 == 0 && a.lda % 4 == 0;
+    const bool b_ok = reinterpret_cast<uintptr_t>(a.B) % 16 == 0 && a.ldb % 4 == 0;
+    auto up4 = [](int64_t x) { return (x + 3) / 4 * 4; };
+    auto up256 = [](size_t b) { return (b + 255) / 256 * 256; };
+    const int64_t b_rows = a.opb ? a.N : a.K, b_cols = a.opb ? a.K : a.N;
+    const int64_t lda_p = up4(a.K), ldb_p = up4(b_cols);
+    const size_t a_bytes = a_ok ? 0 : up256(static_cast<size_t>(a.M) * lda_p * 4);
+    const size_t b_bytes = b_ok ? 0 : up256(static_cast<size_t>(b_rows) * ldb_p * 4);
     void *ws = nullptr;
-    if (cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a.M) * ldt * 4, pool, stream) !=
-        cudaSuccess)
-      return kErrLaunch;
+    int st = pool_alloc(&ws, a_bytes + b_bytes, stream);
+    if (st != kOk) return st;
     GemmArgs t = a;
-    t.A = static_cast<const float *>(ws);
-    t.lda = ldt;
-    t.opa = 0;
-    int st = transpose_launch(a.A, a.lda, a.K, a.M, static_cast<float *>(ws), ldt, sm_count,
-                              stream);
+    if (!a_ok) {
+      float *pa = static_cast<float *>(ws);
+      st = a.opa ? transpose_launch(a.A, a.lda, a.K, a.M, pa, lda_p, sm_count, stream)
+                 : pack_rows_launch(a.A, a.lda, a.M, a.K, pa, lda_p, sm_count, stream);
+      t.A = pa;
+      t.lda = lda_p;
+      t.opa = 0;
+    }
+    if (st == kOk && !b_ok) {
+      float *pb = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + a_bytes);
+      st = pack_rows_launch(a.B, a.ldb, b_rows, b_cols, pb, ldb_p, sm_count, stream);
+      t.B = pb;
+      t.ldb = ldb_p;
+    }
     if (st == kOk) st = tc_launch(t, exact, false, sm_count, stream);
-    if (cudaFreeAsync(ws, stream) != cudaSuccess && st == kOk) st = kErrLaunch;
-    return st;
+    const int fst = pool_free(ws, stream);
+    return st != kOk ? st : fst;
   }
   if (a.opa) {
     // A stored transposed (K x M) for the LSU variant: the producer

@@ -78,7 +78,8 @@ typedef enum {
 typedef enum {
     GEMM_KERNEL_AUTO = 0,    /* what gemm_f32 picks */
     GEMM_KERNEL_SIMT = 1,    /* SIMT FP32 register-tiled kernel (exact modes only) */
-    GEMM_KERNEL_TC_TMA = 2,  /* tcgen05 kernel fed by TMA (needs TMA-legal A and B) */
+    GEMM_KERNEL_TC_TMA = 2,  /* tcgen05 kernel fed by TMA (operands copied first if TMA
+                                cannot read them as given; see gemm_f32_ex) */
     GEMM_KERNEL_TC_LSU = 3   /* tcgen05 kernel fed by plain loads (any strides) */
 } gemm_f32_kernel;
 
@@ -105,10 +106,15 @@ int gemm_f32(int64_t M, int64_t N, int64_t K,
  * gemm_f32_ex -- gemm_f32 with an explicit kernel choice (a gemm_f32_kernel).
  * GEMM_KERNEL_AUTO behaves exactly like gemm_f32. A kernel that cannot serve
  * the arguments returns GEMM_ERR_INVALID_ARG: GEMM_KERNEL_SIMT with mode
- * GEMM_F32_TF32 (it would change the accuracy class), or GEMM_KERNEL_TC_TMA
- * when A or B is not 16-byte aligned or lda, ldb is not a multiple of 4.
- * Mode GEMM_F32_EXACT with a tensor-core kernel forced runs 3xTF32 for every
- * K, including K < 16.
+ * GEMM_F32_TF32 (it would change the accuracy class). TMA reads operands
+ * whose base is 16-byte aligned and whose leading dimension is a multiple of
+ * 4; GEMM_KERNEL_TC_TMA (and AUTO, for the tensor-core modes) copies any
+ * other operand first into a workspace with that layout, taken from the
+ * library's stream-ordered pool on `stream` (rows x round_up(cols, 4) floats
+ * per copied operand) and returned behind the GEMM: one read and one write of
+ * the operand in HBM. GEMM_KERNEL_TC_LSU reads any layout in place with plain
+ * loads instead (slower per flop, no copy). Mode GEMM_F32_EXACT with a
+ * tensor-core kernel forced runs 3xTF32 for every K, including K < 16.
  */
 int gemm_f32_ex(int64_t M, int64_t N, int64_t K,
                 const float *A, int64_t lda,
@@ -154,10 +160,10 @@ typedef enum {
  * op(B)^T op(A)^T): the library swaps the operands and their flags. When a
  * row-major call has transa == GEMM_OP_T (column-major: transb ==
  * GEMM_OP_T), the TMA-fed tensor-core kernel (GEMM_KERNEL_TC_TMA, which AUTO
- * picks when B allows it) runs on a row-major copy of op(A) that a transpose
- * kernel writes first into a workspace of M x K floats (pitch rounded up to
- * 4) from the library's stream-ordered pool; GEMM_KERNEL_TC_LSU instead
- * transposes each tile of A as it stages it, with no workspace. Accuracy
+ * picks) runs on a row-major copy of op(A) that a transpose kernel writes
+ * first, like any operand TMA cannot read as given (see gemm_f32_ex);
+ * GEMM_KERNEL_TC_LSU instead transposes each tile of A as it stages it,
+ * with no workspace. Accuracy
  * classes apply to alpha * op(A) op(B) with S = |op(A)| |op(B)| scaled by
  * |alpha|, plus one rounding of the scale-and-add.
  * gemm_f32(...) is gemm_f32_general(GEMM_ROW_MAJOR, GEMM_OP_N, GEMM_OP_N,
@@ -222,7 +228,9 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K,
  *
  * Arguments, modes, layout and errors are those of gemm_f32 (device
  * pointers owned by the caller, stream ordered, non-blocking), and results
- * are the same. In addition it returns GEMM_ERR_INVALID_ARG, before
+ * are the same. It never copies operands into a workspace: those TMA
+ * cannot read as given (see gemm_f32_ex) go to the tensor-core kernel fed by
+ * plain loads. In addition it returns GEMM_ERR_INVALID_ARG, before
  * enqueuing anything, for a problem whose workspace would not fit in the
  * array. The workspace holds at most two 128 KiB partial tiles per SM plus a
  * few counters (under 39 MiB on a 152-SM GB300, whatever the shape), so on

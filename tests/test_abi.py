@@ -71,18 +71,20 @@ def test_kernel_selection(gemm_lib):
     # TMA-legal operands go to the TMA-fed tensor-core kernel in both TC modes
     assert sel(4096, 4096, 4096, PA, 4096, PB, 4096, PC, 4096, E, 0) == gemm_lib.KERNEL_TC_TMA
     assert sel(4096, 4096, 4096, PA, 4096, PB, 4096, PC, 4096, T, 0) == gemm_lib.KERNEL_TC_TMA
-    # the ragged workload (row pitches 3108 and 6124 bytes) is not TMA-legal
-    assert sel(1000, 1531, 777, PA, 777, PB, 1531, PC, 1531, E, 0) == gemm_lib.KERNEL_TC_LSU
-    assert sel(1000, 1531, 777, PA, 777, PB, 1531, PC, 1531, T, 0) == gemm_lib.KERNEL_TC_LSU
-    # misaligned base address also rules TMA out
-    assert sel(64, 64, 64, PA + 4, 64, PB, 64, PC, 64, T, 0) == gemm_lib.KERNEL_TC_LSU
+    # the ragged workload (row pitches 3108 and 6124 bytes, which TMA cannot
+    # read) and a misaligned base still take the TMA-fed kernel: the
+    # operands are copied into a workspace with 16-byte pitches first
+    assert sel(1000, 1531, 777, PA, 777, PB, 1531, PC, 1531, E, 0) == gemm_lib.KERNEL_TC_TMA
+    assert sel(1000, 1531, 777, PA, 777, PB, 1531, PC, 1531, T, 0) == gemm_lib.KERNEL_TC_TMA
+    assert sel(64, 64, 64, PA + 4, 64, PB, 64, PC, 64, T, 0) == gemm_lib.KERNEL_TC_TMA
     # exact mode with K < 16 uses the FP32 FMA kernel; EXACT_SIMT always does
     assert sel(64, 64, 15, PA, 16, PB, 64, PC, 64, E, 0) == gemm_lib.KERNEL_SIMT
     assert sel(64, 64, 16, PA, 16, PB, 64, PC, 64, E, 0) == gemm_lib.KERNEL_TC_TMA
     assert sel(4096, 4096, 4096, PA, 4096, PB, 4096, PC, 4096, S, 0) == gemm_lib.KERNEL_SIMT
-    # forced kernels: SIMT cannot serve TF32 (accuracy class), TMA needs legal strides
+    # forced kernels: SIMT cannot serve TF32 (accuracy class); TMA takes any
+    # strides (through the copy)
     assert sel(64, 64, 64, PA, 64, PB, 64, PC, 64, T, gemm_lib.KERNEL_SIMT) == -gemm_lib.ERR_INVALID_ARG
-    assert sel(64, 64, 64, PA, 65, PB, 64, PC, 64, T, gemm_lib.KERNEL_TC_TMA) == -gemm_lib.ERR_INVALID_ARG
+    assert sel(64, 64, 64, PA, 65, PB, 64, PC, 64, T, gemm_lib.KERNEL_TC_TMA) == gemm_lib.KERNEL_TC_TMA
     assert sel(64, 64, 64, PA, 64, PB, 64, PC, 64, E, gemm_lib.KERNEL_TC_LSU) == gemm_lib.KERNEL_TC_LSU
     assert sel(64, 64, 64, PA, 64, PB, 64, PC, 64, S, gemm_lib.KERNEL_TC_LSU) == -gemm_lib.ERR_INVALID_ARG
     assert sel(64, 64, 64, PA, 64, PB, 64, PC, 64, E, 9) == -gemm_lib.ERR_INVALID_ARG
@@ -107,7 +109,6 @@ def _general(gemm_lib, **kw):
     dict(order=1, lda=15), dict(order=1, lda=16, ldb=63), dict(order=1, lda=16, ldb=64, ldc=15),
     dict(order=1, transa=1, lda=63, ldb=64, ldc=16),   # A stored K x M column-major: lda >= K
     dict(mode=3), dict(kernel=9), dict(M=-1),
-    dict(transa=1, lda=16, kernel=2, B=PB + 4),        # TMA needs a 16-byte aligned B
     dict(transa=1, lda=16, mode=1, kernel=1),          # SIMT cannot serve TF32
 ])
 def test_general_invalid_arguments_rejected(gemm_lib, args):
@@ -134,6 +135,7 @@ def test_general_valid_layouts_pass_validation_without_gpu(gemm_lib):
     fine = (gemm_lib.ERR_LAUNCH, gemm_lib.ERR_UNSUPPORTED_DEVICE)
     assert _general(gemm_lib, transa=1, lda=16) in fine
     assert _general(gemm_lib, transa=1, lda=17, kernel=2) in fine  # A copied for the TMA kernel
+    assert _general(gemm_lib, transa=1, lda=16, kernel=2, B=PB + 4) in fine  # and B
     assert _general(gemm_lib, transb=1, ldb=64) in fine
     assert _general(gemm_lib, order=1, lda=16, ldb=64, ldc=16) in fine
     assert _general(gemm_lib, order=1, transa=1, transb=1, lda=64, ldb=32, ldc=16) in fine

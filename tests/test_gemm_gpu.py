@@ -112,16 +112,39 @@ def test_all_ones_closed_form(g, mode, kernel):
 
 
 @pytest.mark.parametrize("mode,kernel", [("exact", "tc_lsu"), ("tf32", "tc_lsu"), ("exact", "simt"),
-                                         ("exact", "auto"), ("tf32", "auto")])
+                                         ("exact", "auto"), ("tf32", "auto"), ("exact", "tc_tma"),
+                                         ("tf32", "tc_tma")])
 def test_ragged_strides_and_guard_bands(g, mode, kernel):
-    # odd leading dimensions (not TMA-legal), NaN padding in A and B, sentinel padding in C:
-    # padding must never be read into a result or written
+    # odd leading dimensions (TMA cannot read them: the TMA-fed kernel works on
+    # copies with 16-byte pitches), NaN padding in A and B, sentinel padding in
+    # C: padding must never be read into a result or written
     m, n, k = 203, 301, 117
     a, b = operands(m, n, k, "normal", seed=5)
     c, full = run(g, a, b, mode, kernel, lda=k + 3, ldb=n + 5, ldc=n + 7, c_fill=-12345.0)
     c64, s = oracle.gemm(a, b)
     check_within_bound(c, c64, s, k, mode, f"ragged {mode}/{kernel}")
     assert np.all(full[:, n:] == -12345.0), "write outside C's columns"
+
+
+@pytest.mark.parametrize("mode,kernel", [("exact", "auto"), ("tf32", "auto"), ("exact", "tc_lsu")])
+@pytest.mark.parametrize("off_a,off_b", [(1, 0), (0, 3), (2, 1)])
+def test_misaligned_bases(g, mode, kernel, off_a, off_b):
+    # A and B starting 4, 8 or 12 bytes past a 16-byte boundary, NaN before
+    # and after them: TMA cannot read them in place, so they are copied
+    m, n, k = 300, 260, 190
+    a, b = operands(m, n, k, "normal", seed=off_a * 4 + off_b)
+    ba = torch.full((m * k + 8,), float("nan"), device="cuda")
+    bb = torch.full((k * n + 8,), float("nan"), device="cuda")
+    ba[off_a:off_a + m * k] = torch.from_numpy(a.reshape(-1)).cuda()
+    bb[off_b:off_b + k * n] = torch.from_numpy(b.reshape(-1)).cuda()
+    dc = torch.full((m, n), float("nan"), device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    st = g.gemm_f32_ex(m, n, k, ba.data_ptr() + 4 * off_a, k, bb.data_ptr() + 4 * off_b, n,
+                       dc.data_ptr(), n, g.MODES[mode], g.KERNELS[kernel], s)
+    assert st == g.OK, g.gemm_f32_status_string(st)
+    assert g.gemm_f32_poll_device_status(s) == g.OK
+    c64, sc = oracle.gemm(a, b)
+    check_within_bound(dc.cpu().numpy(), c64, sc, k, mode, f"offsets {off_a},{off_b}")
 
 
 def test_ragged_sweep(g):
