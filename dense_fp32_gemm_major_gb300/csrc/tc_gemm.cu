@@ -128,10 +128,16 @@ __device__ __forceinline__ int split_slot(const TcParams &p, int s, int part) {
 // moves it into TMEM (hi and lo), as for B stored K x N: reading both hi/lo
 // operand pairs from shared memory would exceed the shared-memory bandwidth
 // that the split and the copies leave to the MMAs.
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB>
+// BST > 0 (TMA-fed, B stored K x N): the B tiles get a ring of their own, BST
+// slots, released as soon as the transform warps have moved B^T into TMEM
+// instead of when the MMAs are done with the stage; the A ring then holds
+// more stages in the same shared memory, which is what the pipeline needs
+// (it is bound by the round trip of a stage slot, not by bandwidth).
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, int BST = 0>
 struct TcConfig {
   static_assert(BK == 16 || BK == 32, "BK");
   static_assert(CL == 1 || (CL == 2 && !LSU), "clusters pair TMA-fed CTAs only");
+  static_assert(BST == 0 || (!LSU && !OPB), "a separate B ring: TMA-fed, B stored K x N");
   static constexpr bool kBtTmem = !OPB || (EXACT && !LSU);       // B^T operand in TMEM
   static constexpr int kAPartRows = kTM / CL;                    // A rows each CTA loads
   static constexpr int kAPartBytes = kAPartRows * BK * 4;
@@ -142,14 +148,16 @@ struct TcConfig {
   // B tile: row-major BK x 128 for TMA (OPB = false; LSU keeps none), or
   // K-major 128 x BK like A (OPB = true).
   static constexpr int kBBytes = (LSU && !OPB) ? 0 : BK * kTN * 4;
+  static constexpr int kBInStage = BST > 0 ? 0 : kBBytes;        // B tile bytes inside a stage
   // 3xTF32 lo tiles follow the hi (or raw) tiles at kLoOffset, same layout.
-  static constexpr int kLoOffset = kABytes + kBBytes;
+  static constexpr int kLoOffset = kABytes + kBInStage;
   static constexpr int kLoBytes = EXACT ? (kBtTmem ? kABytes : kABytes + kBBytes) : 0;
-  static constexpr int kStageBytes = kABytes + kBBytes + kLoBytes;
-  static constexpr int kBOffset = kABytes;
+  static constexpr int kStageBytes = kABytes + kBInStage + kLoBytes;
+  static constexpr int kBOffset = kABytes;                       // (BST == 0)
   static constexpr int kALoOffset = kLoOffset;
   static constexpr int kBLoOffset = kLoOffset + kABytes;         // OPB && EXACT
-  static constexpr int kTileBytes = STAGES * kStageBytes;
+  static constexpr int kBRingOffset = STAGES * kStageBytes;      // B ring (BST > 0)
+  static constexpr int kTileBytes = STAGES * kStageBytes + BST * kBBytes;
   static constexpr uint32_t kBtColsPerStage = kBtTmem ? (EXACT ? 2 * BK : BK) : 0;  // hi (+ lo)
   static constexpr int kAccBufs = kBtTmem ? 1 : 2;               // TMEM accumulators
   static constexpr int kProdWarps = LSU ? 4 : 1;
@@ -170,11 +178,13 @@ struct TcConfig {
                 "TMEM budget");
 };
 
-template <int STAGES>
+template <int STAGES, int BST = 0>
 struct alignas(8) TcShared {
   uint64_t full[STAGES];   // stage loaded (TMA bytes, or the LSU producer warps)
   uint64_t ready[STAGES];  // B^T in TMEM (and A split) by the transform warps
   uint64_t empty[STAGES];  // stage consumed by the MMAs (tcgen05.commit)
+  uint64_t bfull[BST > 0 ? BST : 1];   // B ring slot loaded (TMA bytes)
+  uint64_t bempty[BST > 0 ? BST : 1];  // B ring slot read by the transform warps
   uint64_t acc_full[2];    // accumulator complete (tcgen05.commit)
   uint64_t acc_empty[2];   // accumulator drained by the epilogue warps
   uint64_t drain;          // every MMA of this CTA has completed
@@ -471,16 +481,16 @@ __device__ __forceinline__ void stage_cols_lsu(uint8_t *tile, int lo_offset, con
   }
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA>
-__global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kThreads, 1)
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST>
+__global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
-  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>;
+  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>;
   static_assert(!OPA || LSU, "A stored transposed is staged by the LSU producer");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  TcShared<STAGES> *sh = reinterpret_cast<TcShared<STAGES> *>(tiles + Cfg::kTileBytes);
+  TcShared<STAGES, BST> *sh = reinterpret_cast<TcShared<STAGES, BST> *>(tiles + Cfg::kTileBytes);
   volatile int *abort = &sh->abort;
 
   const uint32_t warp = warp_index();
@@ -492,6 +502,10 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kTh
       mbar_init(&sh->full[s], LSU ? Cfg::kProdWarps : 1);
       mbar_init(&sh->ready[s], Cfg::kXformWarps > 0 ? Cfg::kXformWarps : 1);
       mbar_init(&sh->empty[s], CL);  // the MMAs of every CTA that writes this stage
+    }
+    for (int b = 0; b < BST; ++b) {
+      mbar_init(&sh->bfull[b], 1);
+      mbar_init(&sh->bempty[b], Cfg::kXformWarps);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh->acc_full[a], 1);
@@ -522,6 +536,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kTh
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
+      uint32_t bstage = 0, bphase = 0, barmed = 0, barmed_parity = 0;
       bool ok = true;
       UnitIter it(p);
       WorkUnit u;
@@ -536,18 +551,37 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kTh
           }
           uint8_t *st = tiles + stage * Cfg::kStageBytes;
           // The whole A tile arrives (each CTA of the cluster multicasts its
-          // rows to all of them) plus this CTA's own B tile.
-          mbar_arrive_expect_tx(&sh->full[stage], Cfg::kABytes + BK * kTN * 4);
+          // rows to all of them) plus this CTA's own B tile, unless B has a
+          // ring of its own.
+          mbar_arrive_expect_tx(&sh->full[stage], Cfg::kABytes + Cfg::kBInStage);
           if (CL > 1)
             tma_load_2d_multicast(st + rank * Cfg::kAPartBytes, &tmap_a, &sh->full[stage], kb * BK,
                                   mb * kTM + static_cast<int>(rank) * Cfg::kAPartRows,
                                   static_cast<uint16_t>((1u << CL) - 1));
           else
             tma_load_2d(st, &tmap_a, &sh->full[stage], kb * BK, mb * kTM);
-          if (OPB)
+          if (BST > 0) {
+            if (!mbar_wait_bounded(&sh->bempty[bstage], bphase ^ 1, p.timeout_ns, abort,
+                                   &g_tc_status)) {
+              ok = false;
+              armed |= 1u << stage;  // the A copy above is in flight
+              armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+              break;
+            }
+            mbar_arrive_expect_tx(&sh->bfull[bstage], Cfg::kBBytes);
+            tma_load_2d(tiles + Cfg::kBRingOffset + bstage * Cfg::kBBytes, &tmap_b,
+                        &sh->bfull[bstage], nb * kTN, kb * BK);
+            barmed |= 1u << bstage;
+            barmed_parity = (barmed_parity & ~(1u << bstage)) | (bphase << bstage);
+            if (++bstage == static_cast<uint32_t>(BST > 0 ? BST : 1)) {
+              bstage = 0;
+              bphase ^= 1;
+            }
+          } else if (OPB) {
             tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], kb * BK, nb * kTN);
-          else
+          } else {
             tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], nb * kTN, kb * BK);
+          }
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) {
@@ -560,6 +594,9 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kTh
         // Let every TMA copy this thread issued land before the CTA exits.
         for (int s = 0; s < STAGES; ++s)
           if (armed & (1u << s)) drain_wait(&sh->full[s], (armed_parity >> s) & 1u, p.timeout_ns);
+        for (int b = 0; b < BST; ++b)
+          if (barmed & (1u << b))
+            drain_wait(&sh->bfull[b], (barmed_parity >> b) & 1u, p.timeout_ns);
       }
     }
   } else if (LSU && warp < Cfg::kProdWarps) {
@@ -634,6 +671,13 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kTh
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           uint64_t *in_bar = Cfg::kXformWarps > 0 ? &sh->ready[stage] : &sh->full[stage];
           if (!mbar_wait_bounded(in_bar, phase, p.timeout_ns, abort, &g_tc_status)) {
+            ok = false;
+            break;
+          }
+          // With a separate B ring the one-pass transform does not wait for
+          // the A tile; the MMA does.
+          if (BST > 0 && !EXACT &&
+              !mbar_wait_bounded(&sh->full[stage], phase, p.timeout_ns, abort, &g_tc_status)) {
             ok = false;
             break;
           }
@@ -799,13 +843,23 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kTh
     const uint32_t quad = warp & 3;
     const uint32_t part = (warp - Cfg::kXformWarp0) >> 2;
     const int xt = threadIdx.x - Cfg::kXformWarp0 * 32;  // 0 .. 32 * kXformWarps - 1
-    uint32_t stage = 0, phase = 0;
+    uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
     bool ok = true;
     UnitIter it(p);
     WorkUnit u;
     while (ok && it.next(p, u)) {
       for (int kb = u.kb0; kb < u.kb1; ++kb) {
-        if (!warp_wait(&sh->full[stage], phase, p, abort)) {
+        if (BST > 0) {
+          // The B slot has landed and TMEM slot `stage` is free again (the
+          // MMAs of its previous round have completed: the stage's empty
+          // phase); 3xTF32 also splits the A tile, so it waits for it too.
+          if (!warp_wait(&sh->bfull[bstage], bphase, p, abort) ||
+              !warp_wait(&sh->empty[stage], phase ^ 1, p, abort) ||
+              (EXACT && !warp_wait(&sh->full[stage], phase, p, abort))) {
+            ok = false;
+            break;
+          }
+        } else if (!warp_wait(&sh->full[stage], phase, p, abort)) {
           ok = false;
           break;
         }
@@ -815,14 +869,25 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>::kTh
           // B tile is row-major BK k x 128 n (512-byte rows); this thread's
           // column n = 32 quad + lane becomes TMEM lane n.
           constexpr int kW = BK / Cfg::kXformParts;
-          const float *bs = reinterpret_cast<const float *>(st + Cfg::kBOffset) +
-                            part * kW * kTN + quad * 32 + lane;
+          const uint8_t *bslot =
+              BST > 0 ? tiles + Cfg::kBRingOffset + bstage * Cfg::kBBytes : st + Cfg::kBOffset;
+          const float *bs =
+              reinterpret_cast<const float *>(bslot) + part * kW * kTN + quad * 32 + lane;
           float v[kW];
 #pragma unroll
           for (int k = 0; k < kW; ++k) v[k] = bs[k * kTN];
           const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol +
                                stage * Cfg::kBtColsPerStage + part * kW;
           bt_to_tmem<kW, EXACT>(col, col + BK, v);
+          if (BST > 0) {
+            // The values are in registers: the B slot can be refilled.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh->bempty[bstage]);
+            if (++bstage == static_cast<uint32_t>(BST > 0 ? BST : 1)) {
+              bstage = 0;
+              bphase ^= 1;
+            }
+          }
         } else if (Cfg::kBtTmem) {
           // B tile is K-major 128 n x BK k (swizzled rows of BK * 4 bytes):
           // row n = 32 quad + lane holds this thread's TMEM lane, and part
@@ -1043,9 +1108,10 @@ Schedule make_schedule(int tiles, int kb, int sms, int min_chunk) {
 }
 
 // Everything a launch needs except the stream-K workspace.
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false>
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
+          int BST = 0>
 struct LaunchPlan {
-  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL, OPB>;
+  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>;
   TcParams p;
   Schedule sch;
   CUtensorMap map_a, map_b;
@@ -1053,8 +1119,8 @@ struct LaunchPlan {
   size_t counter_bytes = 0, partial_bytes = 0;  // workspace, 0 if no tile is split
 
   int prepare(const GemmArgs &a, int sm_count) {
-    auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA>;
-    smem_bytes = Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
+    auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST>;
+    smem_bytes = Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES, BST>)) + 1024;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kErrLaunch;
     static bool attr_set[64] = {};
@@ -1159,8 +1225,8 @@ struct LaunchPlan {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = CL > 1 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA>, map_a,
-                              map_b, p) ==
+    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST>,
+                              map_a, map_b, p) ==
                    cudaSuccess
                ? kOk
                : kErrLaunch;
@@ -1197,9 +1263,10 @@ int workspace_pool(int dev, cudaMemPool_t *out) {
   return kOk;
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false>
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
+          int BST = 0>
 int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
-  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA> plan;
+  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST> plan;
   int st = plan.prepare(a, sm_count);
   if (st != kOk) return st;
   // Split tiles need a workspace: partial tiles and one counter per split
@@ -1302,12 +1369,18 @@ int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_
     if (lsu) return launch_variant<32, 4, false, true, 1, true>(a, sm_count, stream);
     return launch_variant<32, 4, false, false, kClusterTf32, true>(a, sm_count, stream);
   }
+  // B stored K x N. Stage shapes picked by timing 4096^3 and 8192 x 11008 x
+  // 4096: exact BK = 16 x 5 stages of A 16 KiB + B 8 KiB + A_lo 16 KiB; tf32
+  // BK = 32 x 5 stages of A 32 KiB with B in a ring of its own (4 x 16 KiB,
+  // each slot free again once its B^T is in TMEM): 0.74 / 0.87 of the peak
+  // against 0.69 / 0.81 with B inside 4 stages. The exact variant, whose
+  // transform also splits A, loses with the separate ring.
   if (exact) {
     if (lsu) return launch_variant<16, 6, true, true, 1, false>(a, sm_count, stream);
     return launch_variant<16, 5, true, false, kClusterExact, false>(a, sm_count, stream);
   }
   if (lsu) return launch_variant<32, 6, false, true, 1, false>(a, sm_count, stream);
-  return launch_variant<32, 4, false, false, kClusterTf32, false>(a, sm_count, stream);
+  return launch_variant<32, 5, false, false, kClusterTf32, false, false, 4>(a, sm_count, stream);
 }
 
 int tc_poll_status(cudaStream_t stream) {
@@ -1366,14 +1439,14 @@ int noalloc_scratch(int dev, void **out) {
   return kOk;
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB>
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, int BST = 0>
 int launch_variant_noalloc(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return kErrLaunch;
   void *scratch = nullptr;
   int st = noalloc_scratch(dev, &scratch);
   if (st != kOk) return st;
-  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB> plan;
+  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, false, BST> plan;
   st = plan.prepare(a, sm_count);
   if (st != kOk) return st;
   // The same workspace layout gemm_f32 takes from the pool, here inside the
@@ -1397,7 +1470,7 @@ int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cud
     return launch_variant_noalloc<16, 5, true, false, kClusterExact, false>(a, sm_count, stream);
   }
   if (lsu) return launch_variant_noalloc<32, 6, false, true, 1, false>(a, sm_count, stream);
-  return launch_variant_noalloc<32, 4, false, false, kClusterTf32, false>(a, sm_count, stream);
+  return launch_variant_noalloc<32, 5, false, false, kClusterTf32, false, 4>(a, sm_count, stream);
 }
 
 }  // namespace gemm
