@@ -429,11 +429,18 @@ def main():
             ts, _ = time_steps(torch, gemm_call(mcode), steps, 5, flush, stream)
             ms = statistics.mean(ts)
             ach = mult * flops / (ms / 1e3) / 1e12
+            mk = g.gemm_f32_select(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N,
+                                   mcode, g.KERNEL_AUTO)
+            msuffix = "3xtf32" if mname == "exact" else "tf32"
+            mkname = {g.KERNEL_SIMT: "simt_gemm", g.KERNEL_TC_TMA: f"tc_gemm_tma_{msuffix}",
+                      g.KERNEL_TC_LSU: f"tc_gemm_lsu_{msuffix}"}.get(mk, str(mk))
+            mtraffic, _ = traffic_lookup(mkname, args.config, mname)
             extras[mname] = {"value": round(flops / (ms / 1e3) / 1e9, 1), "unit": "GFLOP/s",
                              "ms_per_step": round(ms, 4), "steps": steps,
                              "roofline": {"bound": bound, "achieved": round(ach, 2),
                                           "peak": round(peak, 1), "unit": "TFLOP/s",
-                                          "frac": round(ach / peak, 4)}}
+                                          "frac": round(ach / peak, 4), "traffic": mtraffic,
+                                          "kernel": mkname}}
         # the pages' second workload: the per-group tree reduction of 2^26 fp32
         # values (two dispatches), HBM-bound; the vector (256 MiB) exceeds L2,
         # so steps run back to back without a flush
