@@ -164,14 +164,33 @@ int run(const GemmArgs &a, int mode, int kernel, cudaStream_t stream) {
   }
 }
 
-// Per-device state of gemm_f32_host: a stream and grow-only device buffers.
+// Per-device state of gemm_f32_host: a compute stream, one stream per copy
+// direction, the events that chain row chunks through them, and grow-only
+// device buffers.
+constexpr int kHostMaxChunks = 16;
 struct HostState {
   std::mutex mu;
-  cudaStream_t stream = nullptr;
+  cudaStream_t stream = nullptr, h2d = nullptr, d2h = nullptr;
+  cudaEvent_t a_in[kHostMaxChunks] = {}, c_done[kHostMaxChunks] = {};
+  bool ready = false;
   float *buf = nullptr;
   size_t cap_bytes = 0;
 };
 HostState g_host[kMaxDevices];
+
+int host_state_init(HostState &hs) {
+  if (hs.ready) return gemm::kOk;
+  if (cudaStreamCreateWithFlags(&hs.stream, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&hs.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&hs.d2h, cudaStreamNonBlocking) != cudaSuccess)
+    return gemm::kErrLaunch;
+  for (int i = 0; i < kHostMaxChunks; ++i)
+    if (cudaEventCreateWithFlags(&hs.a_in[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hs.c_done[i], cudaEventDisableTiming) != cudaSuccess)
+      return gemm::kErrLaunch;
+  hs.ready = true;
+  return gemm::kOk;
+}
 
 int64_t round_up4(int64_t x) { return (x + 3) / 4 * 4; }
 
@@ -233,8 +252,8 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
 
   HostState &hs = g_host[dev];
   std::lock_guard<std::mutex> g(hs.mu);
-  if (!hs.stream && cudaStreamCreateWithFlags(&hs.stream, cudaStreamNonBlocking) != cudaSuccess)
-    return gemm::kErrLaunch;
+  st = host_state_init(hs);
+  if (st != gemm::kOk) return st;
 
   // Device layout: pitches padded to multiples of 4 elements (16 bytes), each
   // matrix starting on a 256-byte boundary.
@@ -256,19 +275,39 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
   float *dB = reinterpret_cast<float *>(base + bytes_a);
   float *dC = reinterpret_cast<float *>(base + bytes_a + bytes_b);
 
-  if (K > 0) {
-    if (cudaMemcpy2DAsync(dA, dlda * 4, A, lda * 4, K * 4, M, cudaMemcpyHostToDevice,
-                          hs.stream) != cudaSuccess ||
-        cudaMemcpy2DAsync(dB, dldb * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice,
-                          hs.stream) != cudaSuccess)
+  // Row chunks pipelined over three streams: B, then A chunk by chunk, go
+  // host to device on one; each chunk's GEMM starts on the compute stream as
+  // soon as its rows of A (and all of B) have landed; its rows of C go back
+  // on the third, so the copies of later and earlier chunks overlap the
+  // GEMM of this one. Chunks are whole 256-row tiles, at most
+  // kHostMaxChunks of them, and at least 512 rows (smaller GEMMs lose more
+  // to their fixed costs than the overlap gains).
+  int64_t chunk = (M + 7) / 8;
+  chunk = (chunk + 255) / 256 * 256;
+  if (chunk < 512) chunk = 512;
+  if ((M + chunk - 1) / chunk > kHostMaxChunks) chunk = (M + kHostMaxChunks - 1) / kHostMaxChunks;
+  const int nchunks = static_cast<int>((M + chunk - 1) / chunk);
+  if (K > 0 && cudaMemcpy2DAsync(dB, dldb * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice,
+                                 hs.h2d) != cudaSuccess)
+    return gemm::kErrLaunch;
+  for (int c = 0; c < nchunks; ++c) {
+    const int64_t r0 = c * chunk, rows = (M - r0 < chunk) ? M - r0 : chunk;
+    if (K > 0 && cudaMemcpy2DAsync(dA + r0 * dlda, dlda * 4, A + r0 * lda, lda * 4, K * 4, rows,
+                                   cudaMemcpyHostToDevice, hs.h2d) != cudaSuccess)
+      return gemm::kErrLaunch;
+    if (cudaEventRecord(hs.a_in[c], hs.h2d) != cudaSuccess ||
+        cudaStreamWaitEvent(hs.stream, hs.a_in[c], 0) != cudaSuccess)
+      return gemm::kErrLaunch;
+    const GemmArgs d{rows, N, K, dA + r0 * dlda, dlda, dB, dldb, dC + r0 * dldc, dldc};
+    st = run(d, mode, GEMM_KERNEL_AUTO, hs.stream);
+    if (st != gemm::kOk) return st;
+    if (cudaEventRecord(hs.c_done[c], hs.stream) != cudaSuccess ||
+        cudaStreamWaitEvent(hs.d2h, hs.c_done[c], 0) != cudaSuccess ||
+        cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, dC + r0 * dldc, dldc * 4, N * 4, rows,
+                          cudaMemcpyDeviceToHost, hs.d2h) != cudaSuccess)
       return gemm::kErrLaunch;
   }
-  const GemmArgs d{M, N, K, dA, dlda, dB, dldb, dC, dldc};
-  st = run(d, mode, GEMM_KERNEL_AUTO, hs.stream);
-  if (st != gemm::kOk) return st;
-  if (cudaMemcpy2DAsync(C, ldc * 4, dC, dldc * 4, N * 4, M, cudaMemcpyDeviceToHost, hs.stream) !=
-      cudaSuccess)
-    return gemm::kErrLaunch;
+  if (cudaStreamSynchronize(hs.d2h) != cudaSuccess) return gemm::kErrLaunch;
   return gemm::tc_poll_status(hs.stream);
 }
 

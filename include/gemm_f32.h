@@ -197,9 +197,16 @@ int gemm_f32_select(int64_t M, int64_t N, int64_t K,
  * Copies A and B to device buffers that the library owns and reuses (grown on
  * demand, one set per device, held until process exit), runs gemm_f32 on a
  * library-owned stream of the current device, copies C back and waits for
- * completion. Blocking. Same size, leading-dimension, mode and alias rules as
- * gemm_f32 (alias checked on the host ranges). Device-side leading dimensions
- * are padded to multiples of 4 so the TMA-fed kernels apply at any K and N.
+ * completion. Blocking. The work is split into row chunks of at least 512
+ * rows (at most 16 chunks): B and then each chunk of A go to the device on
+ * one stream, each chunk's GEMM starts when its rows have landed, and its
+ * rows of C come back on another stream while later chunks compute, so
+ * copies and compute overlap (page-locked host memory copies fastest).
+ * Results meet the accuracy class of the mode; they may differ in the last
+ * bits from one gemm_f32 call on the whole matrices, whose split of the work
+ * differs. Same size, leading-dimension, mode and alias rules as gemm_f32
+ * (alias checked on the host ranges). Device-side leading dimensions are
+ * padded to multiples of 4 so the TMA-fed kernels apply at any K and N.
  * Calls on one device are serialised by a lock.
  */
 int gemm_f32_host(int64_t M, int64_t N, int64_t K,

@@ -248,6 +248,28 @@ def test_host_entry_point(g):
         check_within_bound(c, c64, s, k, mode, f"host {mode} {m}x{n}x{k}")
 
 
+def test_host_entry_point_row_chunks(g):
+    # the host entry pipelines row chunks of A and C through two copy streams
+    # (512-row chunks and up: 3000 rows make six, the last one ragged)
+    for (m, n, k), mode in [((3000, 700, 300), "exact"), ((3000, 700, 300), "tf32"),
+                            ((8192, 64, 40), "exact_simt")]:
+        a, b = operands(m, n, k, "normal", seed=m + k)
+        c = g.matmul_host(a, b, mode)
+        c64, s = oracle.gemm(a, b)
+        check_within_bound(c, c64, s, k, mode, f"host chunks {mode} {m}x{n}x{k}")
+    # integers, bitwise, with strided host rows (views into wider arrays)
+    m, n, k = 2600, 333, 129
+    wa = np.full((m, k + 7), np.nan, np.float32)
+    wb = np.full((k, n + 3), np.nan, np.float32)
+    wc = np.full((m, n + 5), -3.0, np.float32)
+    wa[:, :k] = synth.small_integers((m, k), 91)
+    wb[:, :n] = synth.small_integers((k, n), 92)
+    for mode in ("exact", "tf32"):
+        g.matmul_host(wa[:, :k], wb[:, :n], mode, out=wc[:, :n])
+        assert np.array_equal(wc[:, :n].astype(np.float64), oracle.gemm(wa[:, :k], wb[:, :n])[0])
+        assert np.all(wc[:, n:] == -3.0), "write outside C's columns"
+
+
 def test_bounded_wait_times_out_cleanly(g):
     stream = torch.cuda.current_stream().cuda_stream
     assert g.gemm_f32_selftest_wait_timeout(20_000_000, stream) == g.ERR_TIMEOUT
