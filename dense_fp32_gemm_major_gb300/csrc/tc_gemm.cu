@@ -1056,8 +1056,12 @@ constexpr int kClusterExact = 2;
 constexpr int kClusterTf32 = 2;
 
 // Smallest stream-K chunk, in k: shorter chunks spend more time filling the
-// pipeline and more bytes on partial tiles than they save.
-constexpr int kMinChunkK = 256;
+// pipeline and more bytes on partial tiles than they save. One TF32 pass
+// does a third of the MMA work per k of 3xTF32, so splitting pays only for
+// longer chunks (measured on 512^3, 1024^3 and 1000 x 1531 x 777: 1024 k
+// before a split is worth it in tf32, 256 k in exact mode).
+constexpr int kMinChunkKExact = 256;
+constexpr int kMinChunkKTf32 = 1024;
 // Most CTAs sharing one split tile: the last of them sums every part alone.
 constexpr int kMaxSplit = 8;
 
@@ -1192,7 +1196,8 @@ struct LaunchPlan {
       }
       workers = workers_cached[dev];
     }
-    sch = make_schedule(p.num_tiles, p.num_k_blocks, workers, kMinChunkK / BK);
+    sch = make_schedule(p.num_tiles, p.num_k_blocks, workers,
+                        (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK);
     p.dp_tiles = sch.dp_tiles;
     p.sk_share = sch.sk_share;
     p.sk_ctas = sch.sk_ctas;
