@@ -197,8 +197,8 @@ int gemm_f32_select(int64_t M, int64_t N, int64_t K,
  * Copies A and B to device buffers that the library owns and reuses (grown on
  * demand, one set per device, held until process exit), runs gemm_f32 on a
  * library-owned stream of the current device, copies C back and waits for
- * completion. Blocking. The work is split into row chunks of at least 512
- * rows (at most 16 chunks): B and then each chunk of A go to the device on
+ * completion. Blocking. The work is split into row chunks (a quarter of M,
+ * at least 1024 rows): B and then each chunk of A go to the device on
  * one stream, each chunk's GEMM starts when its rows have landed, and its
  * rows of C come back on another stream while later chunks compute, so
  * copies and compute overlap (page-locked host memory copies fastest).

@@ -252,9 +252,9 @@ def test_host_entry_point(g):
 
 def test_host_entry_point_row_chunks(g):
     # the host entry pipelines row chunks of A and C through two copy streams
-    # (512-row chunks and up: 3000 rows make six, the last one ragged)
+    # (1024-row chunks and up: 3000 rows make three, the last one ragged)
     for (m, n, k), mode in [((3000, 700, 300), "exact"), ((3000, 700, 300), "tf32"),
-                            ((8192, 64, 40), "exact_simt")]:
+                            ((8192, 64, 40), "exact_simt"), ((5000, 260, 70), "exact")]:
         a, b = operands(m, n, k, "normal", seed=m + k)
         c = g.matmul_host(a, b, mode)
         c64, s = oracle.gemm(a, b)
