@@ -269,6 +269,16 @@ def oracle_rows_gflops(a, b, budget_s: float, max_rows: int | None = None):
     return flops / elapsed / 1e9, threads, rows_done, elapsed
 
 
+def check_result(torch, dC, rank):
+    """After the timed steps: every element of C was written (C was NaN-filled
+    before the first step) and is finite. Rank 0 only; the comparison with
+    the oracle is the tests' job."""
+    if rank != 0:
+        return None
+    finite = bool(torch.isfinite(dC).all().item())
+    return {"c_nan_filled_before_first_step": True, "all_finite_after_last_step": finite}
+
+
 def run_reference(args, rank):
     import synth
 
@@ -340,6 +350,8 @@ def main():
     dB = torch.from_numpy(np.ascontiguousarray(b.T) if transb else b).cuda()
     lda, ldb = dA.shape[1], dB.shape[1]
     dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    dA_lib = dA if not transa else dA.t()
+    dB_lib = dB if not transb else dB.t()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
@@ -371,6 +383,7 @@ def main():
     if sampler:
         sampler.start()
     fn = gemm_call(mode)
+    dC.fill_(float("nan"))  # every step overwrites C; checked after the last one
     for _ in range(args.warmup):
         flush.zero_()
         fn()
@@ -384,6 +397,9 @@ def main():
     st = g.gemm_f32_poll_device_status(sptr)
     if st != g.OK:
         raise g.GemmError(st, "device status")
+    check = check_result(torch, dC, rank)
+    if check is not None and not check["all_finite_after_last_step"]:
+        raise RuntimeError("C holds NaN/Inf after the timed steps")
 
     total_ms = reduce_max(sum(times), dist, "cuda")
     flops = 2.0 * M * N * K
@@ -441,6 +457,31 @@ def main():
                                           "peak": round(peak, 1), "unit": "TFLOP/s",
                                           "frac": round(ach / peak, 4), "traffic": mtraffic,
                                           "kernel": mkname}}
+        # context, not a denominator: the vendor library on the same workload
+        # (torch.matmul -> cuBLAS), one TF32 pass and full FP32
+        lib_ref = {}
+        tf32_flag = torch.backends.cuda.matmul.allow_tf32
+        for name, allow in (("cublas_tf32", True), ("cublas_fp32", False)):
+            torch.backends.cuda.matmul.allow_tf32 = allow
+            ref_out = torch.empty((M, N), dtype=torch.float32, device="cuda")
+            ts, _ = time_steps(torch, lambda: torch.matmul(dA_lib, dB_lib, out=ref_out), 50, 5,
+                               flush, stream)
+            lib_ref[name] = {"value": round(flops / (statistics.mean(ts) / 1e3) / 1e9, 1),
+                             "unit": "GFLOP/s", "ms_per_step": round(statistics.mean(ts), 4)}
+            del ref_out
+        torch.backends.cuda.matmul.allow_tf32 = tf32_flag
+        extras["library_reference"] = lib_ref
+        # context, not a denominator: what the TF32 tensor pipe and the FP32
+        # FMA pipe deliver to MMA-only / FFMA-only probe kernels here
+        pst, ptf32, pfp32 = g.gemm_f32_measure_peaks()
+        if pst == g.OK:
+            probe = {"tf32_mma_tflops": round(ptf32, 1), "fp32_fma_tflops": round(pfp32, 1),
+                     "note": "probe kernels (gemm_f32_measure_peaks); the roofline fractions "
+                             "stay against the measured bf16 peak x the nominal ratio"}
+            extras["probe_peaks"] = probe
+            pk_ctx = pfp32 if roofline["bound"] == "alu" else ptf32
+            roofline["probe_peak"] = round(pk_ctx, 1)
+            roofline["frac_of_probe_peak"] = round(roofline["achieved"] / pk_ctx, 4)
         # the pages' second workload: the per-group tree reduction of 2^26 fp32
         # values (two dispatches), HBM-bound; the vector (256 MiB) exceeds L2,
         # so steps run back to back without a flush
@@ -500,6 +541,7 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": args.steps,
+            "check": check,
             "clocks": clocks,
             "modes": extras,
             "timing": {"per_step_ms_median": round(statistics.median(times), 4),

@@ -78,6 +78,9 @@ def _load():
     lib.reduce_f32_sum.restype = i32
     lib.gemm_f32_status_string.argtypes = [i32]
     lib.gemm_f32_status_string.restype = ctypes.c_char_p
+    lib.gemm_f32_measure_peaks.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_double)]
+    lib.gemm_f32_measure_peaks.restype = i32
     lib.gemm_f32_poll_device_status.argtypes = [p]
     lib.gemm_f32_poll_device_status.restype = i32
     lib.gemm_f32_selftest_wait_timeout.argtypes = [i64, p]
@@ -147,6 +150,14 @@ def reduce_f32_sum(n, x, out, groups=0, stream=0) -> int:
 
 def gemm_f32_status_string(status: int) -> str:
     return _load().gemm_f32_status_string(status).decode()
+
+
+def gemm_f32_measure_peaks():
+    """(status, tf32_tflops, fp32_tflops) from the MMA-only and FFMA-only
+    probe kernels on the current device."""
+    t, f = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    st = _load().gemm_f32_measure_peaks(ctypes.byref(t), ctypes.byref(f))
+    return st, t.value, f.value
 
 
 def gemm_f32_poll_device_status(stream=0) -> int:

@@ -20,7 +20,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgemm_f32.so")
-SOURCES = ["api.cu", "simt_gemm.cu", "tc_gemm.cu", "transpose.cu", "pack.cu", "reduce.cu"]
+SOURCES = ["api.cu", "simt_gemm.cu", "tc_gemm.cu", "transpose.cu", "pack.cu", "reduce.cu",
+           "probe.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",

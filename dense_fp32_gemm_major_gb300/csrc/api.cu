@@ -377,6 +377,18 @@ const char *gemm_f32_status_string(int status) {
   }
 }
 
+int gemm_f32_measure_peaks(double *tf32_tflops, double *fp32_tflops) {
+  if (tf32_tflops == nullptr || fp32_tflops == nullptr) return GEMM_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  const int st = current_device(&dev, &sms);
+  if (st != gemm::kOk) return st;
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return GEMM_ERR_LAUNCH;
+  const int r = gemm::probe_peaks(sms, tf32_tflops, fp32_tflops, s);
+  cudaStreamDestroy(s);
+  return r;
+}
+
 int gemm_f32_poll_device_status(void *stream) {
   int dev = 0, sms = 0;
   const int st = current_device(&dev, &sms);

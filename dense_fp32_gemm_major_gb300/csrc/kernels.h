@@ -73,6 +73,10 @@ int reduce_default_groups(int sm_count);
 int pack_rows_launch(const float *src, int64_t lds, int64_t rows, int64_t cols, float *dst,
                      int64_t ldd, int sm_count, cudaStream_t stream);
 
+// Rates of the TF32 tensor pipe (MMA-only kernel) and of the FP32 FMA pipe
+// (FFMA-only kernel) on sm_count SMs, in TFLOP/s. Blocking.
+int probe_peaks(int sm_count, double *tf32_tflops, double *fp32_tflops, cudaStream_t stream);
+
 // SIMT FP32 GEMM. Requires K >= 1, M >= 1, N >= 1.
 int simt_launch(const GemmArgs &a, cudaStream_t stream);
 

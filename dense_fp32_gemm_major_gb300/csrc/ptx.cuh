@@ -49,15 +49,43 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                : "memory");
 }
 
+// Shared::cluster address of the mbarrier at the same offset as `bar` in
+// CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mbar_cluster_addr(uint64_t *bar, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(bar)), "r"(rank));
+  return remote;
+}
+
+// Arrive on the mbarrier at the same offset as `bar` in CTA `rank` of the
+// cluster, releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint64_t *bar, uint32_t rank) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   mbar_cluster_addr(bar, rank))
+               : "memory");
+}
+
+// CLUSTER: acquire at cluster scope, for phases completed by another CTA of
+// the cluster.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if (CLUSTER)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return done != 0;
 }
 
@@ -68,14 +96,15 @@ constexpr int kStatusTimeout = 4;
 // after `timeout_ns` of wall time, or as soon as another role of the CTA has
 // given up (`*abort` != 0). On giving up it sets *abort, records
 // kStatusTimeout in *status (first error wins) and returns false.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t timeout_ns, volatile int *abort,
                                                   int *status) {
   const uint32_t a = smem_addr(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  if (mbar_try_wait<CLUSTER>(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(a, parity)) return true;
     if ((it & 31u) == 0) {
       if (*abort) return false;
       if (global_timer_ns() - t0 > timeout_ns) {
@@ -133,6 +162,18 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// 2-D tiled load into this CTA's shared memory whose completion is signalled
+// on the mbarrier at shared::cluster address `bar_cluster`, which may belong
+// to the peer CTA of the pair (the CTA that issues the pair's MMAs).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst, const CUtensorMap *map,
+                                                 uint32_t bar_cluster, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
 // 2-D tiled load multicast to the CTAs of the cluster in `mask`: the box lands
 // at the same shared-memory offset in each of them and completes on the
 // mbarrier at the same offset in each of them.
@@ -164,22 +205,44 @@ __device__ __forceinline__ void cluster_sync() {
 
 // ---------------------------------------------------------------- tcgen05 --
 
+// The tcgen05 instructions below take the CTA group G: 1 (this CTA's tensor
+// core and TMEM) or 2 (the CTA pair of a cluster acting as one: allocation is
+// made by one warp in each CTA of the pair and yields the same address in
+// both; an MMA issued by the even CTA spans both CTAs' TMEM and shared-memory
+// operands).
+
 // Allocate `ncols` TMEM columns (power of two >= 32); the base address is
 // written to *slot. Whole warp.
+template <int G = 1>
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_addr(slot)),
-               "r"(ncols)
-               : "memory");
+  if (G == 2)
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
 }
 
+template <int G = 1>
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if (G == 2)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <int G = 1>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
+  if (G == 2)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before_sync() {
@@ -190,15 +253,26 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem], kind::tf32, issued by one thread.
+// D[tmem] (+)= A[smem] * B[smem], kind::tf32, issued by one thread. With G = 2
+// (M = 256) each CTA of the pair holds rows 128 r .. 128 r + 127 of A and of
+// D and half of B's N columns behind the same descriptors and addresses.
+template <int G = 1>
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if (G == 2)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem], kind::tf32: A is read from TMEM (lane = row
@@ -223,13 +297,21 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 }
 
 // As mma_commit, arriving on the mbarrier at the same offset in every CTA of
-// the cluster in `mask`.
+// the cluster in `mask` (G: the group of the MMAs tracked).
+template <int G = 1>
 __device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_addr(bar)),
-      "h"(mask)
-      : "memory");
+  if (G == 2)
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_addr(bar)),
+        "h"(mask)
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_addr(bar)),
+        "h"(mask)
+        : "memory");
 }
 
 // Warp-wide TMEM load: lane l of the warp receives 32 consecutive 32-bit
@@ -299,6 +381,9 @@ __device__ __forceinline__ void tmem_load_wait() {
 // and stride byte offsets (all >> 4), the fixed descriptor version 1 at bit
 // 46, base offset 0 (stage tiles are 1024-byte aligned) and the layout type
 // in bits 61..63 (0 none, 2 = 128-byte swizzle, 4 = 64-byte, 6 = 32-byte).
+// Layout codes (bits 61-63): 2 = 128-byte swizzle, 4 = 64-byte swizzle,
+// 1 = 128-byte swizzle of 32-byte atoms (the layout an MN-major TF32 operand
+// needs: TMA writes it with CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint32_t layout) {
   uint64_t d = 0;

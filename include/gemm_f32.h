@@ -256,6 +256,17 @@ int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
                      float *C, int64_t ldc,
                      int mode, void *stream);
 
+/*
+ * gemm_f32_measure_peaks -- measurement helper, not part of any computation:
+ * runs an MMA-only kernel (tcgen05.mma kind::tf32, 128 x 256 x 8, operands
+ * resident in shared memory, one CTA per SM) and an FFMA-only kernel
+ * (independent fused multiply-add chains, 1024 threads per SM) on the
+ * current device and returns the rates they reach, in TFLOP/s, through the
+ * two pointers (host memory). Blocking; takes a fraction of a second. The
+ * pages have no counterpart: they time their kernels against no peak.
+ */
+int gemm_f32_measure_peaks(double *tf32_tflops, double *fp32_tflops);
+
 /* gemm_f32_status_string -- static, NUL-terminated name of a status code. */
 const char *gemm_f32_status_string(int status);
 

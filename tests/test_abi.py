@@ -9,7 +9,7 @@ import pytest
 EXPECTED = {
     "gemm_f32", "gemm_f32_ex", "gemm_f32_select", "gemm_f32_host", "gemm_f32_status_string",
     "gemm_f32_poll_device_status", "gemm_f32_selftest_wait_timeout", "gemm_f32_noalloc",
-    "gemm_f32_general", "reduce_f32_sum",
+    "gemm_f32_general", "reduce_f32_sum", "gemm_f32_measure_peaks",
 }
 
 # Fake, never dereferenced, 256-byte aligned "device" addresses for host-only paths.
@@ -170,6 +170,15 @@ def test_reduce_valid_call_without_gpu_fails_cleanly(gemm_lib):
     fine = (gemm_lib.ERR_LAUNCH, gemm_lib.ERR_UNSUPPORTED_DEVICE)
     assert gemm_lib.reduce_f32_sum(1000, PA, PA + 4 * 1000, 0) in fine
     assert gemm_lib.reduce_f32_sum(0, 0, PC, 0) in fine
+
+
+def test_measure_peaks_without_gpu_fails_cleanly(gemm_lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st, _, _ = gemm_lib.gemm_f32_measure_peaks()
+    assert st in (gemm_lib.ERR_LAUNCH, gemm_lib.ERR_UNSUPPORTED_DEVICE)
 
 
 def test_valid_call_without_gpu_fails_cleanly(gemm_lib):

@@ -272,6 +272,16 @@ def test_host_entry_point_row_chunks(g):
         assert np.all(wc[:, n:] == -3.0), "write outside C's columns"
 
 
+def test_probe_peaks_are_plausible(g):
+    # MMA-only and FFMA-only probe kernels: rates between half and twice the
+    # nominal GB300 figures (1.1 PFLOP/s dense TF32; 152 SMs x 128 lanes x 2
+    # flops x 2.07 GHz = 80.5 TFLOP/s FP32)
+    st, tf32, fp32 = g.gemm_f32_measure_peaks()
+    assert st == g.OK, g.gemm_f32_status_string(st)
+    assert 550.0 < tf32 < 2200.0, tf32
+    assert 40.0 < fp32 < 161.0, fp32
+
+
 def test_bounded_wait_times_out_cleanly(g):
     stream = torch.cuda.current_stream().cuda_stream
     assert g.gemm_f32_selftest_wait_timeout(20_000_000, stream) == g.ERR_TIMEOUT
