@@ -481,6 +481,121 @@ __device__ __forceinline__ void stage_cols_lsu(uint8_t *tile, int lo_offset, con
   }
 }
 
+// Epilogue role: four warps (EPI_WARP0 ..) take each finished accumulator
+// of the CTA's work list out of TMEM (lane = n, column = m) and either store
+// it to C or, for a part of a split tile, to its partial-sum slot; the last
+// part to finish sums all parts in order. PAIR: the accumulator's empty
+// barrier belongs to the even CTA of the pair, which issues the MMAs of both.
+template <int ACC_BUFS, int EPI_WARP0, bool PAIR, class Shared>
+__device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uint32_t tmem,
+                                              uint32_t warp, uint32_t lane, uint32_t rank,
+                                              volatile int *abort) {
+  auto release_acc = [](uint64_t *bar) {
+    if (PAIR)
+      mbar_arrive_cluster(bar, 0);
+    else
+      mbar_arrive(bar);
+  };
+  const uint32_t quad = warp & 3;  // TMEM lanes (columns of C) this warp may read
+  uint32_t acc = 0, acc_phase = 0;
+  UnitIter it(p);
+  WorkUnit u;
+  while (it.next(p, u)) {
+    int mb, nb;
+    tile_coords(p, u.tile, rank, mb, nb);
+    // The four epilogue warps continue or give up together: the split-tile
+    // path below synchronises them with named barriers.
+    if (!named_barrier_and(1, 128, warp_wait(&sh->acc_full[acc], acc_phase, p, abort))) break;
+    tc_fence_after_sync();
+    const int n_loc = quad * 32 + lane;
+    const int gn = nb * kTN + n_loc;
+    const bool n_ok = gn < p.N;
+    const uint32_t t_lane = tmem + ((quad * 32) << 16) + kAccCol + acc * kTM;
+    if (u.nparts == 1) {
+      // Whole tile: straight to C.
+#pragma unroll 1
+      for (int c = 0; c < kTM / 32; ++c) {
+        const int gm0 = mb * kTM + c * 32;
+        if (gm0 >= p.M) break;
+        uint32_t r[32];
+        tmem_load_32cols(t_lane + c * 32, r);
+        tmem_load_wait();
+        float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
+        const int rows = min(32, p.M - gm0);
+        if (n_ok) {
+          if (p.alpha == 1.0f && p.beta == 0.0f) {
+            if (rows == 32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < rows) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < rows) {
+                float *d = dst + static_cast<long long>(j) * p.ldc;
+                *d = scale_out(p, __uint_as_float(r[j]), d);
+              }
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) release_acc(&sh->acc_empty[acc]);
+    } else {
+      // Split tile: write this part's partial sums ([m][n], pitch kTN) to
+      // its slot and free the accumulator; the last part to finish sums all
+      // parts in part order (a fixed order, so results are deterministic)
+      // and writes C.
+      const long long slot_elems = static_cast<long long>(kTM) * kTN;
+      float *slot =
+          p.sk_partials + (static_cast<long long>(u.slot) * p.cl + rank) * slot_elems;
+#pragma unroll 1
+      for (int c = 0; c < kTM / 32; ++c) {
+        uint32_t r[32];
+        tmem_load_32cols(t_lane + c * 32, r);
+        tmem_load_wait();
+        float *dst = slot + (c * 32) * kTN + n_loc;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[j * kTN] = __uint_as_float(r[j]);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) release_acc(&sh->acc_empty[acc]);
+      __threadfence();
+      named_barrier_sync(1, 128);
+      if (warp == EPI_WARP0 && lane == 0)
+        sh->sk_last = atomicAdd(&p.sk_counters[u.sk_tile * p.cl + rank], 1u) ==
+                      static_cast<unsigned>(u.nparts - 1);
+      named_barrier_sync(1, 128);
+      if (sh->sk_last) {
+        if (it.done(p)) {
+          // The CTA's final unit: every warp sums it after the role loops.
+          if (warp == EPI_WARP0 && lane == 0) {
+            sh->fix_tile = u.sk_tile;
+            sh->fix_nparts = u.nparts;
+            sh->fix_mb = mb;
+            sh->fix_nb = nb;
+          }
+        } else {
+          __threadfence();
+          epilogue_fixup(p, u.sk_tile, rank, u.nparts, mb, nb, threadIdx.x - EPI_WARP0 * 32,
+                         128);
+        }
+      }
+      named_barrier_sync(1, 128);  // sk_last is reused by the next split tile
+    }
+    if (++acc == ACC_BUFS) {
+      acc = 0;
+      acc_phase ^= 1;
+    }
+  }
+}
+
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST>
 __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -738,104 +853,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
     __syncwarp();
   } else if (warp >= Cfg::kEpiWarp0 && warp < Cfg::kEpiWarp0 + 4) {
     // --------------------------------------------------------- epilogue --
-    const uint32_t quad = warp & 3;  // TMEM lanes (columns of C) this warp may read
-    uint32_t acc = 0, acc_phase = 0;
-    UnitIter it(p);
-    WorkUnit u;
-    while (it.next(p, u)) {
-      int mb, nb;
-      tile_coords(p, u.tile, rank, mb, nb);
-      // The four epilogue warps continue or give up together: the split-tile
-      // path below synchronises them with named barriers.
-      if (!named_barrier_and(1, 128, warp_wait(&sh->acc_full[acc], acc_phase, p, abort))) break;
-      tc_fence_after_sync();
-      const int n_loc = quad * 32 + lane;
-      const int gn = nb * kTN + n_loc;
-      const bool n_ok = gn < p.N;
-      const uint32_t t_lane = tmem + ((quad * 32) << 16) + kAccCol + acc * kTM;
-      if (u.nparts == 1) {
-        // Whole tile: straight to C.
-#pragma unroll 1
-        for (int c = 0; c < kTM / 32; ++c) {
-          const int gm0 = mb * kTM + c * 32;
-          if (gm0 >= p.M) break;
-          uint32_t r[32];
-          tmem_load_32cols(t_lane + c * 32, r);
-          tmem_load_wait();
-          float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
-          const int rows = min(32, p.M - gm0);
-          if (n_ok) {
-            if (p.alpha == 1.0f && p.beta == 0.0f) {
-              if (rows == 32) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
-              } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  if (j < rows) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < rows) {
-                  float *d = dst + static_cast<long long>(j) * p.ldc;
-                  *d = scale_out(p, __uint_as_float(r[j]), d);
-                }
-            }
-          }
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
-      } else {
-        // Split tile: write this part's partial sums ([m][n], pitch kTN) to
-        // its slot and free the accumulator; the last part to finish sums all
-        // parts in part order (a fixed order, so results are deterministic)
-        // and writes C.
-        const long long slot_elems = static_cast<long long>(kTM) * kTN;
-        float *slot =
-            p.sk_partials + (static_cast<long long>(u.slot) * p.cl + rank) * slot_elems;
-#pragma unroll 1
-        for (int c = 0; c < kTM / 32; ++c) {
-          uint32_t r[32];
-          tmem_load_32cols(t_lane + c * 32, r);
-          tmem_load_wait();
-          float *dst = slot + (c * 32) * kTN + n_loc;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) dst[j * kTN] = __uint_as_float(r[j]);
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->acc_empty[acc]);
-        __threadfence();
-        named_barrier_sync(1, 128);
-        if (warp == Cfg::kEpiWarp0 && lane == 0)
-          sh->sk_last = atomicAdd(&p.sk_counters[u.sk_tile * p.cl + rank], 1u) ==
-                        static_cast<unsigned>(u.nparts - 1);
-        named_barrier_sync(1, 128);
-        if (sh->sk_last) {
-          if (it.done(p)) {
-            // The CTA's final unit: every warp sums it after the role loops.
-            if (warp == Cfg::kEpiWarp0 && lane == 0) {
-              sh->fix_tile = u.sk_tile;
-              sh->fix_nparts = u.nparts;
-              sh->fix_mb = mb;
-              sh->fix_nb = nb;
-            }
-          } else {
-            __threadfence();
-            epilogue_fixup(p, u.sk_tile, rank, u.nparts, mb, nb, threadIdx.x - Cfg::kEpiWarp0 * 32,
-                           128);
-          }
-        }
-        named_barrier_sync(1, 128);  // sk_last is reused by the next split tile
-      }
-      if (++acc == Cfg::kAccBufs) {
-        acc = 0;
-        acc_phase ^= 1;
-      }
-    }
+    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, false>(p, sh, tmem, warp, lane, rank, abort);
   } else if (Cfg::kXformWarps > 0 && warp >= Cfg::kXformWarp0) {
     // -------------------------------------------- transform (TMA variant) --
     // Warp (quad, part) moves k in [part * W, (part + 1) * W), W = BK / parts,
@@ -958,6 +976,218 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
   }
   // No CTA of a cluster leaves while its peer may still signal its barriers.
   if (CL > 1) cluster_sync();
+}
+
+// ------------------------------------------------------ CTA-pair kernel --
+//
+// Single-pass TF32 on the two SMs of a cluster acting as one tensor core
+// (tcgen05 cta_group::2). The pair computes one unit tile, 256 n x 256 m of
+// C^T, with one MMA stream issued by the even CTA: M = 256 (the MMA's A
+// operand is B_tile^T, CTA r holding n rows 128 r .. 128 r + 127), N = 256
+// (the MMA's B operand is the A tile, CTA r holding m rows 128 r ..) and
+// K = 8. Each CTA's TMEM accumulates its own 128 n x 256 m, which is the
+// output tile the multicast pairs of tc_gemm_kernel give that CTA, so the
+// schedule, epilogue and split-tile sums are shared with it.
+//
+// Both operands go from global memory to the tensor core by TMA alone: a
+// K-major operand (A stored M x K, B stored N x K) as a box of BK k x 128
+// rows with the 128-byte swizzle, an MN-major one (B stored K x N, A stored
+// K x M) as four boxes of 32 mn x BK k with the 128-byte swizzle of 32-byte
+// atoms, the layout kind::tf32 takes for MN-major operands. Each CTA's
+// copies complete on the even CTA's stage barrier (which expects the bytes
+// of both), the even CTA's commits release the stage in both, and nothing
+// else crosses the pair per stage; the odd CTA's epilogue returns each
+// accumulator to the even CTA once per tile.
+template <int BK, int STAGES, bool OPA, bool OPB>
+struct PairConfig {
+  static_assert(BK == 32, "128-byte rows: one swizzle span per operand row");
+  static constexpr int kHalfRows = 128;                          // rows of each operand per CTA
+  static constexpr int kOpBytes = kHalfRows * BK * 4;            // one operand tile per CTA
+  static constexpr int kAOffset = 0;                             // A rows (the MMA's B operand)
+  static constexpr int kBtOffset = kOpBytes;                     // B^T rows (the MMA's A operand)
+  static constexpr int kStageBytes = 2 * kOpBytes;
+  static constexpr int kTileBytes = STAGES * kStageBytes;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kMmaWarp = 1;
+  static constexpr int kEpiWarp0 = 2;
+  static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
+  // A operand (B^T) MN-major when B is stored K x N; B operand (A tile)
+  // MN-major when A is stored K x M.
+  static constexpr uint32_t kIdesc =
+      idesc_tf32(2 * kTN, kTM) | (OPB ? 0u : 1u << 15) | (OPA ? 1u << 16 : 0u);
+  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(kAccBufs * kTM <= static_cast<int>(kTmemCols), "TMEM budget");
+};
+
+// Shared-memory descriptor of k-step kk of an operand tile: K-major rows of
+// 128 bytes (8-row swizzle atoms 1024 bytes apart, a k-step 32 bytes along
+// the row), or MN-major chunks of 32 mn (kMnChunkBytes apart, 4-row groups
+// 512 bytes apart, a k-step of 8 rows 1024 bytes on).
+template <int BK, bool MN>
+__device__ __forceinline__ uint64_t pair_operand_desc(uint32_t base, int kk) {
+  if (MN) return smem_desc(base + kk * 1024, BK * 128, 512, 1);
+  return smem_desc(base + kk * 32, 16, 1024, 2);
+}
+
+// Load this CTA's 128 rows x BK k of an operand whose rows start at `row0`
+// (k from k0) into `dst`, completing on the even CTA's barrier `bar`.
+template <int BK, bool MN>
+__device__ __forceinline__ void pair_load_operand(uint8_t *dst, const CUtensorMap *map,
+                                                  uint32_t bar, int row0, int k0) {
+  if (MN) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_2d_pair(dst + c * BK * 128, map, bar, row0 + 32 * c, k0);
+  } else {
+    tma_load_2d_pair(dst, map, bar, k0, row0);
+  }
+}
+
+template <int BK, int STAGES, bool OPA, bool OPB>
+__global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
+    tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
+  using Cfg = PairConfig<BK, STAGES, OPA, OPB>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *tiles = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  TcShared<STAGES> *sh = reinterpret_cast<TcShared<STAGES> *>(tiles + Cfg::kTileBytes);
+  volatile int *abort = &sh->abort;
+
+  const uint32_t warp = warp_index();
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sh->full[s], 1);   // even CTA: its producer's expect-tx; both CTAs' bytes
+      mbar_init(&sh->empty[s], 1);  // the even CTA's commit, multicast to both
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh->acc_full[a], 1);
+      mbar_init(&sh->acc_empty[a], 8);  // even CTA: the four epilogue warps of each CTA
+    }
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    sh->fix_tile = -1;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmap_a);
+    tma_prefetch_map(&tmap_b);
+  }
+  if (warp == Cfg::kMmaWarp) {
+    tmem_alloc<2>(&sh->tmem_base, kTmemCols);
+    tmem_relinquish<2>();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // barriers and TMEM of both CTAs set up before either signals the other
+  tc_fence_after_sync();
+  const uint32_t tmem = sh->tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer --
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
+      bool ok = true;
+      UnitIter it(p);
+      WorkUnit u;
+      while (ok && it.next(p, u)) {
+        int mb, nb;
+        tile_coords(p, u.tile, rank, mb, nb);
+        const int m0 = mb * kTM + static_cast<int>(rank) * Cfg::kHalfRows;
+        const int n0 = nb * kTN;
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          if (!mbar_wait_bounded(&sh->empty[stage], phase ^ 1, p.timeout_ns, abort,
+                                 &g_tc_status)) {
+            ok = false;
+            break;
+          }
+          uint8_t *st = tiles + stage * Cfg::kStageBytes;
+          const uint32_t bar = mbar_cluster_addr(&sh->full[stage], 0);
+          if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * Cfg::kStageBytes);
+          pair_load_operand<BK, OPA>(st + Cfg::kAOffset, &tmap_a, bar, m0, kb * BK);
+          pair_load_operand<BK, !OPB>(st + Cfg::kBtOffset, &tmap_b, bar, n0, kb * BK);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // On a timeout the even CTA lets the stages it armed land (both CTAs'
+      // copies complete there) before the pair exits.
+      if (!ok && rank == 0)
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) drain_wait(&sh->full[s], (armed_parity >> s) & 1u, p.timeout_ns);
+    }
+  } else if (warp == Cfg::kMmaWarp) {
+    // ------------------------------------------------- MMA (even CTA) --
+    if (rank == 0 && lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      UnitIter it(p);
+      WorkUnit u;
+      while (ok && it.next(p, u)) {
+        // Both CTAs' epilogues have drained this accumulator (the odd one's
+        // arrivals come from the peer: acquire at cluster scope).
+        if (!mbar_wait_bounded<true>(&sh->acc_empty[acc], acc_phase ^ 1, p.timeout_ns, abort,
+                                     &g_tc_status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + kAccCol + acc * kTM;
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          if (!mbar_wait_bounded(&sh->full[stage], phase, p.timeout_ns, abort, &g_tc_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t st = smem_addr(tiles + stage * Cfg::kStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / kUmmaK; ++kk)
+            mma_tf32<2>(d_tmem, pair_operand_desc<BK, !OPB>(st + Cfg::kBtOffset, kk),
+                        pair_operand_desc<BK, OPA>(st + Cfg::kAOffset, kk), Cfg::kIdesc,
+                        (kb != u.kb0 || kk != 0) ? 1u : 0u);
+          mma_commit_multicast<2>(&sh->empty[stage], 3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit_multicast<2>(&sh->acc_full[acc], 3);
+        if (++acc == Cfg::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // Every MMA this thread issued completes before TMEM is released.
+      mma_commit_multicast<2>(&sh->drain, 1);
+      drain_wait(&sh->drain, 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------------- epilogue --
+    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, true>(p, sh, tmem, warp, lane, rank, abort);
+  }
+
+  // Neither CTA frees its TMEM or leaves while the pair's MMAs, copies or
+  // arrivals may still reach it.
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  if (warp == Cfg::kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc<2>(tmem, kTmemCols);
+  }
+  if (sh->fix_tile >= 0 && !sh->abort) {
+    __threadfence();
+    epilogue_fixup(p, sh->fix_tile, rank, sh->fix_nparts, sh->fix_mb, sh->fix_nb, threadIdx.x,
+                   blockDim.x);
+  }
 }
 
 // One warp waits, bounded, on a barrier that is never signalled.
@@ -1111,11 +1341,32 @@ Schedule make_schedule(int tiles, int kb, int sms, int min_chunk) {
   return s;
 }
 
+// The kernel a launch plan runs: tc_gemm_kernel, or with PAIR the CTA-pair
+// TF32 kernel (which takes every operand layout by TMA directly).
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST, bool PAIR>
+struct KernelOf {
+  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>;
+  static constexpr int kThreads = Cfg::kThreads;
+  static constexpr int kSmemBytes =
+      Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES, BST>)) + 1024;
+  static constexpr auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST>;
+};
+
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST>
+struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true> {
+  static_assert(!EXACT && !LSU && CL == 2 && BST == 0, "the pair kernel: one TF32 pass, TMA");
+  using Cfg = PairConfig<BK, STAGES, OPA, OPB>;
+  static constexpr int kThreads = Cfg::kThreads;
+  static constexpr int kSmemBytes =
+      Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
+  static constexpr auto kernel = tc_pair_kernel<BK, STAGES, OPA, OPB>;
+};
+
 // Everything a launch needs except the stream-K workspace.
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
-          int BST = 0>
+          int BST = 0, bool PAIR = false>
 struct LaunchPlan {
-  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>;
+  using K = KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR>;
   TcParams p;
   Schedule sch;
   CUtensorMap map_a, map_b;
@@ -1123,8 +1374,8 @@ struct LaunchPlan {
   size_t counter_bytes = 0, partial_bytes = 0;  // workspace, 0 if no tile is split
 
   int prepare(const GemmArgs &a, int sm_count) {
-    auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST>;
-    smem_bytes = Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES, BST>)) + 1024;
+    auto kernel = K::kernel;
+    smem_bytes = K::kSmemBytes;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kErrLaunch;
     static bool attr_set[64] = {};
@@ -1140,10 +1391,21 @@ struct LaunchPlan {
     }
     std::memset(&map_a, 0, sizeof(map_a));
     std::memset(&map_b, 0, sizeof(map_b));
-    if (!LSU) {
+    if constexpr (PAIR) {
+      // K-major operands: BK k x 128 rows, 128-byte swizzle. MN-major ones
+      // (A stored K x M, B stored K x N): 32 mn x BK k, 32-byte atoms.
+      const CUtensorMapSwizzle k_sw = CU_TENSOR_MAP_SWIZZLE_128B;
+      const CUtensorMapSwizzle mn_sw = CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B;
+      if (!(OPA ? get_map(a.A, a.M, a.K, a.lda * 4, 32, BK, mn_sw, &map_a)
+                : get_map(a.A, a.K, a.M, a.lda * 4, BK, 128, k_sw, &map_a)))
+        return kErrLaunch;
+      if (!(OPB ? get_map(a.B, a.K, a.N, a.ldb * 4, BK, 128, k_sw, &map_b)
+                : get_map(a.B, a.N, a.K, a.ldb * 4, 32, BK, mn_sw, &map_b)))
+        return kErrLaunch;
+    } else if constexpr (!LSU) {
       const CUtensorMapSwizzle sw_a =
           BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-      if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, Cfg::kAPartRows, sw_a, &map_a)) return kErrLaunch;
+      if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>::kAPartRows, sw_a, &map_a)) return kErrLaunch;
       if (OPB) {
         // B stored N x K: a K-major BK x 128 box with A's swizzle.
         if (!get_map(a.B, a.K, a.N, a.ldb * 4, BK, kTN, sw_a, &map_b)) return kErrLaunch;
@@ -1180,7 +1442,7 @@ struct LaunchPlan {
       if (workers_cached[dev] == 0) {
         cudaLaunchConfig_t qc = {};
         qc.gridDim = dim3(CL * workers, 1, 1);
-        qc.blockDim = dim3(Cfg::kThreads, 1, 1);
+        qc.blockDim = dim3(K::kThreads, 1, 1);
         qc.dynamicSmemBytes = smem_bytes;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1220,7 +1482,7 @@ struct LaunchPlan {
   int launch(cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sch.grid * CL, 1, 1);
-    cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+    cfg.blockDim = dim3(K::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1230,8 +1492,7 @@ struct LaunchPlan {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = CL > 1 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST>,
-                              map_a, map_b, p) ==
+    return cudaLaunchKernelEx(&cfg, K::kernel, map_a, map_b, p) ==
                    cudaSuccess
                ? kOk
                : kErrLaunch;
@@ -1269,9 +1530,9 @@ int workspace_pool(int dev, cudaMemPool_t *out) {
 }
 
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
-          int BST = 0>
+          int BST = 0, bool PAIR = false>
 int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
-  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST> plan;
+  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR> plan;
   int st = plan.prepare(a, sm_count);
   if (st != kOk) return st;
   // Split tiles need a workspace: partial tiles and one counter per split
@@ -1315,7 +1576,69 @@ bool tc_tma_direct(const GemmArgs &a) {
          reinterpret_cast<uintptr_t>(a.B) % 16 == 0 && a.ldb % 4 == 0;
 }
 
+namespace {
+
+// Stages of the CTA-pair kernel: 32 KiB each (128 A rows and 128 B^T rows of
+// 32 k per CTA). Timed at 4096^3 and 8192 x 11008 x 4096: 4 stages 0.73 /
+// 0.89 of the peak, 5 0.78 / 0.89, 6 0.80 / 0.86-0.96, 7 0.79 / 0.85 (the
+// pipeline waits on copies, not on free slots, from 6 on).
+constexpr int kPairStages = 6;
+
+bool tma_operand_ok(const float *ptr, int64_t ld) {
+  return reinterpret_cast<uintptr_t>(ptr) % 16 == 0 && ld % 4 == 0;
+}
+
+// Single-pass TF32 through the CTA-pair kernel, which reads every operand
+// layout by TMA. Operands whose base or pitch TMA cannot take are first
+// copied, in the layout they have, into rows with 16-byte pitches.
+int pair_launch(const GemmArgs &a, int sm_count, cudaStream_t stream) {
+  const bool a_ok = tma_operand_ok(a.A, a.lda), b_ok = tma_operand_ok(a.B, a.ldb);
+  if (!a_ok || !b_ok) {
+    auto up4 = [](int64_t x) { return (x + 3) / 4 * 4; };
+    auto up256 = [](size_t b) { return (b + 255) / 256 * 256; };
+    const int64_t a_rows = a.opa ? a.K : a.M, a_cols = a.opa ? a.M : a.K;
+    const int64_t b_rows = a.opb ? a.N : a.K, b_cols = a.opb ? a.K : a.N;
+    const int64_t lda_p = up4(a_cols), ldb_p = up4(b_cols);
+    const size_t a_bytes = a_ok ? 0 : up256(static_cast<size_t>(a_rows) * lda_p * 4);
+    const size_t b_bytes = b_ok ? 0 : up256(static_cast<size_t>(b_rows) * ldb_p * 4);
+    void *ws = nullptr;
+    int st = pool_alloc(&ws, a_bytes + b_bytes, stream);
+    if (st != kOk) return st;
+    GemmArgs t = a;
+    if (!a_ok) {
+      float *pa = static_cast<float *>(ws);
+      st = pack_rows_launch(a.A, a.lda, a_rows, a_cols, pa, lda_p, sm_count, stream);
+      t.A = pa;
+      t.lda = lda_p;
+    }
+    if (st == kOk && !b_ok) {
+      float *pb = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + a_bytes);
+      st = pack_rows_launch(a.B, a.ldb, b_rows, b_cols, pb, ldb_p, sm_count, stream);
+      t.B = pb;
+      t.ldb = ldb_p;
+    }
+    if (st == kOk) st = pair_launch(t, sm_count, stream);
+    const int fst = pool_free(ws, stream);
+    return st != kOk ? st : fst;
+  }
+  if (a.opa) {
+    if (a.opb)
+      return launch_variant<32, kPairStages, false, false, 2, true, true, 0, true>(a, sm_count,
+                                                                                    stream);
+    return launch_variant<32, kPairStages, false, false, 2, false, true, 0, true>(a, sm_count,
+                                                                                   stream);
+  }
+  if (a.opb)
+    return launch_variant<32, kPairStages, false, false, 2, true, false, 0, true>(a, sm_count,
+                                                                                   stream);
+  return launch_variant<32, kPairStages, false, false, 2, false, false, 0, true>(a, sm_count,
+                                                                                  stream);
+}
+
+}  // namespace
+
 int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream) {
+  if (!exact && !lsu) return pair_launch(a, sm_count, stream);
   if (!lsu && !tc_tma_direct(a)) {
     // Operands TMA cannot describe as given: copy them into one workspace
     // from the library's pool with 16-byte row pitches (A stored transposed,
@@ -1444,14 +1767,15 @@ int noalloc_scratch(int dev, void **out) {
   return kOk;
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, int BST = 0>
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, int BST = 0,
+          bool PAIR = false>
 int launch_variant_noalloc(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return kErrLaunch;
   void *scratch = nullptr;
   int st = noalloc_scratch(dev, &scratch);
   if (st != kOk) return st;
-  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, false, BST> plan;
+  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, false, BST, PAIR> plan;
   st = plan.prepare(a, sm_count);
   if (st != kOk) return st;
   // The same workspace layout gemm_f32 takes from the pool, here inside the
@@ -1475,7 +1799,8 @@ int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cud
     return launch_variant_noalloc<16, 5, true, false, kClusterExact, false>(a, sm_count, stream);
   }
   if (lsu) return launch_variant_noalloc<32, 6, false, true, 1, false>(a, sm_count, stream);
-  return launch_variant_noalloc<32, 5, false, false, kClusterTf32, false, 4>(a, sm_count, stream);
+  return launch_variant_noalloc<32, kPairStages, false, false, 2, false, 0, true>(a, sm_count,
+                                                                                  stream);
 }
 
 }  // namespace gemm
