@@ -275,7 +275,7 @@ __device__ __forceinline__ float scale_out(const TcParams &p, float acc, const f
 // result to C. Run by `nthreads` threads of the CTA that finished last: the
 // four epilogue warps, or every warp of the CTA for its final unit. The tile
 // is read as float4s, eight per thread and part in flight at a time.
-__device__ __noinline__ void epilogue_fixup(const TcParams &p, int sk_tile, uint32_t rank,
+__device__ __forceinline__ void epilogue_fixup(const TcParams &p, int sk_tile, uint32_t rank,
                                             int nparts, int mb, int nb, int tid, int nthreads) {
   constexpr int kVec = kTM * kTN / 4;  // float4s per tile
   constexpr int kRowVec = kTN / 4;     // float4s per tile row
@@ -284,7 +284,13 @@ __device__ __noinline__ void epilogue_fixup(const TcParams &p, int sk_tile, uint
   // Slot (index, rank) starts at (index * cl + rank) * slot4 float4s.
   const float4 *parts = reinterpret_cast<const float4 *>(p.sk_partials) + rank * slot4;
   const float4 *base = parts + static_cast<long long>(split_slot(p, sk_tile, 0)) * p.cl * slot4;
-  const bool vec_ok = (p.ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+  // Scalars of p in registers: the stores to C could otherwise alias p and
+  // force reloads.
+  const int M = p.M, N = p.N;
+  const long long ldc = p.ldc;
+  float *__restrict__ const C = p.C;
+  const float alpha = p.alpha, beta = p.beta;
+  const bool vec_ok = (ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0);
 #pragma unroll 1
   for (int f0 = 0; f0 < kVec; f0 += nthreads * kBatch) {
     float4 acc[kBatch];
@@ -316,24 +322,23 @@ __device__ __noinline__ void epilogue_fixup(const TcParams &p, int sk_tile, uint
       if (f >= kVec) continue;
       const int gm = mb * kTM + f / kRowVec;
       const int gn = nb * kTN + (f % kRowVec) * 4;
-      if (gm >= p.M) continue;
-      float *dst = p.C + static_cast<long long>(gm) * p.ldc + gn;
-      if (vec_ok && gn + 3 < p.N) {
-        float4 v = make_float4(p.alpha * acc[j].x, p.alpha * acc[j].y, p.alpha * acc[j].z,
-                               p.alpha * acc[j].w);
-        if (p.beta != 0.0f) {
+      if (gm >= M) continue;
+      float *dst = C + static_cast<long long>(gm) * ldc + gn;
+      if (vec_ok && gn + 3 < N) {
+        float4 v = make_float4(alpha * acc[j].x, alpha * acc[j].y, alpha * acc[j].z, alpha * acc[j].w);
+        if (beta != 0.0f) {
           const float4 c = *reinterpret_cast<const float4 *>(dst);
-          v.x += p.beta * c.x;
-          v.y += p.beta * c.y;
-          v.z += p.beta * c.z;
-          v.w += p.beta * c.w;
+          v.x += beta * c.x;
+          v.y += beta * c.y;
+          v.z += beta * c.z;
+          v.w += beta * c.w;
         }
         *reinterpret_cast<float4 *>(dst) = v;
       } else {
         const float e[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          if (gn + i < p.N) dst[i] = scale_out(p, e[i], dst + i);
+          if (gn + i < N) dst[i] = beta != 0.0f ? alpha * e[i] + beta * dst[i] : alpha * e[i];
       }
     }
   }
