@@ -274,12 +274,14 @@ __device__ __forceinline__ float scale_out(const TcParams &p, float acc, const f
 // Sum the partial tiles of split tile `sk_tile` in part order and store the
 // result to C. Run by `nthreads` threads of the CTA that finished last: the
 // four epilogue warps, or every warp of the CTA for its final unit. The tile
-// is read as float4s, eight per thread and part in flight at a time.
+// is read as float4s, BATCH per thread and part in flight at a time (the sum
+// is bound by how many loads are in flight, not by bandwidth).
+template <int BATCH = 8>
 __device__ __forceinline__ void epilogue_fixup(const TcParams &p, int sk_tile, uint32_t rank,
                                             int nparts, int mb, int nb, int tid, int nthreads) {
   constexpr int kVec = kTM * kTN / 4;  // float4s per tile
   constexpr int kRowVec = kTN / 4;     // float4s per tile row
-  constexpr int kBatch = 8;
+  constexpr int kBatch = BATCH;
   const long long slot4 = static_cast<long long>(kTM) * kTN / 4;
   // Slot (index, rank) starts at (index * cl + rank) * slot4 float4s.
   const float4 *parts = reinterpret_cast<const float4 *>(p.sk_partials) + rank * slot4;
@@ -1190,7 +1192,7 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
   }
   if (sh->fix_tile >= 0 && !sh->abort) {
     __threadfence();
-    epilogue_fixup(p, sh->fix_tile, rank, sh->fix_nparts, sh->fix_mb, sh->fix_nb, threadIdx.x,
+    epilogue_fixup<16>(p, sh->fix_tile, rank, sh->fix_nparts, sh->fix_mb, sh->fix_nb, threadIdx.x,
                    blockDim.x);
   }
 }
@@ -1293,10 +1295,12 @@ constexpr int kClusterTf32 = 2;
 // Smallest stream-K chunk, in k: shorter chunks spend more time filling the
 // pipeline and more bytes on partial tiles than they save. One TF32 pass
 // does a third of the MMA work per k of 3xTF32, so splitting pays only for
-// longer chunks (measured on 512^3, 1024^3 and 1000 x 1531 x 777: 1024 k
-// before a split is worth it in tf32, 256 k in exact mode).
+// longer chunks (timed on 512 x 512 x 8192, 1024^3, 1024 x 1024 x 8192,
+// 2048^3, 2048 x 2048 x 8192, 1000 x 1531 x 777 and 3072^3: 2048 k before a
+// split is worth it in tf32 -- at 1024 k 2048^3 takes 49 us instead of 31 --
+// and 256 k in exact mode).
 constexpr int kMinChunkKExact = 256;
-constexpr int kMinChunkKTf32 = 1024;
+constexpr int kMinChunkKTf32 = 2048;
 // Most CTAs sharing one split tile: the last of them sums every part alone.
 constexpr int kMaxSplit = 8;
 
@@ -1305,18 +1309,24 @@ struct Schedule {
   bool splits;  // some tile's k range is shared by two or more chunks
 };
 
-// Data-parallel waves plus a stream-K tail. With T tiles of KB k-blocks on
-// G SMs and T mod G != 0, all but the last full wave are dealt whole; the
-// k-blocks of the remaining G + T mod G tiles are cut into equal contiguous
-// chunks over the G CTAs. Each chunk is then at least one tile long, so a
-// split tile has at most two parts, and every SM ends up with about
-// T * KB / G k-blocks. With fewer tiles than SMs everything is stream-K,
-// with chunks of at least min_chunk k-blocks and at most kMaxSplit parts per
-// tile.
-Schedule make_schedule(int tiles, int kb, int sms, int min_chunk) {
+// Data-parallel waves plus a stream-K tail, over G workers (SMs, or CTA
+// pairs). With T tiles of KB k-blocks and T mod G != 0:
+//  - balanced (full_waves = false): all but the last full wave are dealt
+//    whole; the k-blocks of the remaining G + T mod G tiles are cut into
+//    equal contiguous chunks over the G workers. Each chunk is then at least
+//    one tile long, so a split tile has at most two parts, and every worker
+//    ends up with about T * KB / G k-blocks.
+//  - full_waves: every full wave is dealt whole and only the T mod G tiles of
+//    the last one are split, over as many workers as chunks of at least
+//    min_chunk k-blocks allow. The tail runs on fewer workers, which is faster
+//    for a kernel bound by the operand traffic out of L2 (each worker left
+//    running gets a larger share of it) but not for one bound by its MMAs.
+// With fewer tiles than workers everything is stream-K, with chunks of at
+// least min_chunk k-blocks and at most kMaxSplit parts per tile.
+Schedule make_schedule(int tiles, int kb, int sms, int min_chunk, bool full_waves) {
   Schedule s;
   min_chunk = min_chunk < 1 ? 1 : min_chunk;
-  s.dp_tiles = (tiles >= sms && tiles % sms != 0) ? (tiles / sms - 1) * sms
+  s.dp_tiles = (tiles >= sms && tiles % sms != 0) ? (tiles / sms - (full_waves ? 0 : 1)) * sms
                : (tiles >= sms ? tiles : 0);
   const int split = tiles - s.dp_tiles;
   if (split == 0) {
@@ -1342,7 +1352,7 @@ Schedule make_schedule(int tiles, int kb, int sms, int min_chunk) {
   s.sk_ctas = static_cast<int>((total + s.sk_share - 1) / s.sk_share);
   // Chunks that are whole multiples of a tile never split one.
   s.splits = s.sk_share % kb != 0;
-  s.grid = split >= sms ? sms : s.sk_ctas;
+  s.grid = (split >= sms || s.dp_tiles > 0) ? sms : s.sk_ctas;
   return s;
 }
 
@@ -1463,8 +1473,11 @@ struct LaunchPlan {
       }
       workers = workers_cached[dev];
     }
+    // The TF32 pair kernel is bound by operand traffic from L2, the others by
+    // their MMAs (timed at 4096^3, 5120^3, 2560 x 2560 x 4096 and 8192 x 11008
+    // x 4096: +5-6 % for the pair kernel with full waves, -3 % for 3xTF32).
     sch = make_schedule(p.num_tiles, p.num_k_blocks, workers,
-                        (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK);
+                        (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK, PAIR);
     p.dp_tiles = sch.dp_tiles;
     p.sk_share = sch.sk_share;
     p.sk_ctas = sch.sk_ctas;
