@@ -182,6 +182,18 @@ def time_steps(torch, fn, steps, warmup, flush_buf, stream, barrier=None):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], wall
 
 
+def kernel_label(g, kernel, mode):
+    """Name of the kernel gemm_f32 runs for this selection: the TMA-fed TF32
+    pass is the CTA-pair kernel, 3xTF32 the multicast-pair kernel."""
+    if kernel == g.KERNEL_SIMT:
+        return "simt_gemm"
+    if kernel == g.KERNEL_TC_TMA:
+        return "tc_gemm_tma_3xtf32" if mode == "exact" else "tc_pair_tma_tf32"
+    if kernel == g.KERNEL_TC_LSU:
+        return "tc_gemm_lsu_3xtf32" if mode == "exact" else "tc_gemm_lsu_tf32"
+    return str(kernel)
+
+
 def time_back_to_back(torch, fn, steps, warmup, stream):
     """Mean device time (ms) of fn() over `steps` calls enqueued back to back
     between one pair of CUDA events (for inputs larger than L2, which need no
@@ -375,9 +387,7 @@ def main():
     mode = g.MODES[args.mode]
     kernel = g.gemm_f32_select(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N,
                                mode, g.KERNEL_AUTO)
-    suffix = "3xtf32" if args.mode == "exact" else "tf32"
-    kernel_name = {g.KERNEL_SIMT: "simt_gemm", g.KERNEL_TC_TMA: f"tc_gemm_tma_{suffix}",
-                   g.KERNEL_TC_LSU: f"tc_gemm_lsu_{suffix}"}.get(kernel, str(kernel))
+    kernel_name = kernel_label(g, kernel, args.mode)
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:
@@ -410,9 +420,11 @@ def main():
     tf32_peak = pk["bf16"] * TF32_PER_BF16
     alu_peak = SMS * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
     if args.layout != "nn" and kernel != g.KERNEL_SIMT:
-        # A stored transposed reaches the TMA-fed kernel through a transposed copy
-        kernel_name += "_" + args.layout + ("_after_transpose" if transa and kernel == g.KERNEL_TC_TMA
-                                            else "")
+        # A stored transposed reaches the TMA-fed 3xTF32 kernel through a
+        # transposed copy (the TF32 pair kernel reads it as it is)
+        kernel_name += "_" + args.layout + (
+            "_after_transpose" if transa and kernel == g.KERNEL_TC_TMA and args.mode == "exact"
+            else "")
     traffic, sha = traffic_lookup(kernel_name, args.config, args.mode)
     if args.mode == "exact_simt":
         achieved = flops / (ms_per_step / 1e3) / 1e12
@@ -447,9 +459,7 @@ def main():
             ach = mult * flops / (ms / 1e3) / 1e12
             mk = g.gemm_f32_select(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N,
                                    mcode, g.KERNEL_AUTO)
-            msuffix = "3xtf32" if mname == "exact" else "tf32"
-            mkname = {g.KERNEL_SIMT: "simt_gemm", g.KERNEL_TC_TMA: f"tc_gemm_tma_{msuffix}",
-                      g.KERNEL_TC_LSU: f"tc_gemm_lsu_{msuffix}"}.get(mk, str(mk))
+            mkname = kernel_label(g, mk, mname)
             mtraffic, _ = traffic_lookup(mkname, args.config, mname)
             extras[mname] = {"value": round(flops / (ms / 1e3) / 1e9, 1), "unit": "GFLOP/s",
                              "ms_per_step": round(ms, 4), "steps": steps,
