@@ -69,9 +69,18 @@ int reduce_launch(int64_t n, const float *x, float *out, int groups, float *part
                   cudaStream_t stream);
 int reduce_default_groups(int sm_count);
 
-// dst (rows x cols, pitch ldd) = src (pitch lds), on `stream`. Sizes below 2^31.
-int pack_rows_launch(const float *src, int64_t lds, int64_t rows, int64_t cols, float *dst,
-                     int64_t ldd, int sm_count, cudaStream_t stream);
+// One row-by-row copy: dst (rows x cols, pitch ldd) = src (pitch lds). Sizes
+// below 2^31 columns; rows <= 0 or cols <= 0 is an empty job.
+struct PackJob {
+  const float *src = nullptr;
+  int64_t lds = 0, rows = 0, cols = 0;
+  float *dst = nullptr;
+  int64_t ldd = 0;
+};
+
+// Both jobs in one launch on `stream`.
+int pack_rows_launch(const PackJob &first, const PackJob &second, int sm_count,
+                     cudaStream_t stream);
 
 // Rates of the TF32 tensor pipe (MMA-only kernel) and of the FP32 FMA pipe
 // (FFMA-only kernel) on sm_count SMs, in TFLOP/s. Blocking.

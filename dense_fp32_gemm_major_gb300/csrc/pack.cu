@@ -9,7 +9,8 @@
 //
 // A CTA of 256 threads copies whole rows, the rows taken in steps of the grid;
 // each warp reads and writes 128 consecutive bytes per instruction (one
-// coalesced segment), four instructions in flight per thread.
+// coalesced segment), four instructions in flight per thread. Both operands
+// of a GEMM that need it are copied by one launch.
 
 #include <cuda_runtime.h>
 
@@ -23,12 +24,19 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kBlocksPerSm = 8;
 
+// Copies the rows of up to two matrices in one launch (a GEMM's operands are
+// copied together: one launch less ahead of the GEMM). Rows [0, first.rows)
+// of the combined row range belong to `first`, the rest to `second`.
 __global__ void __launch_bounds__(kThreads)
-    pack_rows_kernel(const float *__restrict__ src, long long lds, int rows, int cols,
-                     float *__restrict__ dst, long long ldd) {
-  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
-    const float *s = src + static_cast<long long>(r) * lds;
-    float *d = dst + static_cast<long long>(r) * ldd;
+    pack_rows_kernel(const PackJob first, const PackJob second) {
+  const long long total = first.rows + second.rows;
+  for (long long rr = blockIdx.x; rr < total; rr += gridDim.x) {
+    const bool in_first = rr < first.rows;
+    const PackJob &j = in_first ? first : second;
+    const long long r = in_first ? rr : rr - first.rows;
+    const float *s = j.src + r * j.lds;
+    float *d = j.dst + r * j.ldd;
+    const int cols = static_cast<int>(j.cols);
     int c = threadIdx.x;
     for (; c + 3 * kThreads < cols; c += 4 * kThreads) {
       const float v0 = __ldg(s + c), v1 = __ldg(s + c + kThreads), v2 = __ldg(s + c + 2 * kThreads),
@@ -44,13 +52,17 @@ __global__ void __launch_bounds__(kThreads)
 
 }  // namespace
 
-int pack_rows_launch(const float *src, int64_t lds, int64_t rows, int64_t cols, float *dst,
-                     int64_t ldd, int sm_count, cudaStream_t stream) {
-  if (rows <= 0 || cols <= 0) return kOk;
+int pack_rows_launch(const PackJob &first, const PackJob &second, int sm_count,
+                     cudaStream_t stream) {
+  const long long total = (first.rows > 0 && first.cols > 0 ? first.rows : 0) +
+                          (second.rows > 0 && second.cols > 0 ? second.rows : 0);
+  if (total <= 0) return kOk;
+  PackJob a = first, b = second;
+  if (a.rows <= 0 || a.cols <= 0) a.rows = 0;
+  if (b.rows <= 0 || b.cols <= 0) b.rows = 0;
   const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * kBlocksPerSm;
-  const unsigned grid = static_cast<unsigned>(rows < cap ? rows : cap);
-  pack_rows_kernel<<<grid, kThreads, 0, stream>>>(src, lds, static_cast<int>(rows),
-                                                  static_cast<int>(cols), dst, ldd);
+  const unsigned grid = static_cast<unsigned>(total < cap ? total : cap);
+  pack_rows_kernel<<<grid, kThreads, 0, stream>>>(a, b);
   return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 

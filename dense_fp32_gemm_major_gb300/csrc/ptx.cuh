@@ -393,7 +393,7 @@ __device__ __forceinline__ void tmem_load_wait() {
 // 46, base offset 0 (stage tiles are 1024-byte aligned) and the layout type
 // in bits 61..63 (0 none, 2 = 128-byte swizzle, 4 = 64-byte, 6 = 32-byte).
 // Layout codes (bits 61-63): 2 = 128-byte swizzle, 4 = 64-byte swizzle,
-// 1 = 128-byte swizzle of 32-byte atoms (the layout an MN-major TF32 operand
+// 6 = 32-byte swizzle, 1 = 128-byte swizzle of 32-byte atoms (the layout an MN-major TF32 operand
 // needs: TMA writes it with CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B).
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint32_t layout) {

@@ -893,7 +893,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
         }
         tc_fence_after_sync();
         uint8_t *st = tiles + stage * Cfg::kStageBytes;
-        if (!OPB) {
+        if constexpr (!OPB) {
           // B tile is row-major BK k x 128 n (512-byte rows); this thread's
           // column n = 32 quad + lane becomes TMEM lane n.
           constexpr int kW = BK / Cfg::kXformParts;
@@ -916,7 +916,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
               bphase ^= 1;
             }
           }
-        } else if (Cfg::kBtTmem) {
+        } else if constexpr (Cfg::kBtTmem) {
           // B tile is K-major 128 n x BK k (swizzled rows of BK * 4 bytes):
           // row n = 32 quad + lane holds this thread's TMEM lane, and part
           // `part` reads its kW consecutive k as 16-byte chunks.
@@ -1660,18 +1660,20 @@ int pair_launch(const GemmArgs &a, int sm_count, cudaStream_t stream) {
     int st = pool_alloc(&ws, a_bytes + b_bytes, stream);
     if (st != kOk) return st;
     GemmArgs t = a;
+    PackJob ja, jb;  // both copies in one launch
     if (!a_ok) {
       float *pa = static_cast<float *>(ws);
-      st = pack_rows_launch(a.A, a.lda, a_rows, a_cols, pa, lda_p, sm_count, stream);
+      ja = PackJob{a.A, a.lda, a_rows, a_cols, pa, lda_p};
       t.A = pa;
       t.lda = lda_p;
     }
-    if (st == kOk && !b_ok) {
+    if (!b_ok) {
       float *pb = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + a_bytes);
-      st = pack_rows_launch(a.B, a.ldb, b_rows, b_cols, pb, ldb_p, sm_count, stream);
+      jb = PackJob{a.B, a.ldb, b_rows, b_cols, pb, ldb_p};
       t.B = pb;
       t.ldb = ldb_p;
     }
+    st = pack_rows_launch(ja, jb, sm_count, stream);
     if (st == kOk) st = pair_launch(t, sm_count, stream);
     const int fst = pool_free(ws, stream);
     return st != kOk ? st : fst;
@@ -1711,20 +1713,24 @@ int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_
     int st = pool_alloc(&ws, a_bytes + b_bytes, stream);
     if (st != kOk) return st;
     GemmArgs t = a;
+    PackJob ja, jb;  // row copies of both operands in one launch
     if (!a_ok) {
       float *pa = static_cast<float *>(ws);
-      st = a.opa ? transpose_launch(a.A, a.lda, a.K, a.M, pa, lda_p, sm_count, stream)
-                 : pack_rows_launch(a.A, a.lda, a.M, a.K, pa, lda_p, sm_count, stream);
+      if (a.opa)
+        st = transpose_launch(a.A, a.lda, a.K, a.M, pa, lda_p, sm_count, stream);
+      else
+        ja = PackJob{a.A, a.lda, a.M, a.K, pa, lda_p};
       t.A = pa;
       t.lda = lda_p;
       t.opa = 0;
     }
-    if (st == kOk && !b_ok) {
+    if (!b_ok) {
       float *pb = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + a_bytes);
-      st = pack_rows_launch(a.B, a.ldb, b_rows, b_cols, pb, ldb_p, sm_count, stream);
+      jb = PackJob{a.B, a.ldb, b_rows, b_cols, pb, ldb_p};
       t.B = pb;
       t.ldb = ldb_p;
     }
+    if (st == kOk) st = pack_rows_launch(ja, jb, sm_count, stream);
     if (st == kOk) st = tc_launch(t, exact, false, sm_count, stream);
     const int fst = pool_free(ws, stream);
     return st != kOk ? st : fst;
