@@ -287,15 +287,27 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
 }
 
 // D[tmem] (+)= A[tmem] * B[smem], kind::tf32: A is read from TMEM (lane = row
-// of A, one 32-bit column per k), B through a shared-memory descriptor.
+// of A, one 32-bit column per k), B through a shared-memory descriptor. With
+// G = 2 (M = 256) each CTA of the pair holds rows 128 r .. 128 r + 127 of A
+// and of D in its own TMEM lanes, at the same addresses, and half of B's N
+// columns behind the same descriptor.
+template <int G = 1>
 __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if (G == 2)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread
@@ -408,10 +420,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 
 // Instruction descriptor for kind::tf32 with an fp32 accumulator:
 // D format F32 (bits 4-5 = 1), A and B format TF32 (bits 7-9 and 10-12 = 2),
-// A and B K-major (bits 15 and 16 = 0), N >> 3 in bits 17-22 and M >> 4 in
-// bits 24-28. (With kind::tf32 an MN-major B operand does not multiply on
-// sm_103a: the instruction leaves D unchanged. Both operands are therefore
-// staged K-major.)
+// A and B K-major (bits 15 and 16 = 0; set, the operand is MN-major), N >> 3
+// in bits 17-22 and M >> 4 in bits 24-28. (An MN-major kind::tf32 operand
+// multiplies only from the 128-byte swizzle of 32-byte atoms, layout code 1;
+// with the plain 128-byte swizzle the instruction leaves D unchanged.)
 __host__ __device__ constexpr uint32_t idesc_tf32(uint32_t m, uint32_t n) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }

@@ -9,13 +9,16 @@
 //     an 8 x 8 register tile laid out as 2 x 2 blocks of 4 x 4 (rows ty*4 and
 //     64 + ty*4, columns tx*4 and 64 + tx*4) so that every shared-memory
 //     fragment read is one 128-bit load shared by many lanes (a broadcast);
-//   * K advances in slices of 8; A is staged transposed (k-major, padded to
-//     132 floats per k-row so the transposing stores do not conflict) and B
-//     as is; two shared-memory buffers and a register prefetch overlap the
-//     global loads of slice s + 1 with the FMAs of slice s;
-//   * global loads and stores are 128-bit and coalesced when the operands
-//     allow (VEC), otherwise scalar; both forms zero-fill outside the
-//     matrices and guard every store, the boundary rule of section 4 of
+//   * K advances in slices of 32 through two shared-memory stages filled by
+//     asynchronous copies (cp.async), so the copies of slice s + 1 run while
+//     slice s is multiplied and no register holds operand data in flight. A
+//     is staged transposed (k-major, rows padded to 132 floats): each lane
+//     copies one 4-byte element into its transposed place, eight lanes per
+//     row so that a warp reads 32-byte row segments and writes 32 distinct
+//     banks. B, and A when it is stored K x M, are copied as they are, 16
+//     bytes per copy when the operands allow (VEC), else 4;
+//   * elements outside the matrices are zero-filled by the copies (source
+//     size 0) and every store is guarded, the boundary rule of section 4 of
 //     "WebGPU WGSL Compute Shaders: Custom Matrix Multiplication (GEMM)
 //     Optimization Guide".
 //
@@ -24,12 +27,13 @@
 // C = alpha * A op(B) + beta * C scales the sum once at the store (C is read
 // only when beta != 0). op(B) = B, or B stored transposed (N x K, the vec4
 // transposed-B storage of the subgroups page, section 7), which is staged
-// through the same transposing stores as A; op(A) = A, or A stored
-// transposed (K x M), whose rows of m are stored into the k-major tile as is.
+// through the same transposing copies as A; op(A) = A, or A stored
+// transposed (K x M), whose rows of m are copied into the k-major tile as is.
 
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "kernels.h"
 
@@ -37,9 +41,11 @@ namespace gemm {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kSliceK = 8;
+constexpr int kSliceK = 32;                  // k per stage
 constexpr int kThreads = 256;
-constexpr int kApad = kTile + 4;
+constexpr int kPitch = kTile + 4;            // floats per k-row of a stage tile
+constexpr int kStageFloats = 2 * kSliceK * kPitch;  // A tile + B tile
+constexpr int kSmemBytes = 2 * kStageFloats * 4;    // two stages: 67,584 bytes
 constexpr int kGroup = 8;  // raster group height in tiles (L2 reuse)
 
 struct SimtParams {
@@ -54,10 +60,28 @@ struct SimtParams {
   int tiles_m, tiles_n;
 };
 
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Asynchronous copy of 4 (or 16) bytes into shared memory; when `in` is
+// false nothing is read and the destination is zero-filled.
+__device__ __forceinline__ void copy4(uint32_t dst, const float *src, bool in) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src),
+               "r"(in ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void copy16(uint32_t dst, const float *src, bool in) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(in ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void copy_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void copy_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
 template <bool VEC, bool OPB, bool OPA>
 __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams p) {
-  __shared__ __align__(16) float As[2][kSliceK][kApad];
-  __shared__ __align__(16) float Bs[2][kSliceK][kApad];
+  extern __shared__ __align__(16) float smem[];
 
   // Grouped raster: kGroup tile-rows sweep all tile-columns before moving on.
   const int bid = blockIdx.x;
@@ -70,18 +94,68 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
   const int n0 = (r / gm_cnt) * kTile;
 
   const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
   const int tx = tid & 15, ty = tid >> 4;
+  const uint32_t sbase = smem_addr(smem);
 
-  // Load assignment: A row (tid / 2), k-offset (tid % 2) * 4 (A stored
-  // transposed: k-row tid / 32, rows (tid % 32) * 4 ...); B k-row (tid / 32),
-  // column (tid % 32) * 4, or for B stored transposed, like A: n-row
-  // (tid / 2), k-offset (tid % 2) * 4.
-  const int a_row = OPA ? (tid & 31) * 4 : tid >> 1;
-  const int a_k = OPA ? tid >> 5 : (tid & 1) * 4;
-  const int b_k = OPB ? (tid & 1) * 4 : tid >> 5;
-  const int b_col = OPB ? tid >> 1 : (tid & 31) * 4;
-  const int ga_row = m0 + a_row;
-  const int gb_col = n0 + b_col;
+  // Copies of slice s (k0 = s * kSliceK) into stage s & 1, in groups of 8 k.
+  // Transposing copies (A stored M x K, B stored N x K): lane -> row
+  // warp * 16 + j * 4 + lane / 8, k lane % 8. Direct copies (A stored K x M,
+  // B stored K x N): k-row tid / 32, columns (tid % 32) * 4 ... + 3 (VEC) or
+  // tid % 32 + 32 j.
+  auto issue = [&](int s) {
+    const uint32_t as = sbase + (s & 1) * kStageFloats * 4;
+    const uint32_t bs = as + kSliceK * kPitch * 4;
+#pragma unroll
+    for (int h = 0; h < kSliceK / 8; ++h) {
+      const int k0 = s * kSliceK + h * 8;
+      if constexpr (!OPA) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int row = warp * 16 + j * 4 + (lane >> 3), kk = lane & 7;
+          const bool in = m0 + row < p.M && k0 + kk < p.K;
+          const float *src = in ? p.A + static_cast<long long>(m0 + row) * p.lda + k0 + kk : p.A;
+          copy4(as + ((h * 8 + kk) * kPitch + row) * 4, src, in);
+        }
+      } else if constexpr (VEC) {
+        const int kk = tid >> 5, col = lane * 4;
+        const bool in = k0 + kk < p.K && m0 + col < p.M;
+        const float *src = in ? p.A + static_cast<long long>(k0 + kk) * p.lda + m0 + col : p.A;
+        copy16(as + ((h * 8 + kk) * kPitch + col) * 4, src, in);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kk = tid >> 5, col = lane + 32 * j;
+          const bool in = k0 + kk < p.K && m0 + col < p.M;
+          const float *src = in ? p.A + static_cast<long long>(k0 + kk) * p.lda + m0 + col : p.A;
+          copy4(as + ((h * 8 + kk) * kPitch + col) * 4, src, in);
+        }
+      }
+      if constexpr (OPB) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int col = warp * 16 + j * 4 + (lane >> 3), kk = lane & 7;
+          const bool in = n0 + col < p.N && k0 + kk < p.K;
+          const float *src = in ? p.B + static_cast<long long>(n0 + col) * p.ldb + k0 + kk : p.B;
+          copy4(bs + ((h * 8 + kk) * kPitch + col) * 4, src, in);
+        }
+      } else if constexpr (VEC) {
+        const int kk = tid >> 5, col = lane * 4;
+        const bool in = k0 + kk < p.K && n0 + col < p.N;
+        const float *src = in ? p.B + static_cast<long long>(k0 + kk) * p.ldb + n0 + col : p.B;
+        copy16(bs + ((h * 8 + kk) * kPitch + col) * 4, src, in);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kk = tid >> 5, col = lane + 32 * j;
+          const bool in = k0 + kk < p.K && n0 + col < p.N;
+          const float *src = in ? p.B + static_cast<long long>(k0 + kk) * p.ldb + n0 + col : p.B;
+          copy4(bs + ((h * 8 + kk) * kPitch + col) * 4, src, in);
+        }
+      }
+    }
+    copy_commit();
+  };
 
   float acc[8][8];
 #pragma unroll
@@ -89,83 +163,24 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
-  float a_reg[4], b_reg[4];
-
-  auto load_slice = [&](int k0) {
-    const int ka = k0 + a_k;
-    const int kb = k0 + b_k;
-    if (VEC) {
-      // Contiguous extents are multiples of 4: a 4-wide group is wholly
-      // inside or outside.
-      float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
-      if (OPA) {
-        if (ka < p.K && ga_row < p.M)
-          va = __ldg(reinterpret_cast<const float4 *>(p.A + static_cast<long long>(ka) * p.lda + ga_row));
-      } else if (ga_row < p.M && ka < p.K) {
-        va = __ldg(reinterpret_cast<const float4 *>(p.A + static_cast<long long>(ga_row) * p.lda + ka));
-      }
-      if (OPB) {
-        if (gb_col < p.N && kb < p.K)
-          vb = __ldg(reinterpret_cast<const float4 *>(p.B + static_cast<long long>(gb_col) * p.ldb + kb));
-      } else if (kb < p.K && gb_col < p.N) {
-        vb = __ldg(reinterpret_cast<const float4 *>(p.B + static_cast<long long>(kb) * p.ldb + gb_col));
-      }
-      a_reg[0] = va.x; a_reg[1] = va.y; a_reg[2] = va.z; a_reg[3] = va.w;
-      b_reg[0] = vb.x; b_reg[1] = vb.y; b_reg[2] = vb.z; b_reg[3] = vb.w;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (OPA)
-          a_reg[j] = (ka < p.K && ga_row + j < p.M)
-                         ? __ldg(p.A + static_cast<long long>(ka) * p.lda + ga_row + j)
-                         : 0.0f;
-        else
-          a_reg[j] = (ga_row < p.M && ka + j < p.K)
-                         ? __ldg(p.A + static_cast<long long>(ga_row) * p.lda + ka + j)
-                         : 0.0f;
-        if (OPB)
-          b_reg[j] = (gb_col < p.N && kb + j < p.K)
-                         ? __ldg(p.B + static_cast<long long>(gb_col) * p.ldb + kb + j)
-                         : 0.0f;
-        else
-          b_reg[j] = (kb < p.K && gb_col + j < p.N)
-                         ? __ldg(p.B + static_cast<long long>(kb) * p.ldb + gb_col + j)
-                         : 0.0f;
-      }
-    }
-  };
-  auto store_slice = [&](int buf) {
-    if (OPA) {
-      *reinterpret_cast<float4 *>(&As[buf][a_k][a_row]) =
-          make_float4(a_reg[0], a_reg[1], a_reg[2], a_reg[3]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) As[buf][a_k + j][a_row] = a_reg[j];
-    }
-    if (OPB) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) Bs[buf][b_k + j][b_col] = b_reg[j];
-    } else {
-      *reinterpret_cast<float4 *>(&Bs[buf][b_k][b_col]) =
-          make_float4(b_reg[0], b_reg[1], b_reg[2], b_reg[3]);
-    }
-  };
-
   const int num_slices = (p.K + kSliceK - 1) / kSliceK;
-  load_slice(0);
-  store_slice(0);
-  __syncthreads();
-
+  issue(0);
   for (int s = 0; s < num_slices; ++s) {
-    const int buf = s & 1;
-    const bool more = s + 1 < num_slices;
-    if (more) load_slice((s + 1) * kSliceK);
-#pragma unroll
+    // Slice s has landed (this thread's copies, then everyone's), and every
+    // thread is done with slice s - 1, whose stage the next copies refill.
+    copy_wait_all();
+    __syncthreads();
+    if (s + 1 < num_slices) issue(s + 1);
+    const float *As = smem + (s & 1) * kStageFloats;
+    const float *Bs = As + kSliceK * kPitch;
+    // Unrolled by 4 only: the whole 32-k slice unrolled (2,000+ instructions)
+    // no longer fits the instruction cache and runs 2-3 % slower.
+#pragma unroll 4
     for (int k = 0; k < kSliceK; ++k) {
-      const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][k][ty * 4]);
-      const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][k][64 + ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][k][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][k][64 + tx * 4]);
+      const float4 a0 = *reinterpret_cast<const float4 *>(&As[k * kPitch + ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4 *>(&As[k * kPitch + 64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[k * kPitch + tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[k * kPitch + 64 + tx * 4]);
       const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -173,8 +188,6 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
-    if (more) store_slice(buf ^ 1);
-    __syncthreads();
   }
 
 #pragma unroll
@@ -212,6 +225,28 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
   }
 }
 
+// Launch one variant; its shared memory (above the 48 KiB default) is
+// enabled once per device.
+template <bool VEC, bool OPB, bool OPA>
+int launch_variant(const SimtParams &p, dim3 grid, cudaStream_t stream) {
+  auto kernel = simt_gemm_kernel<VEC, OPB, OPA>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kErrLaunch;
+  static bool attr_set[64] = {};
+  static std::mutex attr_mu;
+  {
+    std::lock_guard<std::mutex> g(attr_mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+          cudaSuccess)
+        return kErrLaunch;
+      attr_set[dev] = true;
+    }
+  }
+  kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+}
+
 }  // namespace
 
 int simt_launch(const GemmArgs &a, cudaStream_t stream) {
@@ -243,16 +278,15 @@ int simt_launch(const GemmArgs &a, cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(blocks));
   const int variant = (vec ? 4 : 0) | (a.opb ? 2 : 0) | (a.opa ? 1 : 0);
   switch (variant) {
-    case 0: simt_gemm_kernel<false, false, false><<<grid, kThreads, 0, stream>>>(p); break;
-    case 1: simt_gemm_kernel<false, false, true><<<grid, kThreads, 0, stream>>>(p); break;
-    case 2: simt_gemm_kernel<false, true, false><<<grid, kThreads, 0, stream>>>(p); break;
-    case 3: simt_gemm_kernel<false, true, true><<<grid, kThreads, 0, stream>>>(p); break;
-    case 4: simt_gemm_kernel<true, false, false><<<grid, kThreads, 0, stream>>>(p); break;
-    case 5: simt_gemm_kernel<true, false, true><<<grid, kThreads, 0, stream>>>(p); break;
-    case 6: simt_gemm_kernel<true, true, false><<<grid, kThreads, 0, stream>>>(p); break;
-    default: simt_gemm_kernel<true, true, true><<<grid, kThreads, 0, stream>>>(p); break;
+    case 0: return launch_variant<false, false, false>(p, grid, stream);
+    case 1: return launch_variant<false, false, true>(p, grid, stream);
+    case 2: return launch_variant<false, true, false>(p, grid, stream);
+    case 3: return launch_variant<false, true, true>(p, grid, stream);
+    case 4: return launch_variant<true, false, false>(p, grid, stream);
+    case 5: return launch_variant<true, false, true>(p, grid, stream);
+    case 6: return launch_variant<true, true, false>(p, grid, stream);
+    default: return launch_variant<true, true, true>(p, grid, stream);
   }
-  return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 
 }  // namespace gemm

@@ -51,6 +51,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/gemm_f32.h"
 #include "kernels.h"
@@ -1208,6 +1209,308 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
   }
 }
 
+// -------------------------------------------------- CTA-pair 3xTF32 kernel --
+//
+// 3xTF32 on the two SMs of a cluster acting as one tensor core, for A stored
+// M x K and B stored K x N. The pair computes one unit tile, 256 n x 256 m
+// of C^T, as in tc_pair_kernel: M = 256 (B_tile^T, CTA r holding n rows
+// 128 r ..), N = 256 (the A tile, CTA r holding m rows 128 r ..), K = 8.
+//
+// Shared-memory traffic decides the design. With one SM per 128 n x 256 m
+// output tile (tc_gemm_kernel) every MMA reads 256 rows of its B operand and
+// every SM splits a 256-row A tile, about 1.3 times the bytes per cycle
+// shared memory can serve at full tensor rate; with the pair each SM reads
+// and splits only its own 128 rows, for the same MMA work per SM.
+//
+// Per stage each CTA loads, by TMA on its own barrier, its 128 A rows x BK k
+// (K-major, swizzled) and its B tile BK k x 128 n (row-major). Its transform
+// warps move B^T as hi and lo into its own TMEM (lane = n, one column per k)
+// and split its A rows in place (hi) and into a sibling tile (lo). The even
+// CTA's transform warps then arrive on its `ready` barrier; the odd CTA's
+// arrive on a local barrier, and one relay thread passes the stage on with a
+// single remote arrive (a release at cluster scope, which orders the odd
+// CTA's shared-memory and TMEM writes before the even CTA's MMAs). The even
+// CTA issues B_lo*A_hi, B_hi*A_lo, B_hi*A_hi per k-step of 8 with A from TMEM
+// and B from shared memory, and its commits free the stage in both CTAs.
+// TMEM: one 256-column accumulator, then 2 BK columns (hi, lo) per stage.
+template <int BK, int STAGES, int XW>
+struct PairExactConfig {
+  static_assert(BK == 16 || BK == 32, "BK");
+  static constexpr int kHalfRows = 128;                          // A rows per CTA
+  static constexpr int kRowBytes = BK * 4;                       // one K-major A row
+  static constexpr int kAtomBytes = 8 * kRowBytes;               // 8-row swizzle atom (SBO)
+  static constexpr uint32_t kLayout = BK == 32 ? 2u : 4u;        // 128- or 64-byte swizzle
+  static constexpr int kABytes = kHalfRows * BK * 4;             // A rows (hi after the split)
+  static constexpr int kALoOffset = kABytes;                     // A lo, same layout
+  static constexpr int kBOffset = 2 * kABytes;                   // B tile, BK x 128, row-major
+  static constexpr int kBBytes = BK * kTN * 4;
+  static constexpr int kStageBytes = 2 * kABytes + kBBytes;
+  static constexpr int kTileBytes = STAGES * kStageBytes;
+  static constexpr uint32_t kBtColsPerStage = 2 * BK;            // B^T hi, then lo
+  static constexpr int kAccBufs = 1;
+  static constexpr int kMmaWarp = 1;
+  static constexpr int kEpiWarp0 = 2;
+  static constexpr int kXformWarp0 = 6;
+  static constexpr int kXformParts = XW / 4;                     // per TMEM lane quadrant
+  static constexpr int kThreads = 32 * (kXformWarp0 + XW);
+  static constexpr uint32_t kIdesc = idesc_tf32(2 * kTN, kTM);   // both operands K-major
+  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(XW % 4 == 0 && BK % kXformParts == 0 && (BK / kXformParts) % 4 == 0,
+                "transform partition");
+  static_assert(kBtCol + STAGES * kBtColsPerStage <= kTmemCols, "TMEM budget");
+};
+
+// Shared state of the 3xTF32 pair kernel: TcShared plus the odd CTA's local
+// barriers on which its transform warps arrive before one thread passes the
+// stage on to the even CTA.
+template <int STAGES>
+struct alignas(8) PairExactShared : TcShared<STAGES> {
+  uint64_t relay[STAGES];
+};
+
+template <int BK, int STAGES, int XW>
+__global__ void __launch_bounds__(PairExactConfig<BK, STAGES, XW>::kThreads, 1)
+    tc_pair_exact_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
+  using Cfg = PairExactConfig<BK, STAGES, XW>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *tiles = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  PairExactShared<STAGES> *sh = reinterpret_cast<PairExactShared<STAGES> *>(tiles + Cfg::kTileBytes);
+  volatile int *abort = &sh->abort;
+
+  const uint32_t warp = warp_index();
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sh->full[s], 1);        // this CTA's producer; its own copies' bytes
+      mbar_init(&sh->ready[s], XW + 1);  // even CTA: its transform warps, the odd CTA's relay
+      mbar_init(&sh->empty[s], 1);       // the even CTA's commit, multicast to both
+      mbar_init(&sh->relay[s], XW);      // odd CTA: its transform warps
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh->acc_full[a], 1);
+      mbar_init(&sh->acc_empty[a], 8);   // even CTA: the four epilogue warps of each CTA
+    }
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    sh->fix_tile = -1;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmap_a);
+    tma_prefetch_map(&tmap_b);
+  }
+  if (warp == Cfg::kMmaWarp) {
+    tmem_alloc<2>(&sh->tmem_base, kTmemCols);
+    tmem_relinquish<2>();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // barriers and TMEM of both CTAs set up before either signals the other
+  tc_fence_after_sync();
+  const uint32_t tmem = sh->tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer --
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
+      bool ok = true;
+      UnitIter it(p);
+      WorkUnit u;
+      while (ok && it.next(p, u)) {
+        int mb, nb;
+        tile_coords(p, u.tile, rank, mb, nb);
+        const int m0 = mb * kTM + static_cast<int>(rank) * Cfg::kHalfRows;
+        const int n0 = nb * kTN;
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          if (!mbar_wait_bounded(&sh->empty[stage], phase ^ 1, p.timeout_ns, abort,
+                                 &g_tc_status)) {
+            ok = false;
+            break;
+          }
+          uint8_t *st = tiles + stage * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(&sh->full[stage], Cfg::kABytes + Cfg::kBBytes);
+          tma_load_2d(st, &tmap_a, &sh->full[stage], kb * BK, m0);
+          tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], n0, kb * BK);
+          armed |= 1u << stage;
+          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Let every copy this thread issued land before the CTA exits.
+      if (!ok)
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s)) drain_wait(&sh->full[s], (armed_parity >> s) & 1u, p.timeout_ns);
+    }
+  } else if (warp == Cfg::kMmaWarp) {
+    // ------------------------------------------------- MMA (even CTA) --
+    if (rank == 0 && lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      UnitIter it(p);
+      WorkUnit u;
+      while (ok && it.next(p, u)) {
+        // Both CTAs' epilogues have drained the accumulator.
+        if (!mbar_wait_bounded<true>(&sh->acc_empty[acc], acc_phase ^ 1, p.timeout_ns, abort,
+                                     &g_tc_status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + kAccCol + acc * kTM;
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          // Both CTAs' transform warps are done with the stage (the odd
+          // CTA's arrivals come from the peer: acquire at cluster scope).
+          if (!mbar_wait_bounded<true>(&sh->ready[stage], phase, p.timeout_ns, abort,
+                                       &g_tc_status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_hi = smem_addr(tiles + stage * Cfg::kStageBytes);
+          const uint32_t bt_hi = tmem + kBtCol + stage * Cfg::kBtColsPerStage;
+#pragma unroll
+          for (int kk = 0; kk < BK / kUmmaK; ++kk) {
+            const uint64_t da = smem_desc(a_hi + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
+            const uint64_t da_lo =
+                smem_desc(a_hi + Cfg::kALoOffset + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
+            const uint32_t accumulate = (kb != u.kb0 || kk != 0) ? 1u : 0u;
+            mma_tf32_ts<2>(d_tmem, bt_hi + BK + kk * kUmmaK, da, Cfg::kIdesc, accumulate);
+            mma_tf32_ts<2>(d_tmem, bt_hi + kk * kUmmaK, da_lo, Cfg::kIdesc, 1);
+            mma_tf32_ts<2>(d_tmem, bt_hi + kk * kUmmaK, da, Cfg::kIdesc, 1);
+          }
+          mma_commit_multicast<2>(&sh->empty[stage], 3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit_multicast<2>(&sh->acc_full[acc], 3);
+        if (++acc == Cfg::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // Every MMA this thread issued completes before TMEM is released.
+      mma_commit_multicast<2>(&sh->drain, 1);
+      drain_wait(&sh->drain, 0, p.timeout_ns);
+    } else if (rank == 1 && lane == 0) {
+      // -------------------------------------------- relay (odd CTA) --
+      // Once all of this CTA's transform warps are done with a stage, one
+      // release at cluster scope passes it on to the even CTA's MMAs (eight
+      // warps each arriving remotely took twice as long per stage).
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      UnitIter it(p);
+      WorkUnit u;
+      while (ok && it.next(p, u)) {
+        for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          if (!mbar_wait_bounded(&sh->relay[stage], phase, p.timeout_ns, abort, &g_tc_status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(&sh->ready[stage], 0);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < Cfg::kEpiWarp0 + 4) {
+    // --------------------------------------------------------- epilogue --
+    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, true>(p, sh, tmem, warp, lane, rank, abort);
+  } else {
+    // --------------------------------------------------------- transform --
+    // Warp (quad, part) moves k in [part * W, (part + 1) * W), W = BK / parts,
+    // of B^T rows n = 32 quad + lane into TMEM as hi and lo; all of them
+    // split this CTA's A rows.
+    const uint32_t quad = warp & 3;
+    const uint32_t part = (warp - Cfg::kXformWarp0) >> 2;
+    const int xt = threadIdx.x - Cfg::kXformWarp0 * 32;
+    constexpr int kW = BK / Cfg::kXformParts;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    UnitIter it(p);
+    WorkUnit u;
+    while (ok && it.next(p, u)) {
+      for (int kb = u.kb0; kb < u.kb1; ++kb) {
+        if (!warp_wait(&sh->full[stage], phase, p, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint8_t *st = tiles + stage * Cfg::kStageBytes;
+        const float *bs = reinterpret_cast<const float *>(st + Cfg::kBOffset) + part * kW * kTN +
+                          quad * 32 + lane;
+        float v[kW];
+#pragma unroll
+        for (int k = 0; k < kW; ++k) v[k] = bs[k * kTN];
+        const uint32_t col =
+            tmem + ((quad * 32) << 16) + kBtCol + stage * Cfg::kBtColsPerStage + part * kW;
+        bt_to_tmem<kW, true>(col, col + BK, v);
+        float4 *raw = reinterpret_cast<float4 *>(st);
+        float4 *lo = reinterpret_cast<float4 *>(st + Cfg::kALoOffset);
+#pragma unroll
+        for (int i = xt; i < Cfg::kABytes / 16; i += 32 * XW) {
+          const float4 x = raw[i];
+          float4 h, l;
+          h.x = round_tf32(x.x);
+          h.y = round_tf32(x.y);
+          h.z = round_tf32(x.z);
+          h.w = round_tf32(x.w);
+          l.x = round_tf32(x.x - h.x);
+          l.y = round_tf32(x.y - h.y);
+          l.z = round_tf32(x.z - h.z);
+          l.w = round_tf32(x.w - h.w);
+          raw[i] = h;
+          lo[i] = l;
+        }
+        // The MMAs read the split tile through the async proxy and B^T from
+        // TMEM; both are ordered before the arrival.
+        fence_proxy_async_smem();
+        tmem_store_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if (rank == 0)
+            mbar_arrive(&sh->ready[stage]);
+          else
+            mbar_arrive(&sh->relay[stage]);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  }
+
+  // Neither CTA frees its TMEM or leaves while the pair's MMAs, copies or
+  // arrivals may still reach it.
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  if (warp == Cfg::kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc<2>(tmem, kTmemCols);
+  }
+  if (sh->fix_tile >= 0 && !sh->abort) {
+    __threadfence();
+    epilogue_fixup<(Cfg::kThreads > 512 ? 8 : 16)>(p, sh->fix_tile, rank, sh->fix_nparts,
+                                                   sh->fix_mb, sh->fix_nb, threadIdx.x,
+                                                   blockDim.x);
+  }
+}
+
 // One warp waits, bounded, on a barrier that is never signalled.
 __global__ void selftest_wait_kernel(unsigned long long timeout_ns) {
   __shared__ uint64_t bar;
@@ -1398,14 +1701,35 @@ struct KernelOf {
   static constexpr auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST>;
 };
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST>
-struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true> {
-  static_assert(!EXACT && !LSU && CL == 2 && BST == 0, "the pair kernel: one TF32 pass, TMA");
+template <int BK, int STAGES, bool OPA, bool OPB>
+struct PairTf32Kernel {
   using Cfg = PairConfig<BK, STAGES, OPA, OPB>;
   static constexpr int kThreads = Cfg::kThreads;
   static constexpr int kSmemBytes =
       Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
   static constexpr auto kernel = tc_pair_kernel<BK, STAGES, OPA, OPB>;
+};
+
+// Transform warps per CTA of the 3xTF32 pair kernel (16 time the same).
+constexpr int kPairExactXform = 8;
+
+template <int BK, int STAGES, int XW>
+struct PairExactKernel {
+  using Cfg = PairExactConfig<BK, STAGES, XW>;
+  static constexpr int kThreads = Cfg::kThreads;
+  static constexpr int kSmemBytes =
+      Cfg::kTileBytes + static_cast<int>(sizeof(PairExactShared<STAGES>)) + 1024;
+  static constexpr auto kernel = tc_pair_exact_kernel<BK, STAGES, XW>;
+};
+
+// PAIR: the CTA-pair kernels, one TF32 pass (every layout) or 3xTF32 (A
+// stored M x K, B stored K x N).
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST>
+struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true>
+    : std::conditional_t<EXACT, PairExactKernel<BK, STAGES, kPairExactXform>,
+                         PairTf32Kernel<BK, STAGES, OPA, OPB>> {
+  static_assert(!LSU && CL == 2 && BST == 0, "the pair kernels are fed by TMA");
+  static_assert(!EXACT || (!OPA && !OPB), "3xTF32 pairs: A stored M x K, B stored K x N");
 };
 
 // Everything a launch needs except the stream-K workspace.
@@ -1439,7 +1763,7 @@ struct LaunchPlan {
     std::memset(&map_b, 0, sizeof(map_b));
     p.a_one_copy = 0;
     p.b_one_copy = 0;
-    if constexpr (PAIR) {
+    if constexpr (PAIR && !EXACT) {
       // K-major operands: BK k x 128 rows, 128-byte swizzle. MN-major ones
       // (A stored K x M, B stored K x N): 32 mn x BK k, 32-byte atoms.
       const CUtensorMapSwizzle k_sw = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -1457,7 +1781,9 @@ struct LaunchPlan {
     } else if constexpr (!LSU) {
       const CUtensorMapSwizzle sw_a =
           BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-      if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>::kAPartRows, sw_a, &map_a)) return kErrLaunch;
+      // Each CTA of a cluster loads kTM / CL rows of the A tile (the 3xTF32
+      // pair kernel: its own half; tc_gemm_kernel: its half of the multicast).
+      if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, kTM / CL, sw_a, &map_a)) return kErrLaunch;
       if (OPB) {
         // B stored N x K: a K-major BK x 128 box with A's swizzle.
         if (!get_map(a.B, a.K, a.N, a.ldb * 4, BK, kTN, sw_a, &map_b)) return kErrLaunch;
@@ -1514,7 +1840,7 @@ struct LaunchPlan {
     // their MMAs (timed at 4096^3, 5120^3, 2560 x 2560 x 4096 and 8192 x 11008
     // x 4096: +5-6 % for the pair kernel with full waves, -3 % for 3xTF32).
     sch = make_schedule(p.num_tiles, p.num_k_blocks, workers,
-                        (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK, PAIR);
+                        (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK, PAIR && !EXACT);
     p.dp_tiles = sch.dp_tiles;
     p.sk_share = sch.sk_share;
     p.sk_ctas = sch.sk_ctas;
@@ -1638,6 +1964,15 @@ namespace {
 // 0.89 of the peak, 5 0.78 / 0.89, 6 0.80 / 0.86-0.96, 7 0.79 / 0.85 (the
 // pipeline waits on copies, not on free slots, from 6 on).
 constexpr int kPairStages = 6;
+
+// Stages of the 3xTF32 pair kernel: BK k of A (hi and lo, 128 rows) and B
+// (BK x 128) per CTA, 48 KiB at BK = 32; TMEM holds 256 accumulator columns
+// and 2 BK B^T columns per stage, so four stages fill it. Each stage costs one
+// hand-over between the CTAs, which sets the pace of short stages: at 4096^3
+// BK = 16 x 8 stages took 0.64 ms (0.49 with two relay threads), BK = 32 x 4
+// 0.43 ms.
+constexpr int kPairExactBK = 32;
+constexpr int kPairExactStages = 4;
 
 bool tma_operand_ok(const float *ptr, int64_t ld) {
   return reinterpret_cast<uintptr_t>(ptr) % 16 == 0 && ld % 4 == 0;
@@ -1766,7 +2101,8 @@ int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_
   // transform also splits A, loses with the separate ring.
   if (exact) {
     if (lsu) return launch_variant<16, 6, true, true, 1, false>(a, sm_count, stream);
-    return launch_variant<16, 5, true, false, kClusterExact, false>(a, sm_count, stream);
+    return launch_variant<kPairExactBK, kPairExactStages, true, false, 2, false, false, 0, true>(
+        a, sm_count, stream);
   }
   if (lsu) return launch_variant<32, 6, false, true, 1, false>(a, sm_count, stream);
   return launch_variant<32, 5, false, false, kClusterTf32, false, false, 4>(a, sm_count, stream);
@@ -1857,7 +2193,8 @@ int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cud
   // Same kernels and stage shapes as tc_launch.
   if (exact) {
     if (lsu) return launch_variant_noalloc<16, 6, true, true, 1, false>(a, sm_count, stream);
-    return launch_variant_noalloc<16, 5, true, false, kClusterExact, false>(a, sm_count, stream);
+    return launch_variant_noalloc<kPairExactBK, kPairExactStages, true, false, 2, false, 0, true>(
+        a, sm_count, stream);
   }
   if (lsu) return launch_variant_noalloc<32, 6, false, true, 1, false>(a, sm_count, stream);
   return launch_variant_noalloc<32, kPairStages, false, false, 2, false, 0, true>(a, sm_count,

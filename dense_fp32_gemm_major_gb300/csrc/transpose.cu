@@ -5,10 +5,12 @@
 // first rewritten as a row-major M x K copy with a 16-byte pitch. The copy is
 // bound by HBM bandwidth (one read and one write of the matrix).
 //
-// A CTA of 256 threads moves 32 x 32 tiles through shared memory (a padded
-// 32 x 33 array, so that the column reads of the transposed store do not
+// A CTA of 256 threads moves 64 x 64 tiles through shared memory (a padded
+// 64 x 65 array, so that the column reads of the transposed store do not
 // conflict): loads and stores are each one coalesced 128-byte row segment
-// per warp. CTAs are persistent and walk the tiles in steps of the grid.
+// per warp, sixteen loads in flight per thread (the copy is bound by how many
+// bytes are in flight per SM). CTAs are persistent and walk the tiles in
+// steps of the grid.
 
 #include <cuda_runtime.h>
 
@@ -19,29 +21,40 @@
 namespace gemm {
 namespace {
 
-constexpr int kT = 32;
-constexpr int kRowsPerPass = 8;  // 256 threads = 8 rows of 32
-constexpr int kBlocksPerSm = 8;
+constexpr int kT = 64;            // tile edge
+constexpr int kW = 32;            // columns per warp access
+constexpr int kRowsPerPass = 8;   // 256 threads = 8 warps
+constexpr int kBlocksPerSm = 32;  // grid cap: up to one tile per CTA at the usual sizes
 
-__global__ void __launch_bounds__(kT * kRowsPerPass)
+__global__ void __launch_bounds__(kW * kRowsPerPass)
     transpose_kernel(const float *__restrict__ src, long long lds, int rows, int cols,
                      float *__restrict__ dst, long long ldd, int tiles_c, long long tiles) {
   __shared__ float t[kT][kT + 1];
-  const int tx = threadIdx.x % kT, ty = threadIdx.x / kT;
+  const int tx = threadIdx.x % kW, ty = threadIdx.x / kW;
   for (long long tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int r0 = static_cast<int>(tile / tiles_c) * kT;
     const int c0 = static_cast<int>(tile % tiles_c) * kT;
+    float v[kT / kRowsPerPass][2];
 #pragma unroll
-    for (int i = ty; i < kT; i += kRowsPerPass) {
-      const int r = r0 + i, c = c0 + tx;
-      if (r < rows && c < cols) t[i][tx] = __ldg(src + static_cast<long long>(r) * lds + c);
-    }
+    for (int i = 0; i < kT / kRowsPerPass; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int r = r0 + ty + i * kRowsPerPass, c = c0 + tx + h * kW;
+        v[i][h] = (r < rows && c < cols) ? __ldg(src + static_cast<long long>(r) * lds + c) : 0.0f;
+      }
+#pragma unroll
+    for (int i = 0; i < kT / kRowsPerPass; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) t[ty + i * kRowsPerPass][tx + h * kW] = v[i][h];
     __syncthreads();
 #pragma unroll
-    for (int i = ty; i < kT; i += kRowsPerPass) {
-      const int c = c0 + i, r = r0 + tx;  // dst row c, column r
-      if (c < cols && r < rows) dst[static_cast<long long>(c) * ldd + r] = t[tx][i];
-    }
+    for (int i = 0; i < kT / kRowsPerPass; ++i)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = c0 + ty + i * kRowsPerPass, r = r0 + tx + h * kW;  // dst row c, column r
+        if (c < cols && r < rows)
+          dst[static_cast<long long>(c) * ldd + r] = t[tx + h * kW][ty + i * kRowsPerPass];
+      }
     __syncthreads();
   }
 }
@@ -55,7 +68,7 @@ int transpose_launch(const float *src, int64_t lds, int64_t rows, int64_t cols, 
   const long long tiles = tiles_r * tiles_c;
   const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * kBlocksPerSm;
   const unsigned grid = static_cast<unsigned>(tiles < cap ? tiles : cap);
-  transpose_kernel<<<grid, kT * kRowsPerPass, 0, stream>>>(
+  transpose_kernel<<<grid, kW * kRowsPerPass, 0, stream>>>(
       src, lds, static_cast<int>(rows), static_cast<int>(cols), dst, ldd,
       static_cast<int>(tiles_c), tiles);
   return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
