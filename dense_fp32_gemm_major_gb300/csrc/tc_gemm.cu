@@ -1222,18 +1222,25 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
 // shared memory can serve at full tensor rate; with the pair each SM reads
 // and splits only its own 128 rows, for the same MMA work per SM.
 //
-// Per stage each CTA loads, by TMA on its own barrier, its 128 A rows x BK k
-// (K-major, swizzled) and its B tile BK k x 128 n (row-major). Its transform
-// warps move B^T as hi and lo into its own TMEM (lane = n, one column per k)
-// and split its A rows in place (hi) and into a sibling tile (lo). The even
-// CTA's transform warps then arrive on its `ready` barrier; the odd CTA's
-// arrive on a local barrier, and one relay thread passes the stage on with a
-// single remote arrive (a release at cluster scope, which orders the odd
-// CTA's shared-memory and TMEM writes before the even CTA's MMAs). The even
-// CTA issues B_lo*A_hi, B_hi*A_lo, B_hi*A_hi per k-step of 8 with A from TMEM
-// and B from shared memory, and its commits free the stage in both CTAs.
-// TMEM: one 256-column accumulator, then 2 BK columns (hi, lo) per stage.
-template <int BK, int STAGES, int XW>
+// Per k-block of BK each CTA loads, by TMA on its own barriers, its 128 A
+// rows x BK k (K-major, swizzled) into a ring of A stages and its B tile
+// BK k x 128 n (row-major) into a ring of B slots. Its transform warps take
+// the B tile into registers (freeing the slot), write B^T as hi and lo into
+// a TMEM slot of its own (lane = n, one column per k) and split the A rows in
+// place (hi) and into a sibling tile (lo). The even CTA's transform warps
+// then arrive on its `ready` barrier; the odd CTA's arrive on a local barrier,
+// and one relay thread passes the k-block on with a single remote arrive (a
+// release at cluster scope, which orders the odd CTA's shared-memory and
+// TMEM writes before the even CTA's MMAs). The even CTA issues B_lo*A_hi,
+// B_hi*A_lo, B_hi*A_hi per k-step of 8 with A from TMEM and B from shared
+// memory; its commits free the A stage and the TMEM slot in both CTAs.
+//
+// TMEM holds one 256-column accumulator and TST = 256 / (2 BK) B^T slots. The
+// A ring is deeper than that, and B has a ring of its own, so the copies run
+// ahead of the TMEM slots: a slot's round trip (the MMAs that read it, the
+// transform of the next k-block, the hand-over) does not include a copy's
+// latency.
+template <int BK, int AST, int BST, int XW>
 struct PairExactConfig {
   static_assert(BK == 16 || BK == 32, "BK");
   static constexpr int kHalfRows = 128;                          // A rows per CTA
@@ -1242,11 +1249,12 @@ struct PairExactConfig {
   static constexpr uint32_t kLayout = BK == 32 ? 2u : 4u;        // 128- or 64-byte swizzle
   static constexpr int kABytes = kHalfRows * BK * 4;             // A rows (hi after the split)
   static constexpr int kALoOffset = kABytes;                     // A lo, same layout
-  static constexpr int kBOffset = 2 * kABytes;                   // B tile, BK x 128, row-major
-  static constexpr int kBBytes = BK * kTN * 4;
-  static constexpr int kStageBytes = 2 * kABytes + kBBytes;
-  static constexpr int kTileBytes = STAGES * kStageBytes;
-  static constexpr uint32_t kBtColsPerStage = 2 * BK;            // B^T hi, then lo
+  static constexpr int kAStageBytes = 2 * kABytes;
+  static constexpr int kBBytes = BK * kTN * 4;                   // B tile, BK x 128, row-major
+  static constexpr int kBRingOffset = AST * kAStageBytes;
+  static constexpr int kTileBytes = AST * kAStageBytes + BST * kBBytes;
+  static constexpr uint32_t kBtColsPerSlot = 2 * BK;             // B^T hi, then lo
+  static constexpr int kTmemSlots = static_cast<int>((kTmemCols - kBtCol) / kBtColsPerSlot);
   static constexpr int kAccBufs = 1;
   static constexpr int kMmaWarp = 1;
   static constexpr int kEpiWarp0 = 2;
@@ -1254,29 +1262,54 @@ struct PairExactConfig {
   static constexpr int kXformParts = XW / 4;                     // per TMEM lane quadrant
   static constexpr int kThreads = 32 * (kXformWarp0 + XW);
   static constexpr uint32_t kIdesc = idesc_tf32(2 * kTN, kTM);   // both operands K-major
-  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(kAStageBytes % 1024 == 0 && kBRingOffset % 1024 == 0,
+                "swizzled A stages keep 1024-byte alignment");
   static_assert(XW % 4 == 0 && BK % kXformParts == 0 && (BK / kXformParts) % 4 == 0,
                 "transform partition");
-  static_assert(kBtCol + STAGES * kBtColsPerStage <= kTmemCols, "TMEM budget");
+  static_assert(AST >= kTmemSlots, "the A ring covers the TMEM slots");
 };
 
-// Shared state of the 3xTF32 pair kernel: TcShared plus the odd CTA's local
-// barriers on which its transform warps arrive before one thread passes the
-// stage on to the even CTA.
-template <int STAGES>
-struct alignas(8) PairExactShared : TcShared<STAGES> {
-  uint64_t relay[STAGES];
+// Shared state of the 3xTF32 pair kernel.
+template <int AST, int BST, int TST>
+struct alignas(8) PairExactShared {
+  uint64_t full[AST];      // A stage loaded (TMA bytes)
+  uint64_t empty[AST];     // A stage consumed by the MMAs (the even CTA's commit, both CTAs)
+  uint64_t bfull[BST];     // B slot loaded (TMA bytes)
+  uint64_t bempty[BST];    // B slot read by this CTA's transform warps
+  uint64_t ready[TST];     // even CTA: k-block transformed in both CTAs
+  uint64_t relay[TST];     // odd CTA: k-block transformed by its own transform warps
+  uint64_t tfree[TST];     // TMEM slot's MMAs completed (the even CTA's commit, both CTAs)
+  uint64_t acc_full[2];    // accumulator complete
+  uint64_t acc_empty[2];   // accumulator drained by the epilogue warps of both CTAs
+  uint64_t drain;          // every MMA of the pair has completed
+  uint32_t tmem_base;
+  int abort;
+  int sk_last;
+  int fix_tile, fix_nparts, fix_mb, fix_nb;
 };
 
-template <int BK, int STAGES, int XW>
-__global__ void __launch_bounds__(PairExactConfig<BK, STAGES, XW>::kThreads, 1)
+// Ring position: index and phase parity of a ring of N entries.
+template <int N>
+struct RingPos {
+  uint32_t idx = 0, phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++idx == N) {
+      idx = 0;
+      phase ^= 1;
+    }
+  }
+};
+
+template <int BK, int AST, int BST, int XW>
+__global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW>::kThreads, 1)
     tc_pair_exact_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
-  using Cfg = PairExactConfig<BK, STAGES, XW>;
+  using Cfg = PairExactConfig<BK, AST, BST, XW>;
+  constexpr int TST = Cfg::kTmemSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  PairExactShared<STAGES> *sh = reinterpret_cast<PairExactShared<STAGES> *>(tiles + Cfg::kTileBytes);
+  auto *sh = reinterpret_cast<PairExactShared<AST, BST, TST> *>(tiles + Cfg::kTileBytes);
   volatile int *abort = &sh->abort;
 
   const uint32_t warp = warp_index();
@@ -1284,11 +1317,18 @@ __global__ void __launch_bounds__(PairExactConfig<BK, STAGES, XW>::kThreads, 1)
   const uint32_t rank = cluster_ctarank();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sh->full[s], 1);        // this CTA's producer; its own copies' bytes
-      mbar_init(&sh->ready[s], XW + 1);  // even CTA: its transform warps, the odd CTA's relay
-      mbar_init(&sh->empty[s], 1);       // the even CTA's commit, multicast to both
-      mbar_init(&sh->relay[s], XW);      // odd CTA: its transform warps
+    for (int s = 0; s < AST; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    for (int b = 0; b < BST; ++b) {
+      mbar_init(&sh->bfull[b], 1);
+      mbar_init(&sh->bempty[b], XW);
+    }
+    for (int t = 0; t < TST; ++t) {
+      mbar_init(&sh->ready[t], XW + 1);  // the even CTA's transform warps, the odd CTA's relay
+      mbar_init(&sh->relay[t], XW);
+      mbar_init(&sh->tfree[t], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh->acc_full[a], 1);
@@ -1316,7 +1356,9 @@ __global__ void __launch_bounds__(PairExactConfig<BK, STAGES, XW>::kThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
-      uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
+      RingPos<AST> a;
+      RingPos<BST> b;
+      uint32_t armed = 0, armed_parity = 0, barmed = 0, barmed_parity = 0;
       bool ok = true;
       UnitIter it(p);
       WorkUnit u;
@@ -1326,32 +1368,44 @@ __global__ void __launch_bounds__(PairExactConfig<BK, STAGES, XW>::kThreads, 1)
         const int m0 = mb * kTM + static_cast<int>(rank) * Cfg::kHalfRows;
         const int n0 = nb * kTN;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          if (!mbar_wait_bounded(&sh->empty[stage], phase ^ 1, p.timeout_ns, abort,
+          if (!mbar_wait_bounded(&sh->empty[a.idx], a.phase ^ 1, p.timeout_ns, abort,
                                  &g_tc_status)) {
             ok = false;
             break;
           }
-          uint8_t *st = tiles + stage * Cfg::kStageBytes;
-          mbar_arrive_expect_tx(&sh->full[stage], Cfg::kABytes + Cfg::kBBytes);
-          tma_load_2d(st, &tmap_a, &sh->full[stage], kb * BK, m0);
-          tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], n0, kb * BK);
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
+          mbar_arrive_expect_tx(&sh->full[a.idx], Cfg::kABytes);
+          tma_load_2d(tiles + a.idx * Cfg::kAStageBytes, &tmap_a, &sh->full[a.idx], kb * BK, m0);
+          armed |= 1u << a.idx;
+          armed_parity = (armed_parity & ~(1u << a.idx)) | (a.phase << a.idx);
+          a.next();
+          if (!mbar_wait_bounded(&sh->bempty[b.idx], b.phase ^ 1, p.timeout_ns, abort,
+                                 &g_tc_status)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(&sh->bfull[b.idx], Cfg::kBBytes);
+          tma_load_2d(tiles + Cfg::kBRingOffset + b.idx * Cfg::kBBytes, &tmap_b, &sh->bfull[b.idx],
+                      n0, kb * BK);
+          barmed |= 1u << b.idx;
+          barmed_parity = (barmed_parity & ~(1u << b.idx)) | (b.phase << b.idx);
+          b.next();
         }
       }
       // Let every copy this thread issued land before the CTA exits.
-      if (!ok)
-        for (int s = 0; s < STAGES; ++s)
+      if (!ok) {
+        for (int s = 0; s < AST; ++s)
           if (armed & (1u << s)) drain_wait(&sh->full[s], (armed_parity >> s) & 1u, p.timeout_ns);
+        for (int s = 0; s < BST; ++s)
+          if (barmed & (1u << s))
+            drain_wait(&sh->bfull[s], (barmed_parity >> s) & 1u, p.timeout_ns);
+      }
     }
   } else if (warp == Cfg::kMmaWarp) {
-    // ------------------------------------------------- MMA (even CTA) --
     if (rank == 0 && lane == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      // ----------------------------------------------- MMA (even CTA) --
+      RingPos<AST> a;
+      RingPos<TST> t;
+      uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
       UnitIter it(p);
       WorkUnit u;
@@ -1365,16 +1419,16 @@ __global__ void __launch_bounds__(PairExactConfig<BK, STAGES, XW>::kThreads, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem + kAccCol + acc * kTM;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          // Both CTAs' transform warps are done with the stage (the odd
-          // CTA's arrivals come from the peer: acquire at cluster scope).
-          if (!mbar_wait_bounded<true>(&sh->ready[stage], phase, p.timeout_ns, abort,
+          // Both CTAs' transform warps are done with the k-block (the odd
+          // CTA's relay arrives from the peer: acquire at cluster scope).
+          if (!mbar_wait_bounded<true>(&sh->ready[t.idx], t.phase, p.timeout_ns, abort,
                                        &g_tc_status)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a_hi = smem_addr(tiles + stage * Cfg::kStageBytes);
-          const uint32_t bt_hi = tmem + kBtCol + stage * Cfg::kBtColsPerStage;
+          const uint32_t a_hi = smem_addr(tiles + a.idx * Cfg::kAStageBytes);
+          const uint32_t bt_hi = tmem + kBtCol + t.idx * Cfg::kBtColsPerSlot;
 #pragma unroll
           for (int kk = 0; kk < BK / kUmmaK; ++kk) {
             const uint64_t da = smem_desc(a_hi + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
@@ -1385,11 +1439,10 @@ __global__ void __launch_bounds__(PairExactConfig<BK, STAGES, XW>::kThreads, 1)
             mma_tf32_ts<2>(d_tmem, bt_hi + kk * kUmmaK, da_lo, Cfg::kIdesc, 1);
             mma_tf32_ts<2>(d_tmem, bt_hi + kk * kUmmaK, da, Cfg::kIdesc, 1);
           }
-          mma_commit_multicast<2>(&sh->empty[stage], 3);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+          mma_commit_multicast<2>(&sh->empty[a.idx], 3);
+          mma_commit_multicast<2>(&sh->tfree[t.idx], 3);
+          a.next();
+          t.next();
         }
         if (!ok) break;
         mma_commit_multicast<2>(&sh->acc_full[acc], 3);
@@ -1402,25 +1455,22 @@ __global__ void __launch_bounds__(PairExactConfig<BK, STAGES, XW>::kThreads, 1)
       mma_commit_multicast<2>(&sh->drain, 1);
       drain_wait(&sh->drain, 0, p.timeout_ns);
     } else if (rank == 1 && lane == 0) {
-      // -------------------------------------------- relay (odd CTA) --
-      // Once all of this CTA's transform warps are done with a stage, one
+      // ---------------------------------------------- relay (odd CTA) --
+      // Once all of this CTA's transform warps are done with a k-block, one
       // release at cluster scope passes it on to the even CTA's MMAs (eight
-      // warps each arriving remotely took twice as long per stage).
-      uint32_t stage = 0, phase = 0;
+      // warps each arriving remotely took twice as long per k-block).
+      RingPos<TST> t;
       bool ok = true;
       UnitIter it(p);
       WorkUnit u;
       while (ok && it.next(p, u)) {
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          if (!mbar_wait_bounded(&sh->relay[stage], phase, p.timeout_ns, abort, &g_tc_status)) {
+          if (!mbar_wait_bounded(&sh->relay[t.idx], t.phase, p.timeout_ns, abort, &g_tc_status)) {
             ok = false;
             break;
           }
-          mbar_arrive_cluster(&sh->ready[stage], 0);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
+          mbar_arrive_cluster(&sh->ready[t.idx], 0);
+          t.next();
         }
       }
     }
@@ -1437,28 +1487,44 @@ __global__ void __launch_bounds__(PairExactConfig<BK, STAGES, XW>::kThreads, 1)
     const uint32_t part = (warp - Cfg::kXformWarp0) >> 2;
     const int xt = threadIdx.x - Cfg::kXformWarp0 * 32;
     constexpr int kW = BK / Cfg::kXformParts;
-    uint32_t stage = 0, phase = 0;
+    RingPos<AST> a;
+    RingPos<BST> b;
+    RingPos<TST> t;
     bool ok = true;
     UnitIter it(p);
     WorkUnit u;
     while (ok && it.next(p, u)) {
       for (int kb = u.kb0; kb < u.kb1; ++kb) {
-        if (!warp_wait(&sh->full[stage], phase, p, abort)) {
+        // B tile into registers; the slot can then be refilled.
+        if (!warp_wait(&sh->bfull[b.idx], b.phase, p, abort)) {
+          ok = false;
+          break;
+        }
+        const float *bs =
+            reinterpret_cast<const float *>(tiles + Cfg::kBRingOffset + b.idx * Cfg::kBBytes) +
+            part * kW * kTN + quad * 32 + lane;
+        float v[kW];
+#pragma unroll
+        for (int k = 0; k < kW; ++k) v[k] = bs[k * kTN];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->bempty[b.idx]);
+        b.next();
+        // B^T into the TMEM slot once the MMAs that last read it are done.
+        if (!warp_wait(&sh->tfree[t.idx], t.phase ^ 1, p, abort)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        uint8_t *st = tiles + stage * Cfg::kStageBytes;
-        const float *bs = reinterpret_cast<const float *>(st + Cfg::kBOffset) + part * kW * kTN +
-                          quad * 32 + lane;
-        float v[kW];
-#pragma unroll
-        for (int k = 0; k < kW; ++k) v[k] = bs[k * kTN];
         const uint32_t col =
-            tmem + ((quad * 32) << 16) + kBtCol + stage * Cfg::kBtColsPerStage + part * kW;
+            tmem + ((quad * 32) << 16) + kBtCol + t.idx * Cfg::kBtColsPerSlot + part * kW;
         bt_to_tmem<kW, true>(col, col + BK, v);
-        float4 *raw = reinterpret_cast<float4 *>(st);
-        float4 *lo = reinterpret_cast<float4 *>(st + Cfg::kALoOffset);
+        // Split the A rows: hi in place, lo in the sibling tile.
+        if (!warp_wait(&sh->full[a.idx], a.phase, p, abort)) {
+          ok = false;
+          break;
+        }
+        float4 *raw = reinterpret_cast<float4 *>(tiles + a.idx * Cfg::kAStageBytes);
+        float4 *lo = reinterpret_cast<float4 *>(tiles + a.idx * Cfg::kAStageBytes + Cfg::kALoOffset);
 #pragma unroll
         for (int i = xt; i < Cfg::kABytes / 16; i += 32 * XW) {
           const float4 x = raw[i];
@@ -1480,16 +1546,9 @@ __global__ void __launch_bounds__(PairExactConfig<BK, STAGES, XW>::kThreads, 1)
         tmem_store_wait();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
-          if (rank == 0)
-            mbar_arrive(&sh->ready[stage]);
-          else
-            mbar_arrive(&sh->relay[stage]);
-        }
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
+        if (lane == 0) mbar_arrive(rank == 0 ? &sh->ready[t.idx] : &sh->relay[t.idx]);
+        a.next();
+        t.next();
       }
     }
   }
@@ -1713,22 +1772,24 @@ struct PairTf32Kernel {
 // Transform warps per CTA of the 3xTF32 pair kernel (16 time the same).
 constexpr int kPairExactXform = 8;
 
-template <int BK, int STAGES, int XW>
+template <int BK, int AST, int BST, int XW>
 struct PairExactKernel {
-  using Cfg = PairExactConfig<BK, STAGES, XW>;
+  using Cfg = PairExactConfig<BK, AST, BST, XW>;
   static constexpr int kThreads = Cfg::kThreads;
   static constexpr int kSmemBytes =
-      Cfg::kTileBytes + static_cast<int>(sizeof(PairExactShared<STAGES>)) + 1024;
-  static constexpr auto kernel = tc_pair_exact_kernel<BK, STAGES, XW>;
+      Cfg::kTileBytes +
+      static_cast<int>(sizeof(PairExactShared<AST, BST, Cfg::kTmemSlots>)) + 1024;
+  static constexpr auto kernel = tc_pair_exact_kernel<BK, AST, BST, XW>;
 };
 
 // PAIR: the CTA-pair kernels, one TF32 pass (every layout) or 3xTF32 (A
 // stored M x K, B stored K x N).
+// With EXACT, STAGES counts A stages and BST the B slots.
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST>
 struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true>
-    : std::conditional_t<EXACT, PairExactKernel<BK, STAGES, kPairExactXform>,
+    : std::conditional_t<EXACT, PairExactKernel<BK, STAGES, BST, kPairExactXform>,
                          PairTf32Kernel<BK, STAGES, OPA, OPB>> {
-  static_assert(!LSU && CL == 2 && BST == 0, "the pair kernels are fed by TMA");
+  static_assert(!LSU && CL == 2 && (EXACT ? BST > 0 : BST == 0), "the pair kernels are fed by TMA");
   static_assert(!EXACT || (!OPA && !OPB), "3xTF32 pairs: A stored M x K, B stored K x N");
 };
 
@@ -1965,14 +2026,15 @@ namespace {
 // pipeline waits on copies, not on free slots, from 6 on).
 constexpr int kPairStages = 6;
 
-// Stages of the 3xTF32 pair kernel: BK k of A (hi and lo, 128 rows) and B
-// (BK x 128) per CTA, 48 KiB at BK = 32; TMEM holds 256 accumulator columns
-// and 2 BK B^T columns per stage, so four stages fill it. Each stage costs one
-// hand-over between the CTAs, which sets the pace of short stages: at 4096^3
-// BK = 16 x 8 stages took 0.64 ms (0.49 with two relay threads), BK = 32 x 4
-// 0.43 ms.
+// Rings of the 3xTF32 pair kernel, per CTA: A stages of BK k (hi and lo, 128
+// rows: 32 KiB at BK = 32) and B slots (BK x 128: 16 KiB); TMEM holds 256
+// accumulator columns and four B^T slots of 2 BK columns. Each k-block costs
+// one hand-over between the CTAs, which sets the pace of short k-blocks: at
+// 4096^3 BK = 16 took 0.64 ms (0.49 with two relay threads), BK = 32 with
+// the B tile inside four 48 KiB stages 0.43 ms.
 constexpr int kPairExactBK = 32;
-constexpr int kPairExactStages = 4;
+constexpr int kPairExactStages = 6;
+constexpr int kPairExactBSlots = 2;
 
 bool tma_operand_ok(const float *ptr, int64_t ld) {
   return reinterpret_cast<uintptr_t>(ptr) % 16 == 0 && ld % 4 == 0;
@@ -2101,8 +2163,8 @@ int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_
   // transform also splits A, loses with the separate ring.
   if (exact) {
     if (lsu) return launch_variant<16, 6, true, true, 1, false>(a, sm_count, stream);
-    return launch_variant<kPairExactBK, kPairExactStages, true, false, 2, false, false, 0, true>(
-        a, sm_count, stream);
+    return launch_variant<kPairExactBK, kPairExactStages, true, false, 2, false, false,
+                          kPairExactBSlots, true>(a, sm_count, stream);
   }
   if (lsu) return launch_variant<32, 6, false, true, 1, false>(a, sm_count, stream);
   return launch_variant<32, 5, false, false, kClusterTf32, false, false, 4>(a, sm_count, stream);
@@ -2193,8 +2255,8 @@ int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cud
   // Same kernels and stage shapes as tc_launch.
   if (exact) {
     if (lsu) return launch_variant_noalloc<16, 6, true, true, 1, false>(a, sm_count, stream);
-    return launch_variant_noalloc<kPairExactBK, kPairExactStages, true, false, 2, false, 0, true>(
-        a, sm_count, stream);
+    return launch_variant_noalloc<kPairExactBK, kPairExactStages, true, false, 2, false,
+                                  kPairExactBSlots, true>(a, sm_count, stream);
   }
   if (lsu) return launch_variant_noalloc<32, 6, false, true, 1, false>(a, sm_count, stream);
   return launch_variant_noalloc<32, kPairStages, false, false, 2, false, 0, true>(a, sm_count,
