@@ -1897,11 +1897,13 @@ struct LaunchPlan {
       }
       workers = workers_cached[dev];
     }
-    // The TF32 pair kernel is bound by operand traffic from L2, the others by
-    // their MMAs (timed at 4096^3, 5120^3, 2560 x 2560 x 4096 and 8192 x 11008
-    // x 4096: +5-6 % for the pair kernel with full waves, -3 % for 3xTF32).
+    // Full waves for the pair kernels, balanced for tc_gemm_kernel (timed at
+    // 4096^3, 5120^3, 2560 x 2560 x 4096 and 8192 x 11008 x 4096: +5-6 % for
+    // the TF32 pair kernel, which is bound by operand traffic from L2, +3 % at
+    // 4096^3 for the 3xTF32 pair kernel, whose split tiles then have fewer
+    // parts to sum, and -3 % for tc_gemm_kernel's 3xTF32).
     sch = make_schedule(p.num_tiles, p.num_k_blocks, workers,
-                        (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK, PAIR && !EXACT);
+                        (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK, PAIR);
     p.dp_tiles = sch.dp_tiles;
     p.sk_share = sch.sk_share;
     p.sk_ctas = sch.sk_ctas;
