@@ -182,16 +182,13 @@ def time_steps(torch, fn, steps, warmup, flush_buf, stream, barrier=None):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], wall
 
 
-def kernel_label(g, kernel, mode, transb=False):
+def kernel_label(g, kernel, mode):
     """Name of the kernel gemm_f32 runs for this selection: the TMA-fed TF32
-    pass and 3xTF32 with B stored K x N run on CTA-pair kernels, 3xTF32 with B
-    stored transposed on the multicast-pair kernel."""
+    pass and 3xTF32 run on CTA-pair kernels."""
     if kernel == g.KERNEL_SIMT:
         return "simt_gemm"
     if kernel == g.KERNEL_TC_TMA:
-        if mode == "exact":
-            return "tc_gemm_tma_3xtf32" if transb else "tc_pair_tma_3xtf32"
-        return "tc_pair_tma_tf32"
+        return "tc_pair_tma_3xtf32" if mode == "exact" else "tc_pair_tma_tf32"
     if kernel == g.KERNEL_TC_LSU:
         return "tc_gemm_lsu_3xtf32" if mode == "exact" else "tc_gemm_lsu_tf32"
     return str(kernel)
@@ -390,7 +387,7 @@ def main():
     mode = g.MODES[args.mode]
     kernel = g.gemm_f32_select(M, N, K, dA.data_ptr(), K, dB.data_ptr(), N, dC.data_ptr(), N,
                                mode, g.KERNEL_AUTO)
-    kernel_name = kernel_label(g, kernel, args.mode, transb=args.layout in ("nt", "tt"))
+    kernel_name = kernel_label(g, kernel, args.mode)
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if sampler:

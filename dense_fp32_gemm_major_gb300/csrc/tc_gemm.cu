@@ -1212,7 +1212,7 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
 // -------------------------------------------------- CTA-pair 3xTF32 kernel --
 //
 // 3xTF32 on the two SMs of a cluster acting as one tensor core, for A stored
-// M x K and B stored K x N. The pair computes one unit tile, 256 n x 256 m
+// M x K and B stored K x N or (OPB) N x K. The pair computes one unit tile, 256 n x 256 m
 // of C^T, as in tc_pair_kernel: M = 256 (B_tile^T, CTA r holding n rows
 // 128 r ..), N = 256 (the A tile, CTA r holding m rows 128 r ..), K = 8.
 //
@@ -1224,7 +1224,8 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
 //
 // Per k-block of BK each CTA loads, by TMA on its own barriers, its 128 A
 // rows x BK k (K-major, swizzled) into a ring of A stages and its B tile
-// BK k x 128 n (row-major) into a ring of B slots. Its transform warps take
+// (BK k x 128 n row-major, or with OPB 128 n x BK k K-major and swizzled like
+// A) into a ring of B slots. Its transform warps take
 // the B tile into registers (freeing the slot), write B^T as hi and lo into
 // a TMEM slot of its own (lane = n, one column per k) and split the A rows in
 // place (hi) and into a sibling tile (lo). The even CTA's transform warps
@@ -1240,7 +1241,7 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
 // ahead of the TMEM slots: a slot's round trip (the MMAs that read it, the
 // transform of the next k-block, the hand-over) does not include a copy's
 // latency.
-template <int BK, int AST, int BST, int XW>
+template <int BK, int AST, int BST, int XW, bool OPB>
 struct PairExactConfig {
   static_assert(BK == 16 || BK == 32, "BK");
   static constexpr int kHalfRows = 128;                          // A rows per CTA
@@ -1250,7 +1251,9 @@ struct PairExactConfig {
   static constexpr int kABytes = kHalfRows * BK * 4;             // A rows (hi after the split)
   static constexpr int kALoOffset = kABytes;                     // A lo, same layout
   static constexpr int kAStageBytes = 2 * kABytes;
-  static constexpr int kBBytes = BK * kTN * 4;                   // B tile, BK x 128, row-major
+  // B tile: BK k x 128 n row-major (B stored K x N), or 128 n x BK k K-major
+  // with A's swizzle (B stored N x K).
+  static constexpr int kBBytes = BK * kTN * 4;
   static constexpr int kBRingOffset = AST * kAStageBytes;
   static constexpr int kTileBytes = AST * kAStageBytes + BST * kBBytes;
   static constexpr uint32_t kBtColsPerSlot = 2 * BK;             // B^T hi, then lo
@@ -1300,11 +1303,11 @@ struct RingPos {
   }
 };
 
-template <int BK, int AST, int BST, int XW>
-__global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW>::kThreads, 1)
+template <int BK, int AST, int BST, int XW, bool OPB>
+__global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThreads, 1)
     tc_pair_exact_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
-  using Cfg = PairExactConfig<BK, AST, BST, XW>;
+  using Cfg = PairExactConfig<BK, AST, BST, XW, OPB>;
   constexpr int TST = Cfg::kTmemSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
@@ -1384,8 +1387,12 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW>::kThreads, 1
             break;
           }
           mbar_arrive_expect_tx(&sh->bfull[b.idx], Cfg::kBBytes);
-          tma_load_2d(tiles + Cfg::kBRingOffset + b.idx * Cfg::kBBytes, &tmap_b, &sh->bfull[b.idx],
-                      n0, kb * BK);
+          if (OPB)
+            tma_load_2d(tiles + Cfg::kBRingOffset + b.idx * Cfg::kBBytes, &tmap_b,
+                        &sh->bfull[b.idx], kb * BK, n0);
+          else
+            tma_load_2d(tiles + Cfg::kBRingOffset + b.idx * Cfg::kBBytes, &tmap_b,
+                        &sh->bfull[b.idx], n0, kb * BK);
           barmed |= 1u << b.idx;
           barmed_parity = (barmed_parity & ~(1u << b.idx)) | (b.phase << b.idx);
           b.next();
@@ -1500,12 +1507,27 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW>::kThreads, 1
           ok = false;
           break;
         }
-        const float *bs =
-            reinterpret_cast<const float *>(tiles + Cfg::kBRingOffset + b.idx * Cfg::kBBytes) +
-            part * kW * kTN + quad * 32 + lane;
+        const uint8_t *bslot = tiles + Cfg::kBRingOffset + b.idx * Cfg::kBBytes;
         float v[kW];
+        if constexpr (OPB) {
+          // Row n = 32 quad + lane of the K-major tile; this part's kW k as
+          // 16-byte chunks of the swizzled row.
+          const int n = quad * 32 + lane;
 #pragma unroll
-        for (int k = 0; k < kW; ++k) v[k] = bs[k * kTN];
+          for (int c = 0; c < kW / 4; ++c) {
+            const float4 x = *reinterpret_cast<const float4 *>(
+                bslot + swizzle_a<BK>(n * Cfg::kRowBytes + (part * kW + c * 4) * 4));
+            v[c * 4 + 0] = x.x;
+            v[c * 4 + 1] = x.y;
+            v[c * 4 + 2] = x.z;
+            v[c * 4 + 3] = x.w;
+          }
+        } else {
+          // Column n = 32 quad + lane of the row-major tile.
+          const float *bs = reinterpret_cast<const float *>(bslot) + part * kW * kTN + quad * 32 + lane;
+#pragma unroll
+          for (int k = 0; k < kW; ++k) v[k] = bs[k * kTN];
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->bempty[b.idx]);
         b.next();
@@ -1680,11 +1702,6 @@ bool get_map(const void *ptr, uint64_t d0, uint64_t d1, uint64_t pitch_bytes, ui
   return get_map_rank(ptr, d0, d1, pitch_bytes, b0, b1, swizzle, 2, out);
 }
 
-// CTAs per cluster of the TMA-fed kernels (pairs share the A tile by
-// multicast, which halves its L2 reads).
-constexpr int kClusterExact = 2;
-constexpr int kClusterTf32 = 2;
-
 // Smallest stream-K chunk, in k: shorter chunks spend more time filling the
 // pipeline and more bytes on partial tiles than they save. One TF32 pass
 // does a third of the MMA work per k of 3xTF32, so splitting pays only for
@@ -1772,25 +1789,25 @@ struct PairTf32Kernel {
 // Transform warps per CTA of the 3xTF32 pair kernel (16 time the same).
 constexpr int kPairExactXform = 8;
 
-template <int BK, int AST, int BST, int XW>
+template <int BK, int AST, int BST, int XW, bool OPB>
 struct PairExactKernel {
-  using Cfg = PairExactConfig<BK, AST, BST, XW>;
+  using Cfg = PairExactConfig<BK, AST, BST, XW, OPB>;
   static constexpr int kThreads = Cfg::kThreads;
   static constexpr int kSmemBytes =
       Cfg::kTileBytes +
       static_cast<int>(sizeof(PairExactShared<AST, BST, Cfg::kTmemSlots>)) + 1024;
-  static constexpr auto kernel = tc_pair_exact_kernel<BK, AST, BST, XW>;
+  static constexpr auto kernel = tc_pair_exact_kernel<BK, AST, BST, XW, OPB>;
 };
 
 // PAIR: the CTA-pair kernels, one TF32 pass (every layout) or 3xTF32 (A
-// stored M x K, B stored K x N).
+// stored M x K, B in either storage).
 // With EXACT, STAGES counts A stages and BST the B slots.
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST>
 struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true>
-    : std::conditional_t<EXACT, PairExactKernel<BK, STAGES, BST, kPairExactXform>,
+    : std::conditional_t<EXACT, PairExactKernel<BK, STAGES, BST, kPairExactXform, OPB>,
                          PairTf32Kernel<BK, STAGES, OPA, OPB>> {
   static_assert(!LSU && CL == 2 && (EXACT ? BST > 0 : BST == 0), "the pair kernels are fed by TMA");
-  static_assert(!EXACT || (!OPA && !OPB), "3xTF32 pairs: A stored M x K, B stored K x N");
+  static_assert(!EXACT || !OPA, "3xTF32 pairs: A stored M x K");
 };
 
 // Everything a launch needs except the stream-K workspace.
@@ -2146,30 +2163,24 @@ int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_
     return launch_variant<32, 6, false, true, 1, false, true>(a, sm_count, stream);
   }
   if (a.opb) {
-    // B stored transposed: both tiles K-major in shared memory. Stages of
-    // 48 KiB (LSU exact: A, B and their lo tiles at BK = 16; tf32: A and B
-    // at 32) or 40 KiB (TMA exact: B^T hi and lo go to TMEM, as for B
-    // stored K x N).
+    // B stored transposed (N x K): its tile is K-major. The TMA-fed 3xTF32
+    // pair kernel moves it into TMEM as B^T hi and lo, as for B stored K x N;
+    // the LSU variants stage 48 KiB per stage (exact: A, B and their lo tiles
+    // at BK = 16; tf32: A and B at 32).
     if (exact) {
       if (lsu) return launch_variant<16, 4, true, true, 1, true>(a, sm_count, stream);
-      return launch_variant<16, 5, true, false, kClusterExact, true>(a, sm_count, stream);
+      return launch_variant<kPairExactBK, kPairExactStages, true, false, 2, true, false,
+                            kPairExactBSlots, true>(a, sm_count, stream);
     }
-    if (lsu) return launch_variant<32, 4, false, true, 1, true>(a, sm_count, stream);
-    return launch_variant<32, 4, false, false, kClusterTf32, true>(a, sm_count, stream);
+    return launch_variant<32, 4, false, true, 1, true>(a, sm_count, stream);
   }
-  // B stored K x N. Stage shapes picked by timing 4096^3 and 8192 x 11008 x
-  // 4096: exact BK = 16 x 5 stages of A 16 KiB + B 8 KiB + A_lo 16 KiB; tf32
-  // BK = 32 x 5 stages of A 32 KiB with B in a ring of its own (4 x 16 KiB,
-  // each slot free again once its B^T is in TMEM): 0.74 / 0.87 of the peak
-  // against 0.69 / 0.81 with B inside 4 stages. The exact variant, whose
-  // transform also splits A, loses with the separate ring.
+  // B stored K x N. (One TF32 pass fed by TMA went to pair_launch above.)
   if (exact) {
     if (lsu) return launch_variant<16, 6, true, true, 1, false>(a, sm_count, stream);
     return launch_variant<kPairExactBK, kPairExactStages, true, false, 2, false, false,
                           kPairExactBSlots, true>(a, sm_count, stream);
   }
-  if (lsu) return launch_variant<32, 6, false, true, 1, false>(a, sm_count, stream);
-  return launch_variant<32, 5, false, false, kClusterTf32, false, false, 4>(a, sm_count, stream);
+  return launch_variant<32, 6, false, true, 1, false>(a, sm_count, stream);
 }
 
 int tc_poll_status(cudaStream_t stream) {
