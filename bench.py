@@ -190,7 +190,7 @@ def kernel_label(g, kernel, mode):
     if kernel == g.KERNEL_TC_TMA:
         return "tc_pair_tma_3xtf32" if mode == "exact" else "tc_pair_tma_tf32"
     if kernel == g.KERNEL_TC_LSU:
-        return "tc_gemm_lsu_3xtf32" if mode == "exact" else "tc_gemm_lsu_tf32"
+        return "tc_lsu_3xtf32" if mode == "exact" else "tc_lsu_tf32"
     return str(kernel)
 
 

@@ -8,28 +8,30 @@
 //
 //     D = C_tile^T  (128 n x 256 m)  =  B_tile^T (128 n x K)  *  A_tile^T (K x 256 m),
 //
-// with B_tile^T as the MMA's A operand held in TMEM (lane = n, one 32-bit
-// column per k: the transpose happens on the way from shared memory through
-// registers into TMEM) and the A tile, staged K-major by TMA, as the MMA's B
-// operand in shared memory. The accumulator D lives in TMEM with lane = n and
+// with B_tile^T as the MMA's A operand (in TMEM, lane = n, one 32-bit column
+// per k, where threads write it; or an MN-major shared-memory tile, the
+// 32-byte-atom swizzle, in the one-pass pair kernel) and the A tile, staged
+// K-major, as the MMA's B operand in shared memory. The accumulator D lives in TMEM with lane = n and
 // column = m, so each epilogue store writes 32 consecutive columns of one row
 // of C (a coalesced 128-byte segment).
 //
-// Roles (warp-specialised, persistent, one CTA per SM, grouped raster):
-//   producer   TMA: one thread loads the 256 x BK A tile (swizzled, K-major)
-//              and the BK x 128 B tile per stage into a ring of stages
-//              (BK = 16 or 32 k per stage).
-//              LSU (operands TMA cannot describe): four warps load both with
-//              plain loads and place the A tile in shared memory and B^T in
-//              TMEM themselves.
-//   transform  (TMA variant) 8 (tf32) or 16 (3xTF32) warps move B^T into TMEM
-//              and, in 3xTF32 mode, split the A tile into hi (in place) and lo
-//              (sibling tile).
-//   MMA        one thread issues tcgen05.mma kind::tf32, M = 128, N = 256,
-//              K = 8. 3xTF32 issues B_lo*A_hi, B_hi*A_lo, B_hi*A_hi per k-step
-//              (small terms first), hi = tf32(x), lo = tf32(x - hi).
-//   epilogue   four warps read D from TMEM and store C with row/column
-//              guards.
+// Kernels (warp-specialised, persistent, one CTA per SM, grouped raster, the
+// same work list, epilogue and split-tile sum):
+//   tc_pair_kernel        one TF32 pass on CTA pairs (tcgen05 cta_group::2,
+//                         M = 256, N = 256): both operands by TMA, in every
+//                         layout, straight from shared memory to the MMA.
+//   tc_pair_exact_kernel  3xTF32 on CTA pairs: TMA copies; transform warps
+//                         write B^T hi/lo into TMEM and split A into hi (in
+//                         place) and lo (sibling tile); B_lo*A_hi,
+//                         B_hi*A_lo, B_hi*A_hi per k-step (small terms
+//                         first), hi = tf32(x), lo = tf32(x - hi).
+//   tc_lsu_kernel         either mode on one SM per tile (M = 128, N = 256),
+//                         for operands TMA cannot describe: four warps stage
+//                         both with plain loads (A into shared memory, B^T
+//                         into TMEM, split on the way for 3xTF32).
+// Roles: a producer (one TMA thread or four load warps), one MMA-issuing
+// thread, four epilogue warps that read D from TMEM and store C with
+// row/column guards, and in the 3xTF32 pair kernel eight transform warps.
 //
 // This is the tiled product of "Optimizing a WebGPU Matmul Kernel using
 // Subgroups" (sections 4-8: shared-memory tiles, register tiles, vector
@@ -120,78 +122,54 @@ __device__ __forceinline__ int split_slot(const TcParams &p, int s, int part) {
   return (c * p.sk_share >= s * p.num_k_blocks) ? 2 * c : 2 * c + 1;
 }
 
+// tc_lsu_kernel: operands staged by plain loads (any leading dimension, any
+// alignment, A in either storage), one SM per output tile 128 n x 256 m.
 // BK = K per stage: 32 (A rows of 128 bytes, 128-byte swizzle) or 16 (rows of
 // 64 bytes, 64-byte swizzle). Either way a row of the A tile is one swizzle
 // span, 8-row groups are the swizzle atom, and a k-step of 8 advances the
 // descriptor by 32 bytes along the row.
-// OPB = false: B is stored K x N (N contiguous); its tile goes through
-// registers into TMEM as B^T. OPB = true: B is stored transposed, N x K (K
-// contiguous), so its tile is K-major like A's. One TF32 pass (and the LSU
-// variants) feed it to the MMA from shared memory directly, and TMEM then
-// holds only accumulators, two of them. The TMA-fed 3xTF32 variant still
-// moves it into TMEM (hi and lo), as for B stored K x N: reading both hi/lo
-// operand pairs from shared memory would exceed the shared-memory bandwidth
-// that the split and the copies leave to the MMAs.
-// BST > 0 (TMA-fed, B stored K x N): the B tiles get a ring of their own, BST
-// slots, released as soon as the transform warps have moved B^T into TMEM
-// instead of when the MMAs are done with the stage; the A ring then holds
-// more stages in the same shared memory, which is what the pipeline needs
-// (it is bound by the round trip of a stage slot, not by bandwidth).
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, int BST = 0>
+// OPB = false: B is stored K x N (N contiguous); the producer warps write its
+// tile straight into TMEM as B^T (hi and lo for 3xTF32). OPB = true: B is
+// stored transposed, N x K (K contiguous), so its tile is staged K-major like
+// A's (with its lo tile for 3xTF32) and read by the MMA from shared memory;
+// TMEM then holds only accumulators, two of them.
+template <int BK, int STAGES, bool EXACT, bool OPB>
 struct TcConfig {
   static_assert(BK == 16 || BK == 32, "BK");
-  static_assert(CL == 1 || (CL == 2 && !LSU), "clusters pair TMA-fed CTAs only");
-  static_assert(BST == 0 || (!LSU && !OPB), "a separate B ring: TMA-fed, B stored K x N");
-  static constexpr bool kBtTmem = !OPB || (EXACT && !LSU);       // B^T operand in TMEM
-  static constexpr int kAPartRows = kTM / CL;                    // A rows each CTA loads
-  static constexpr int kAPartBytes = kAPartRows * BK * 4;
+  static constexpr bool kBtTmem = !OPB;                          // B^T operand in TMEM
   static constexpr int kRowBytes = BK * 4;                       // one K-major tile row
   static constexpr int kAtomBytes = 8 * kRowBytes;               // 8-row swizzle atom (SBO)
   static constexpr uint32_t kLayout = BK == 32 ? 2u : 4u;        // 128- or 64-byte swizzle
   static constexpr int kABytes = kTM * BK * 4;                   // A tile, K-major, swizzled
-  // B tile: row-major BK x 128 for TMA (OPB = false; LSU keeps none), or
-  // K-major 128 x BK like A (OPB = true).
-  static constexpr int kBBytes = (LSU && !OPB) ? 0 : BK * kTN * 4;
-  static constexpr int kBInStage = BST > 0 ? 0 : kBBytes;        // B tile bytes inside a stage
-  // 3xTF32 lo tiles follow the hi (or raw) tiles at kLoOffset, same layout.
-  static constexpr int kLoOffset = kABytes + kBInStage;
-  static constexpr int kLoBytes = EXACT ? (kBtTmem ? kABytes : kABytes + kBBytes) : 0;
-  static constexpr int kStageBytes = kABytes + kBInStage + kLoBytes;
-  static constexpr int kBOffset = kABytes;                       // (BST == 0)
+  static constexpr int kBBytes = OPB ? BK * kTN * 4 : 0;         // K-major B tile (OPB)
+  // 3xTF32 lo tiles follow the hi tiles at kLoOffset, same layout.
+  static constexpr int kLoOffset = kABytes + kBBytes;
+  static constexpr int kLoBytes = EXACT ? kABytes + kBBytes : 0;
+  static constexpr int kStageBytes = kABytes + kBBytes + kLoBytes;
+  static constexpr int kBOffset = kABytes;
   static constexpr int kALoOffset = kLoOffset;
   static constexpr int kBLoOffset = kLoOffset + kABytes;         // OPB && EXACT
-  static constexpr int kBRingOffset = STAGES * kStageBytes;      // B ring (BST > 0)
-  static constexpr int kTileBytes = STAGES * kStageBytes + BST * kBBytes;
+  static constexpr int kTileBytes = STAGES * kStageBytes;
   static constexpr uint32_t kBtColsPerStage = kBtTmem ? (EXACT ? 2 * BK : BK) : 0;  // hi (+ lo)
   static constexpr int kAccBufs = kBtTmem ? 1 : 2;               // TMEM accumulators
-  static constexpr int kProdWarps = LSU ? 4 : 1;
+  static constexpr int kProdWarps = 4;
   static constexpr int kMmaWarp = kProdWarps;
   static constexpr int kEpiWarp0 = kMmaWarp + 1;
-  // Transform warps, a multiple of 4 (whole TMEM lane quadrants). The 3xTF32
-  // split is the most work per stage: 16 warps keep it ahead of the MMAs.
-  // With B transposed and one TF32 pass there is nothing to transform.
-  static constexpr int kXformWarps = LSU ? 0 : (kBtTmem ? (EXACT ? 16 : 8) : 0);
-  static constexpr int kXformParts = kXformWarps > 0 ? kXformWarps / 4 : 1;  // per lane quadrant
-  static constexpr int kXformWarp0 = kEpiWarp0 + 4;
-  static constexpr int kThreads = 32 * (kXformWarp0 + kXformWarps);
+  static constexpr int kThreads = 32 * (kEpiWarp0 + 4);
   static constexpr uint32_t kIdesc = idesc_tf32(kTN, kTM);
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
-  static_assert(kXformWarps % 4 == 0 && BK % kXformParts == 0, "transform partition");
   static_assert(kBtTmem ? kBtCol + STAGES * kBtColsPerStage <= kTmemCols
                         : kAccBufs * kTM <= static_cast<int>(kTmemCols),
                 "TMEM budget");
 };
 
-template <int STAGES, int BST = 0>
+template <int STAGES>
 struct alignas(8) TcShared {
   uint64_t full[STAGES];   // stage loaded (TMA bytes, or the LSU producer warps)
-  uint64_t ready[STAGES];  // B^T in TMEM (and A split) by the transform warps
   uint64_t empty[STAGES];  // stage consumed by the MMAs (tcgen05.commit)
-  uint64_t bfull[BST > 0 ? BST : 1];   // B ring slot loaded (TMA bytes)
-  uint64_t bempty[BST > 0 ? BST : 1];  // B ring slot read by the transform warps
   uint64_t acc_full[2];    // accumulator complete (tcgen05.commit)
   uint64_t acc_empty[2];   // accumulator drained by the epilogue warps
-  uint64_t drain;          // every MMA of this CTA has completed
+  uint64_t drain;          // every MMA of this CTA (pair) has completed
   uint32_t tmem_base;
   int abort;
   int sk_last;             // epilogue: this CTA finished a split tile last
@@ -607,31 +585,27 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
   }
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST>
-__global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>::kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                   const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
-  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>;
-  static_assert(!OPA || LSU, "A stored transposed is staged by the LSU producer");
+// The tensor maps are unused: the parameter list is that of the TMA-fed
+// kernels, so one launch path serves all of them.
+template <int BK, int STAGES, bool EXACT, bool OPB, bool OPA>
+__global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, OPB>::kThreads, 1)
+    tc_lsu_kernel(const __grid_constant__ CUtensorMap, const __grid_constant__ CUtensorMap,
+                  const TcParams p) {
+  using Cfg = TcConfig<BK, STAGES, EXACT, OPB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *tiles = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  TcShared<STAGES, BST> *sh = reinterpret_cast<TcShared<STAGES, BST> *>(tiles + Cfg::kTileBytes);
+  TcShared<STAGES> *sh = reinterpret_cast<TcShared<STAGES> *>(tiles + Cfg::kTileBytes);
   volatile int *abort = &sh->abort;
 
   const uint32_t warp = warp_index();
   const uint32_t lane = threadIdx.x & 31;
-  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0;
+  const uint32_t rank = 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sh->full[s], LSU ? Cfg::kProdWarps : 1);
-      mbar_init(&sh->ready[s], Cfg::kXformWarps > 0 ? Cfg::kXformWarps : 1);
-      mbar_init(&sh->empty[s], CL);  // the MMAs of every CTA that writes this stage
-    }
-    for (int b = 0; b < BST; ++b) {
-      mbar_init(&sh->bfull[b], 1);
-      mbar_init(&sh->bempty[b], Cfg::kXformWarps);
+      mbar_init(&sh->full[s], Cfg::kProdWarps);
+      mbar_init(&sh->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh->acc_full[a], 1);
@@ -642,91 +616,17 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
     sh->fix_tile = -1;
     fence_barrier_init();
   }
-  if (!LSU && warp == 0 && lane == 0) {
-    tma_prefetch_map(&tmap_a);
-    tma_prefetch_map(&tmap_b);
-  }
   if (warp == Cfg::kMmaWarp) {
     tmem_alloc(&sh->tmem_base, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before_sync();
   __syncthreads();
-  // The peer's multicast copies and commits target this CTA's barriers: they
-  // must be initialised cluster-wide before either CTA issues one.
-  if (CL > 1) cluster_sync();
   tc_fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
 
-  if (!LSU && warp == 0) {
-    // ------------------------------------------------------ TMA producer --
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
-      uint32_t bstage = 0, bphase = 0, barmed = 0, barmed_parity = 0;
-      bool ok = true;
-      UnitIter it(p);
-      WorkUnit u;
-      while (ok && it.next(p, u)) {
-        int mb, nb;
-        tile_coords(p, u.tile, rank, mb, nb);
-        for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          if (!mbar_wait_bounded(&sh->empty[stage], phase ^ 1, p.timeout_ns, abort,
-                                 &g_tc_status)) {
-            ok = false;
-            break;
-          }
-          uint8_t *st = tiles + stage * Cfg::kStageBytes;
-          // The whole A tile arrives (each CTA of the cluster multicasts its
-          // rows to all of them) plus this CTA's own B tile, unless B has a
-          // ring of its own.
-          mbar_arrive_expect_tx(&sh->full[stage], Cfg::kABytes + Cfg::kBInStage);
-          if (CL > 1)
-            tma_load_2d_multicast(st + rank * Cfg::kAPartBytes, &tmap_a, &sh->full[stage], kb * BK,
-                                  mb * kTM + static_cast<int>(rank) * Cfg::kAPartRows,
-                                  static_cast<uint16_t>((1u << CL) - 1));
-          else
-            tma_load_2d(st, &tmap_a, &sh->full[stage], kb * BK, mb * kTM);
-          if (BST > 0) {
-            if (!mbar_wait_bounded(&sh->bempty[bstage], bphase ^ 1, p.timeout_ns, abort,
-                                   &g_tc_status)) {
-              ok = false;
-              armed |= 1u << stage;  // the A copy above is in flight
-              armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-              break;
-            }
-            mbar_arrive_expect_tx(&sh->bfull[bstage], Cfg::kBBytes);
-            tma_load_2d(tiles + Cfg::kBRingOffset + bstage * Cfg::kBBytes, &tmap_b,
-                        &sh->bfull[bstage], nb * kTN, kb * BK);
-            barmed |= 1u << bstage;
-            barmed_parity = (barmed_parity & ~(1u << bstage)) | (bphase << bstage);
-            if (++bstage == static_cast<uint32_t>(BST > 0 ? BST : 1)) {
-              bstage = 0;
-              bphase ^= 1;
-            }
-          } else if (OPB) {
-            tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], kb * BK, nb * kTN);
-          } else {
-            tma_load_2d(st + Cfg::kBOffset, &tmap_b, &sh->full[stage], nb * kTN, kb * BK);
-          }
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
-      if (!ok) {
-        // Let every TMA copy this thread issued land before the CTA exits.
-        for (int s = 0; s < STAGES; ++s)
-          if (armed & (1u << s)) drain_wait(&sh->full[s], (armed_parity >> s) & 1u, p.timeout_ns);
-        for (int b = 0; b < BST; ++b)
-          if (barmed & (1u << b))
-            drain_wait(&sh->bfull[b], (barmed_parity >> b) & 1u, p.timeout_ns);
-      }
-    }
-  } else if (LSU && warp < Cfg::kProdWarps) {
-    // ------------------------------------------------------ LSU producer --
+  if (warp < Cfg::kProdWarps) {
+    // ---------------------------------------------------------- producer --
     // Warp w stages A rows w, w + 4, ... (lane = k) and B^T rows
     // n = 32 w + lane (TMEM lanes of this warp's quadrant).
     uint32_t stage = 0, phase = 0;
@@ -795,15 +695,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem + kAccCol + acc * kTM;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
-          uint64_t *in_bar = Cfg::kXformWarps > 0 ? &sh->ready[stage] : &sh->full[stage];
-          if (!mbar_wait_bounded(in_bar, phase, p.timeout_ns, abort, &g_tc_status)) {
-            ok = false;
-            break;
-          }
-          // With a separate B ring the one-pass transform does not wait for
-          // the A tile; the MMA does.
-          if (BST > 0 && !EXACT &&
-              !mbar_wait_bounded(&sh->full[stage], phase, p.timeout_ns, abort, &g_tc_status)) {
+          if (!mbar_wait_bounded(&sh->full[stage], phase, p.timeout_ns, abort, &g_tc_status)) {
             ok = false;
             break;
           }
@@ -816,7 +708,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
             // 8-row groups (the swizzle atom) are kAtomBytes apart.
             const uint64_t da = smem_desc(a_hi + kk * 32, 16, Cfg::kAtomBytes, Cfg::kLayout);
             const uint32_t accumulate = (kb != u.kb0 || kk != 0) ? 1u : 0u;
-            if (!Cfg::kBtTmem) {
+            if constexpr (OPB) {
               // B^T rows straight from the K-major B tile in shared memory.
               const uint64_t db = smem_desc(a_hi + Cfg::kBOffset + kk * 32, 16, Cfg::kAtomBytes,
                                             Cfg::kLayout);
@@ -841,10 +733,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
               mma_tf32_ts(d_tmem, bt_hi + kk * kUmmaK, da, Cfg::kIdesc, accumulate);
             }
           }
-          if (CL > 1)
-            mma_commit_multicast(&sh->empty[stage], static_cast<uint16_t>((1u << CL) - 1));
-          else
-            mma_commit(&sh->empty[stage]);
+          mma_commit(&sh->empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -862,116 +751,9 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
       drain_wait(&sh->drain, 0, p.timeout_ns);
     }
     __syncwarp();
-  } else if (warp >= Cfg::kEpiWarp0 && warp < Cfg::kEpiWarp0 + 4) {
+  } else {
     // --------------------------------------------------------- epilogue --
     epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, false>(p, sh, tmem, warp, lane, rank, abort);
-  } else if (Cfg::kXformWarps > 0 && warp >= Cfg::kXformWarp0) {
-    // -------------------------------------------- transform (TMA variant) --
-    // Warp (quad, part) moves k in [part * W, (part + 1) * W), W = BK / parts,
-    // of B^T rows n = 32 quad + lane into TMEM; all of them split the A tile.
-    const uint32_t quad = warp & 3;
-    const uint32_t part = (warp - Cfg::kXformWarp0) >> 2;
-    const int xt = threadIdx.x - Cfg::kXformWarp0 * 32;  // 0 .. 32 * kXformWarps - 1
-    uint32_t stage = 0, phase = 0, bstage = 0, bphase = 0;
-    bool ok = true;
-    UnitIter it(p);
-    WorkUnit u;
-    while (ok && it.next(p, u)) {
-      for (int kb = u.kb0; kb < u.kb1; ++kb) {
-        if (BST > 0) {
-          // The B slot has landed and TMEM slot `stage` is free again (the
-          // MMAs of its previous round have completed: the stage's empty
-          // phase); 3xTF32 also splits the A tile, so it waits for it too.
-          if (!warp_wait(&sh->bfull[bstage], bphase, p, abort) ||
-              !warp_wait(&sh->empty[stage], phase ^ 1, p, abort) ||
-              (EXACT && !warp_wait(&sh->full[stage], phase, p, abort))) {
-            ok = false;
-            break;
-          }
-        } else if (!warp_wait(&sh->full[stage], phase, p, abort)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        uint8_t *st = tiles + stage * Cfg::kStageBytes;
-        if constexpr (!OPB) {
-          // B tile is row-major BK k x 128 n (512-byte rows); this thread's
-          // column n = 32 quad + lane becomes TMEM lane n.
-          constexpr int kW = BK / Cfg::kXformParts;
-          const uint8_t *bslot =
-              BST > 0 ? tiles + Cfg::kBRingOffset + bstage * Cfg::kBBytes : st + Cfg::kBOffset;
-          const float *bs =
-              reinterpret_cast<const float *>(bslot) + part * kW * kTN + quad * 32 + lane;
-          float v[kW];
-#pragma unroll
-          for (int k = 0; k < kW; ++k) v[k] = bs[k * kTN];
-          const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol +
-                               stage * Cfg::kBtColsPerStage + part * kW;
-          bt_to_tmem<kW, EXACT>(col, col + BK, v);
-          if (BST > 0) {
-            // The values are in registers: the B slot can be refilled.
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh->bempty[bstage]);
-            if (++bstage == static_cast<uint32_t>(BST > 0 ? BST : 1)) {
-              bstage = 0;
-              bphase ^= 1;
-            }
-          }
-        } else if constexpr (Cfg::kBtTmem) {
-          // B tile is K-major 128 n x BK k (swizzled rows of BK * 4 bytes):
-          // row n = 32 quad + lane holds this thread's TMEM lane, and part
-          // `part` reads its kW consecutive k as 16-byte chunks.
-          constexpr int kW = BK / Cfg::kXformParts;
-          static_assert(kW % 4 == 0, "whole 16-byte chunks per part");
-          const int n = quad * 32 + lane;
-          float v[kW];
-#pragma unroll
-          for (int c = 0; c < kW / 4; ++c) {
-            const float4 x = *reinterpret_cast<const float4 *>(
-                st + Cfg::kBOffset + swizzle_a<BK>(n * Cfg::kRowBytes + (part * kW + c * 4) * 4));
-            v[c * 4 + 0] = x.x;
-            v[c * 4 + 1] = x.y;
-            v[c * 4 + 2] = x.z;
-            v[c * 4 + 3] = x.w;
-          }
-          const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol +
-                               stage * Cfg::kBtColsPerStage + part * kW;
-          bt_to_tmem<kW, EXACT>(col, col + BK, v);
-        }
-        if (EXACT) {
-          // Split the K-major tiles held in shared memory as MMA operands (A,
-          // and B when it is not moved into TMEM): hi in place, lo kLoOffset
-          // bytes further.
-          constexpr int kSplitVecs = (Cfg::kBtTmem ? Cfg::kABytes : Cfg::kABytes + Cfg::kBBytes) / 16;
-          float4 *raw = reinterpret_cast<float4 *>(st);
-          float4 *lo = reinterpret_cast<float4 *>(st + Cfg::kLoOffset);
-#pragma unroll 4
-          for (int i = xt; i < kSplitVecs; i += 32 * Cfg::kXformWarps) {
-            const float4 x = raw[i];
-            float4 h, l;
-            h.x = round_tf32(x.x);
-            h.y = round_tf32(x.y);
-            h.z = round_tf32(x.z);
-            h.w = round_tf32(x.w);
-            l.x = round_tf32(x.x - h.x);
-            l.y = round_tf32(x.y - h.y);
-            l.z = round_tf32(x.z - h.z);
-            l.w = round_tf32(x.w - h.w);
-            raw[i] = h;
-            lo[i] = l;
-          }
-          fence_proxy_async_smem();
-        }
-        tmem_store_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->ready[stage]);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-      }
-    }
   }
 
   tc_fence_before_sync();
@@ -985,8 +767,6 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
     epilogue_fixup(p, sh->fix_tile, rank, sh->fix_nparts, sh->fix_mb, sh->fix_nb, threadIdx.x,
                    blockDim.x);
   }
-  // No CTA of a cluster leaves while its peer may still signal its barriers.
-  if (CL > 1) cluster_sync();
 }
 
 // ------------------------------------------------------ CTA-pair kernel --
@@ -996,9 +776,9 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>
 // C^T, with one MMA stream issued by the even CTA: M = 256 (the MMA's A
 // operand is B_tile^T, CTA r holding n rows 128 r .. 128 r + 127), N = 256
 // (the MMA's B operand is the A tile, CTA r holding m rows 128 r ..) and
-// K = 8. Each CTA's TMEM accumulates its own 128 n x 256 m, which is the
-// output tile the multicast pairs of tc_gemm_kernel give that CTA, so the
-// schedule, epilogue and split-tile sums are shared with it.
+// K = 8. Each CTA's TMEM accumulates its own 128 n x 256 m, the same output
+// tile tc_lsu_kernel gives one SM, so the schedule, epilogue and split-tile
+// sums are shared with it.
 //
 // Both operands go from global memory to the tensor core by TMA alone: a
 // K-major operand (A stored M x K, B stored N x K) as a box of BK k x 128
@@ -1217,10 +997,11 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
 // 128 r ..), N = 256 (the A tile, CTA r holding m rows 128 r ..), K = 8.
 //
 // Shared-memory traffic decides the design. With one SM per 128 n x 256 m
-// output tile (tc_gemm_kernel) every MMA reads 256 rows of its B operand and
-// every SM splits a 256-row A tile, about 1.3 times the bytes per cycle
-// shared memory can serve at full tensor rate; with the pair each SM reads
-// and splits only its own 128 rows, for the same MMA work per SM.
+// output tile (an earlier TMA-fed design, 0.466 ms at 4096^3 against 0.398)
+// every MMA reads 256 rows of its B operand and every SM splits a 256-row A
+// tile, about 1.3 times the bytes per cycle shared memory can serve at full
+// tensor rate; with the pair each SM reads and splits only its own 128 rows,
+// for the same MMA work per SM.
 //
 // Per k-block of BK each CTA loads, by TMA on its own barriers, its 128 A
 // rows x BK k (K-major, swizzled) into a ring of A stages and its B tile
@@ -1766,15 +1547,16 @@ Schedule make_schedule(int tiles, int kb, int sms, int min_chunk, bool full_wave
   return s;
 }
 
-// The kernel a launch plan runs: tc_gemm_kernel, or with PAIR the CTA-pair
-// TF32 kernel (which takes every operand layout by TMA directly).
+// The kernel a launch plan runs: tc_lsu_kernel, or with PAIR a CTA-pair
+// kernel.
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST, bool PAIR>
 struct KernelOf {
-  using Cfg = TcConfig<BK, STAGES, EXACT, LSU, CL, OPB, BST>;
+  static_assert(LSU && CL == 1 && BST == 0, "tc_lsu_kernel: plain-load producers, one SM per tile");
+  using Cfg = TcConfig<BK, STAGES, EXACT, OPB>;
   static constexpr int kThreads = Cfg::kThreads;
   static constexpr int kSmemBytes =
-      Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES, BST>)) + 1024;
-  static constexpr auto kernel = tc_gemm_kernel<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST>;
+      Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
+  static constexpr auto kernel = tc_lsu_kernel<BK, STAGES, EXACT, OPB, OPA>;
 };
 
 template <int BK, int STAGES, bool OPA, bool OPB>
@@ -1859,8 +1641,7 @@ struct LaunchPlan {
     } else if constexpr (!LSU) {
       const CUtensorMapSwizzle sw_a =
           BK == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-      // Each CTA of a cluster loads kTM / CL rows of the A tile (the 3xTF32
-      // pair kernel: its own half; tc_gemm_kernel: its half of the multicast).
+      // Each CTA of the 3xTF32 pair loads its own half of the A tile.
       if (!get_map(a.A, a.K, a.M, a.lda * 4, BK, kTM / CL, sw_a, &map_a)) return kErrLaunch;
       if (OPB) {
         // B stored N x K: a K-major BK x 128 box with A's swizzle.
@@ -1914,11 +1695,11 @@ struct LaunchPlan {
       }
       workers = workers_cached[dev];
     }
-    // Full waves for the pair kernels, balanced for tc_gemm_kernel (timed at
+    // Full waves for the pair kernels, balanced for tc_lsu_kernel (timed at
     // 4096^3, 5120^3, 2560 x 2560 x 4096 and 8192 x 11008 x 4096: +5-6 % for
     // the TF32 pair kernel, which is bound by operand traffic from L2, +3 % at
     // 4096^3 for the 3xTF32 pair kernel, whose split tiles then have fewer
-    // parts to sum, and -3 % for tc_gemm_kernel's 3xTF32).
+    // parts to sum, and -3 % for an earlier one-SM 3xTF32 kernel).
     sch = make_schedule(p.num_tiles, p.num_k_blocks, workers,
                         (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK, PAIR);
     p.dp_tiles = sch.dp_tiles;
