@@ -296,36 +296,36 @@ def test_bounded_wait_times_out_cleanly(g):
 
 # ---------------------------------------------------------- full sizes --
 
-def _sample_rows(m, count, seed):
-    rng = np.random.default_rng(seed)
-    rows = set(rng.choice(m, size=min(count, m), replace=False).tolist())
-    rows |= {0, m - 1, 127, 128, min(m - 1, 1000)}
-    return np.array(sorted(r for r in rows if r < m), dtype=np.int64)
+# Oracle product of the current workload, computed once and shared by its
+# modes, which run one after another (8192 x 11008 x 4096 takes about 25 s on
+# 16 host cores and 1.4 GB for C64 and S).
+_ORACLE_CACHE = {}
 
 
-@pytest.mark.parametrize("cfg", ["c1", "c2", "c3", "c5a"])
+def _oracle_product(cfg, a, b):
+    if cfg not in _ORACLE_CACHE:
+        _ORACLE_CACHE.clear()
+        _ORACLE_CACHE[cfg] = oracle.gemm(a, b)
+    return _ORACLE_CACHE[cfg]
+
+
 @pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("cfg", ["c1", "c2", "c3", "c5a"])
 def test_config_full_comparison(g, cfg, mode):
     a, b, c = config_operands(cfg)
     out, _ = run(g, a, b, mode)
-    if cfg == "c3":
-        rows = _sample_rows(c["M"], 512, 3)
-        c64, s = oracle.gemm_rows(a, b, rows)
-        check_within_bound(out[rows], c64, s, c["K"], mode, f"{cfg} {mode}")
-    else:
-        c64, s = oracle.gemm(a, b)
-        check_within_bound(out, c64, s, c["K"], mode, f"{cfg} {mode}")
+    c64, s = _oracle_product(cfg, a, b)
+    check_within_bound(out, c64, s, c["K"], mode, f"{cfg} {mode}")
 
 
-@pytest.mark.parametrize("cfg", ["c4", "c5b"])
 @pytest.mark.parametrize("mode", ["exact", "tf32"])
-def test_config_full_size_sampled_rows(g, cfg, mode):
+@pytest.mark.parametrize("cfg", ["c4", "c5b"])
+def test_config_full_size(g, cfg, mode):
     # full-size workload in the benchmark's launch configuration (dense leading
-    # dimensions, default kernel choice, torch's current stream); the oracle
-    # computes a sample of whole rows, including first and last
+    # dimensions, default kernel choice, torch's current stream), every element
+    # against the fp64 oracle
     a, b, c = config_operands(cfg)
     out, _ = run(g, a, b, mode)
     assert np.isfinite(out).all()
-    rows = _sample_rows(c["M"], 96, 4)
-    c64, s = oracle.gemm_rows(a, b, rows)
-    check_within_bound(out[rows], c64, s, c["K"], mode, f"{cfg} {mode}")
+    c64, s = _oracle_product(cfg, a, b)
+    check_within_bound(out, c64, s, c["K"], mode, f"{cfg} {mode}")

@@ -201,20 +201,36 @@ def test_general_matches_plain_entry_point_bitwise(g):
         assert np.array_equal(plain.cpu().numpy(), gen), mode
 
 
+# The product A B of the 4096^3 operands, computed once by the oracle: every
+# storage of A and B below holds the same two matrices.
+_FULL = {}
+
+
+def _full_product(a, b):
+    if "ab" not in _FULL:
+        _FULL["ab"] = oracle.gemm(a, b)
+    return _FULL["ab"]
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("mode", ["exact", "tf32"])
 @pytest.mark.parametrize("transa,transb", LAYOUTS)
-def test_general_full_size_sampled_rows(g, mode, transa, transb):
+def test_general_full_size(g, mode, transa, transb):
     # 4096^3 in the launch configuration of the benchmark (TMA-fed kernel when
-    # the layout allows it), checked on sampled rows the oracle computes one
-    # by one
+    # the layout allows it): every element against alpha * (A B) + beta * C0
+    # from the oracle's product, and sampled rows against the oracle's general
+    # form applied to the operands as stored
     m = n = k = 4096
     a = synth.uniform_pm1((m, k), 1008)
     b = synth.uniform_pm1((k, n), 1009)
     c0 = synth.uniform_pm1((m, n), 1010)
     alpha, beta = 1.25, -0.5
     c = run_general(g, a, b, transa, transb, alpha, beta, c0, mode, "auto")
+    c64, s = _full_product(a, b)
+    full64 = alpha * c64 + beta * c0.astype(np.float64)
+    check_within_bound(c, full64, abs(alpha) * s, k, mode, f"4096^3 T{transa}{transb} full",
+                       extra=general_slack(s, alpha, beta, c0))
     rows = np.array([0, 1, 255, 256, 2047, 3000, 4095])
-    out64, s = expect(a, b, transa, transb, alpha, beta, c0, rows=rows)
-    check_within_bound(c[rows], out64, abs(alpha) * s, k, mode, f"4096^3 T{transa}{transb}",
-                       extra=general_slack(s, alpha, beta, c0[rows]))
+    out64, s_rows = expect(a, b, transa, transb, alpha, beta, c0, rows=rows)
+    check_within_bound(c[rows], out64, abs(alpha) * s_rows, k, mode, f"4096^3 T{transa}{transb}",
+                       extra=general_slack(s_rows, alpha, beta, c0[rows]))
