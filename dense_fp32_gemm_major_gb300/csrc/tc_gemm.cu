@@ -1022,6 +1022,12 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
 // ahead of the TMEM slots: a slot's round trip (the MMAs that read it, the
 // transform of the next k-block, the hand-over) does not include a copy's
 // latency.
+// float4 loads per thread and part in flight in the 3xTF32 pair kernel's final
+// split-tile sum (timed: 4 beats 16 by 1.5-2 us at 512^3-2048^3; the sum of a
+// 128 KiB tile from parts just written by other SMs takes 5-10 us whatever
+// the batch, bound by the latency of those loads).
+constexpr int kPairExactFixBatch = 4;
+
 template <int BK, int AST, int BST, int XW, bool OPB>
 struct PairExactConfig {
   static_assert(BK == 16 || BK == 32, "BK");
@@ -1367,9 +1373,8 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
   }
   if (sh->fix_tile >= 0 && !sh->abort) {
     __threadfence();
-    epilogue_fixup<(Cfg::kThreads > 512 ? 8 : 16)>(p, sh->fix_tile, rank, sh->fix_nparts,
-                                                   sh->fix_mb, sh->fix_nb, threadIdx.x,
-                                                   blockDim.x);
+    epilogue_fixup<kPairExactFixBatch>(p, sh->fix_tile, rank, sh->fix_nparts, sh->fix_mb,
+                                       sh->fix_nb, threadIdx.x, blockDim.x);
   }
 }
 
