@@ -1497,6 +1497,12 @@ bool get_map(const void *ptr, uint64_t d0, uint64_t d1, uint64_t pitch_bytes, ui
 // and 256 k in exact mode).
 constexpr int kMinChunkKExact = 256;
 constexpr int kMinChunkKTf32 = 2048;
+// What splitting the last wave's tiles costs the 3xTF32 pair kernel, in k of
+// MMA work: writing the partial tiles and the final sums (timed with 0, 448,
+// 768 and 1024: at 768, 2048^3 runs its 64 tiles whole on 64 pairs, 74 -> 67
+// us, 1000 x 1531 x 777 46 -> 44 us, 512^3 28.5 -> 27 us; 4096^3 and 8192 x
+// 11008 x 4096 keep their split last wave; 1024 made 1024^3 slower).
+constexpr int kSplitCostKExact = 768;
 // Most CTAs sharing one split tile: the last of them sums every part alone.
 constexpr int kMaxSplit = 8;
 
@@ -1519,11 +1525,20 @@ struct Schedule {
 //    running gets a larger share of it) but not for one bound by its MMAs.
 // With fewer tiles than workers everything is stream-K, with chunks of at
 // least min_chunk k-blocks and at most kMaxSplit parts per tile.
-Schedule make_schedule(int tiles, int kb, int sms, int min_chunk, bool full_waves) {
+Schedule make_schedule(int tiles, int kb, int sms, int min_chunk, bool full_waves,
+                       int split_cost = 0) {
   Schedule s;
   min_chunk = min_chunk < 1 ? 1 : min_chunk;
   s.dp_tiles = (tiles >= sms && tiles % sms != 0) ? (tiles / sms - (full_waves ? 0 : 1)) * sms
                : (tiles >= sms ? tiles : 0);
+  // Full waves: the last R = tiles - dp_tiles tiles are dealt whole as well
+  // when splitting them would save less than it costs: (1 - R / G) of a
+  // tile's kb k-blocks against split_cost k-blocks for writing and summing
+  // partial tiles.
+  if (full_waves && tiles > s.dp_tiles &&
+      static_cast<long long>(kb) * (sms - (tiles - s.dp_tiles)) <
+          static_cast<long long>(split_cost) * sms)
+    s.dp_tiles = tiles;
   const int split = tiles - s.dp_tiles;
   if (split == 0) {
     s.grid = sms < tiles ? sms : tiles;
@@ -1706,7 +1721,8 @@ struct LaunchPlan {
     // 4096^3 for the 3xTF32 pair kernel, whose split tiles then have fewer
     // parts to sum, and -3 % for an earlier one-SM 3xTF32 kernel).
     sch = make_schedule(p.num_tiles, p.num_k_blocks, workers,
-                        (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK, PAIR);
+                        (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK, PAIR,
+                        PAIR && EXACT ? kSplitCostKExact / BK : 0);
     p.dp_tiles = sch.dp_tiles;
     p.sk_share = sch.sk_share;
     p.sk_ctas = sch.sk_ctas;
