@@ -176,9 +176,12 @@ def test_ragged_sweep(g):
 @pytest.mark.parametrize("m,n,k", [
     (256, 128, 4096),     # one tile, k split over the most CTAs
     (200, 100, 2000),     # one ragged tile, split
-    (3328, 1536, 512),    # 156 tiles: one full wave plus 4 split tiles
-    (3328, 1536, 4096),   # one TF32 pass: a full wave of pair tiles whole, 2 tiles split
-    (512, 512, 512),      # 8 tiles, each split (3xTF32; one TF32 pass splits from 1024 k)
+    (3328, 1536, 512),    # 78 pair tiles: a full wave, the last 2 dealt whole (3xTF32: too
+                          # short to split)
+    (3328, 1536, 1024),   # 78 pair tiles: a full wave whole, 2 tiles split (3xTF32)
+    (3328, 1536, 4096),   # a full wave of pair tiles whole, 2 tiles split
+    (512, 512, 512),      # 4 pair tiles, whole (3xTF32: too short to split)
+    (512, 512, 1024),     # 4 pair tiles, each split (3xTF32)
     (200, 100, 8000),     # one ragged tile, split in both modes
     (512, 512, 4096),     # 8 tiles, each split in both modes
 ])
