@@ -276,6 +276,29 @@ def test_host_entry_point_row_chunks(g):
         assert np.all(wc[:, n:] == -3.0), "write outside C's columns"
 
 
+def test_host_entry_point_long_k(g):
+    # the host entry with K past 2048 (row chunks of 1024+ rows, ragged K):
+    # within the bound on random data, bitwise on integers with strided host
+    # rows
+    for (m, n, k), mode in [((2100, 300, 2500), "exact"), ((2100, 300, 2500), "tf32"),
+                            ((1100, 260, 2053), "exact_simt")]:
+        a, b = operands(m, n, k, "normal", seed=m + n + k)
+        c = g.matmul_host(a, b, mode)
+        c64, s = oracle.gemm(a, b)
+        check_within_bound(c, c64, s, k, mode, f"host long k {mode} {m}x{n}x{k}")
+    m, n, k = 1100, 129, 2053
+    wa = np.full((m, k + 5), np.nan, np.float32)
+    wb = np.full((k, n + 3), np.nan, np.float32)
+    wc = np.full((m, n + 2), -7.0, np.float32)
+    wa[:, :k] = synth.small_integers((m, k), 93)
+    wb[:, :n] = synth.small_integers((k, n), 94)
+    expect64 = oracle.gemm(wa[:, :k], wb[:, :n])[0]
+    for mode in ("exact", "tf32", "exact_simt"):
+        g.matmul_host(wa[:, :k], wb[:, :n], mode, out=wc[:, :n])
+        assert np.array_equal(wc[:, :n].astype(np.float64), expect64), mode
+        assert np.all(wc[:, n:] == -7.0), "write outside C's columns"
+
+
 def test_probe_peaks_are_plausible(g):
     # MMA-only and FFMA-only probe kernels: rates between half and twice the
     # nominal GB300 figures (1.1 PFLOP/s dense TF32; 152 SMs x 128 lanes x 2
