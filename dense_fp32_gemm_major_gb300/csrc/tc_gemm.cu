@@ -501,36 +501,40 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
     const bool n_ok = gn < p.N;
     const uint32_t t_lane = tmem + ((quad * 32) << 16) + kAccCol + acc * kTM;
     if (u.nparts == 1) {
-      // Whole tile: straight to C.
-#pragma unroll 1
-      for (int c = 0; c < kTM / 32; ++c) {
+      // Whole tile: straight to C, two 32-column chunks per TMEM load wait.
+      auto store_chunk = [&](int c, const uint32_t (&r)[32]) {
         const int gm0 = mb * kTM + c * 32;
-        if (gm0 >= p.M) break;
-        uint32_t r[32];
-        tmem_load_32cols(t_lane + c * 32, r);
-        tmem_load_wait();
+        if (gm0 >= p.M || !n_ok) return;
         float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
         const int rows = min(32, p.M - gm0);
-        if (n_ok) {
-          if (p.alpha == 1.0f && p.beta == 0.0f) {
-            if (rows == 32) {
+        if (p.alpha == 1.0f && p.beta == 0.0f) {
+          if (rows == 32) {
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < rows) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
-            }
+            for (int j = 0; j < 32; ++j)
+              dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (j < rows) {
-                float *d = dst + static_cast<long long>(j) * p.ldc;
-                *d = scale_out(p, __uint_as_float(r[j]), d);
-              }
+              if (j < rows) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
           }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < rows) {
+              float *d = dst + static_cast<long long>(j) * p.ldc;
+              *d = scale_out(p, __uint_as_float(r[j]), d);
+            }
         }
+      };
+#pragma unroll 1
+      for (int c = 0; c < kTM / 32; c += 2) {
+        if (mb * kTM + c * 32 >= p.M) break;
+        uint32_t r0[32], r1[32];
+        tmem_load_32cols(t_lane + c * 32, r0);
+        tmem_load_32cols(t_lane + (c + 1) * 32, r1);
+        tmem_load_wait();
+        store_chunk(c, r0);
+        store_chunk(c + 1, r1);
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -544,13 +548,16 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
       float *slot =
           p.sk_partials + (static_cast<long long>(u.slot) * p.cl + rank) * slot_elems;
 #pragma unroll 1
-      for (int c = 0; c < kTM / 32; ++c) {
-        uint32_t r[32];
-        tmem_load_32cols(t_lane + c * 32, r);
+      for (int c = 0; c < kTM / 32; c += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_load_32cols(t_lane + c * 32, r0);
+        tmem_load_32cols(t_lane + (c + 1) * 32, r1);
         tmem_load_wait();
         float *dst = slot + (c * 32) * kTN + n_loc;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) dst[j * kTN] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j) dst[j * kTN] = __uint_as_float(r0[j]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[(32 + j) * kTN] = __uint_as_float(r1[j]);
       }
       tc_fence_before_sync();
       __syncwarp();
