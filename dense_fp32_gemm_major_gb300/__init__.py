@@ -85,6 +85,8 @@ def _load():
     lib.gemm_f32_poll_device_status.restype = i32
     lib.gemm_f32_selftest_wait_timeout.argtypes = [i64, p]
     lib.gemm_f32_selftest_wait_timeout.restype = i32
+    lib.gemm_f32_schedule_check.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int64)]
+    lib.gemm_f32_schedule_check.restype = i32
     _lib = lib
     return lib
 
@@ -166,6 +168,19 @@ def gemm_f32_poll_device_status(stream=0) -> int:
 
 def gemm_f32_selftest_wait_timeout(timeout_ns: int, stream=0) -> int:
     return _load().gemm_f32_selftest_wait_timeout(timeout_ns, stream or None)
+
+
+SCHEDULE_KINDS = {"exact_pair": 0, "tf32_pair": 1, "exact_lsu": 2, "tf32_lsu": 3}
+SCHEDULE_STATS = ("tiles", "k_blocks", "whole_tiles", "sk_share", "sk_clusters", "splits",
+                  "max_parts", "clusters")
+
+
+def gemm_f32_schedule_check(m: int, n: int, k: int, workers: int, kind):
+    """Host-only check of the tile schedule (no GPU): (status, stats dict)."""
+    stats = (ctypes.c_int64 * 8)()
+    kind = SCHEDULE_KINDS[kind] if isinstance(kind, str) else int(kind)
+    st = _load().gemm_f32_schedule_check(m, n, k, workers, kind, stats)
+    return st, dict(zip(SCHEDULE_STATS, list(stats)))
 
 
 # ---------------------------------------------------------- conveniences --

@@ -54,6 +54,7 @@
 #include <cstring>
 #include <mutex>
 #include <type_traits>
+#include <vector>
 
 #include "../../include/gemm_f32.h"
 #include "kernels.h"
@@ -113,7 +114,7 @@ struct WorkUnit {
 
 // Slot index of part `part` of split unit tile `s` (2 * cluster + 0 for the
 // first unit of that cluster's chunk, + 1 for its last).
-__device__ __forceinline__ int split_slot(const TcParams &p, int s, int part) {
+__host__ __device__ __forceinline__ int split_slot(const TcParams &p, int s, int part) {
   const int first = (s * p.num_k_blocks) / p.sk_share;
   const int c = first + part;
   if (part > 0) return 2 * c;  // later parts start their cluster's chunk
@@ -197,22 +198,30 @@ __device__ __forceinline__ void tile_coords(const TcParams &p, int t, uint32_t r
 // remaining unit tiles, in order, cut at tile boundaries). Every cluster sees
 // the same partition, so the number of clusters contributing to a split tile
 // and each one's part index follow from the chunk boundaries alone.
+// (Host and device code: the host-side self-check gemm_f32_schedule_check
+// walks the same work lists.)
+__host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
+
 struct UnitIter {
   int sk_pos, sk_end, dp_next;
   int c, workers;
-  __device__ explicit UnitIter(const TcParams &p) {
-    c = static_cast<int>(blockIdx.x) / p.cl;
-    workers = static_cast<int>(gridDim.x) / p.cl;
+  // The work list of cluster `cluster` of `clusters`.
+  __host__ __device__ UnitIter(const TcParams &p, int cluster, int clusters) {
+    c = cluster;
+    workers = clusters;
     const int sk_total = (p.num_tiles - p.dp_tiles) * p.num_k_blocks;
     if (c < p.sk_ctas && sk_total > 0) {
-      sk_pos = min(c * p.sk_share, sk_total);
-      sk_end = min(sk_pos + p.sk_share, sk_total);
+      sk_pos = imin(c * p.sk_share, sk_total);
+      sk_end = imin(sk_pos + p.sk_share, sk_total);
     } else {
       sk_pos = sk_end = 0;
     }
     dp_next = c;
   }
-  __device__ bool next(const TcParams &p, WorkUnit &u) {
+  // This CTA's cluster.
+  __device__ explicit UnitIter(const TcParams &p)
+      : UnitIter(p, static_cast<int>(blockIdx.x) / p.cl, static_cast<int>(gridDim.x) / p.cl) {}
+  __host__ __device__ bool next(const TcParams &p, WorkUnit &u) {
     if (dp_next < p.dp_tiles) {
       u.tile = dp_next;
       u.kb0 = 0;
@@ -230,7 +239,7 @@ struct UnitIter {
       u.sk_tile = s;
       u.tile = p.dp_tiles + s;
       u.kb0 = sk_pos - s * kbt;
-      u.kb1 = min(kbt, u.kb0 + (sk_end - sk_pos));
+      u.kb1 = imin(kbt, u.kb0 + (sk_end - sk_pos));
       const int first = (s * kbt) / p.sk_share;
       const int last = ((s + 1) * kbt - 1) / p.sk_share;
       u.nparts = last - first + 1;
@@ -242,7 +251,7 @@ struct UnitIter {
     return false;
   }
   // True when no unit follows the one last returned by next().
-  __device__ bool done(const TcParams &p) const {
+  __host__ __device__ bool done(const TcParams &p) const {
     return dp_next >= p.dp_tiles && sk_pos >= sk_end;
   }
 };
@@ -1561,8 +1570,10 @@ Schedule make_schedule(int tiles, int kb, int sms, int min_chunk, bool full_wave
   } else {
     ctas = total / min_chunk;
     if (ctas > sms) ctas = sms;
-    if (ctas > static_cast<long long>(split) * kMaxSplit)
-      ctas = static_cast<long long>(split) * kMaxSplit;
+    // A tile meets at most floor((kb - 1) / share) + 2 chunks; a share of at
+    // least ceil(kb / (kMaxSplit - 1)) keeps that at kMaxSplit.
+    const long long min_share = (kb + kMaxSplit - 2) / (kMaxSplit - 1);
+    if (ctas > total / min_share) ctas = total / min_share;
     if (ctas < split) ctas = split;  // at least one CTA per tile
     if (ctas > total) ctas = total;
   }
@@ -1572,6 +1583,30 @@ Schedule make_schedule(int tiles, int kb, int sms, int min_chunk, bool full_wave
   s.splits = s.sk_share % kb != 0;
   s.grid = (split >= sms || s.dp_tiles > 0) ? sms : s.sk_ctas;
   return s;
+}
+
+// Tile counts of a launch: unit tiles of kTM rows x CL * kTN columns, k-blocks
+// of BK.
+void set_tiles(TcParams &p, int64_t M, int64_t N, int64_t K, int bk, int cl) {
+  p.num_m_blocks = static_cast<int>((M + kTM - 1) / kTM);
+  p.num_n_blocks = static_cast<int>((N + kTN - 1) / kTN);
+  p.num_k_blocks = static_cast<int>((K + bk - 1) / bk);
+  p.cl = cl;
+  p.num_nu_blocks = (p.num_n_blocks + cl - 1) / cl;
+  p.num_tiles = p.num_m_blocks * p.num_nu_blocks;
+}
+
+// The schedule policy of each kernel (see make_schedule and the constants
+// above), on `workers` clusters.
+Schedule schedule_for(const TcParams &p, int workers, int bk, bool exact, bool pair) {
+  // Full waves for the pair kernels, balanced for tc_lsu_kernel (timed at
+  // 4096^3, 5120^3, 2560 x 2560 x 4096 and 8192 x 11008 x 4096: +5-6 % for
+  // the TF32 pair kernel, which is bound by operand traffic from L2, +3 % at
+  // 4096^3 for the 3xTF32 pair kernel, whose split tiles then have fewer
+  // parts to sum, and -3 % for an earlier one-SM 3xTF32 kernel).
+  return make_schedule(p.num_tiles, p.num_k_blocks, workers,
+                       (exact ? kMinChunkKExact : kMinChunkKTf32) / bk, pair,
+                       pair && exact ? kSplitCostKExact / bk : 0);
 }
 
 // The kernel a launch plan runs: tc_lsu_kernel, or with PAIR a CTA-pair
@@ -1688,12 +1723,7 @@ struct LaunchPlan {
     p.ldc = a.ldc;
     p.alpha = a.alpha;
     p.beta = a.beta;
-    p.num_m_blocks = static_cast<int>((a.M + kTM - 1) / kTM);
-    p.num_n_blocks = static_cast<int>((a.N + kTN - 1) / kTN);
-    p.num_k_blocks = static_cast<int>((a.K + BK - 1) / BK);
-    p.cl = CL;
-    p.num_nu_blocks = (p.num_n_blocks + CL - 1) / CL;
-    p.num_tiles = p.num_m_blocks * p.num_nu_blocks;
+    set_tiles(p, a.M, a.N, a.K, BK, CL);
     // Generous: a stage takes microseconds; one tile's mainloop about K * 25 ns.
     p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
     // Workers: clusters that can be resident at once (the placement of CTA
@@ -1722,14 +1752,7 @@ struct LaunchPlan {
       }
       workers = workers_cached[dev];
     }
-    // Full waves for the pair kernels, balanced for tc_lsu_kernel (timed at
-    // 4096^3, 5120^3, 2560 x 2560 x 4096 and 8192 x 11008 x 4096: +5-6 % for
-    // the TF32 pair kernel, which is bound by operand traffic from L2, +3 % at
-    // 4096^3 for the 3xTF32 pair kernel, whose split tiles then have fewer
-    // parts to sum, and -3 % for an earlier one-SM 3xTF32 kernel).
-    sch = make_schedule(p.num_tiles, p.num_k_blocks, workers,
-                        (EXACT ? kMinChunkKExact : kMinChunkKTf32) / BK, PAIR,
-                        PAIR && EXACT ? kSplitCostKExact / BK : 0);
+    sch = schedule_for(p, workers, BK, EXACT, PAIR);
     p.dp_tiles = sch.dp_tiles;
     p.sk_share = sch.sk_share;
     p.sk_ctas = sch.sk_ctas;
@@ -2086,3 +2109,85 @@ int tc_launch_noalloc(const GemmArgs &a, bool exact, bool lsu, int sm_count, cud
 }
 
 }  // namespace gemm
+
+// ------------------------------------------------- schedule self-check --
+//
+// gemm_f32_schedule_check: the stream-K partition of a launch, built and
+// walked on the host with the kernels' own work-list code (UnitIter), and
+// checked: every k-block of every unit tile covered exactly once, whole
+// units spanning their tile's k range, a split tile's parts numbered 0 ..
+// nparts - 1 in k order with the same part count, at most kMaxSplit parts,
+// and partial-sum slots owned by their cluster and never shared.
+extern "C" int gemm_f32_schedule_check(int64_t M, int64_t N, int64_t K, int64_t workers,
+                                       int kernel_kind, int64_t *stats) {
+  using namespace gemm;
+  if (M < 1 || N < 1 || K < 1 || workers < 1 || workers > 4096 || kernel_kind < 0 ||
+      kernel_kind > 3 || stats == nullptr || M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31) ||
+      K >= (int64_t{1} << 31))
+    return GEMM_ERR_INVALID_ARG;
+  // The launch shapes tc_launch uses: 3xTF32 and TF32 pairs, and the
+  // plain-load kernel in 3xTF32 (BK 16) and TF32 (BK 32) mode.
+  const bool pair = kernel_kind < 2, exact = kernel_kind == 0 || kernel_kind == 2;
+  const int bk = kernel_kind == 0 ? kPairExactBK : (kernel_kind == 2 ? 16 : 32);
+  TcParams p = {};
+  set_tiles(p, M, N, K, bk, pair ? 2 : 1);
+  const int64_t cells = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
+  if (cells > (int64_t{1} << 26)) return GEMM_ERR_INVALID_ARG;  // keep the check's memory small
+  const Schedule sch = schedule_for(p, static_cast<int>(workers), bk, exact, pair);
+  p.dp_tiles = sch.dp_tiles;
+  p.sk_share = sch.sk_share;
+  p.sk_ctas = sch.sk_ctas;
+  const int kb = p.num_k_blocks, clusters = sch.grid;
+  std::vector<int> cover(static_cast<size_t>(cells), 0);
+  std::vector<int> part_owner(static_cast<size_t>(p.num_tiles) * kMaxSplit, -1);
+  std::vector<int> part_kb0(static_cast<size_t>(p.num_tiles) * kMaxSplit, -1);
+  std::vector<int> tile_parts(static_cast<size_t>(p.num_tiles), 0);
+  std::vector<char> slot_used(static_cast<size_t>(2 * (p.sk_ctas > 0 ? p.sk_ctas : 1)), 0);
+  int max_parts = 1;
+  for (int c = 0; c < clusters; ++c) {
+    UnitIter it(p, c, clusters);
+    WorkUnit u;
+    while (it.next(p, u)) {
+      if (u.tile < 0 || u.tile >= p.num_tiles || u.kb0 < 0 || u.kb1 > kb || u.kb0 >= u.kb1)
+        return 10;  // unit outside the problem
+      for (int k = u.kb0; k < u.kb1; ++k)
+        if (++cover[static_cast<size_t>(u.tile) * kb + k] > 1) return 11;  // covered twice
+      if (u.nparts == 1) {
+        if (u.kb0 != 0 || u.kb1 != kb) return 12;  // a whole unit must span the tile
+        continue;
+      }
+      if (u.nparts < 1 || u.nparts > kMaxSplit) return 13;
+      if (u.sk_tile != u.tile - p.dp_tiles || u.part < 0 || u.part >= u.nparts) return 14;
+      if (u.slot < 0 || u.slot >= 2 * p.sk_ctas || u.slot / 2 != c) return 15;
+      if (slot_used[static_cast<size_t>(u.slot)]++) return 16;  // slot shared
+      const size_t t = static_cast<size_t>(u.tile) * kMaxSplit + u.part;
+      if (part_owner[t] != -1) return 17;  // part index given twice
+      part_owner[t] = c;
+      part_kb0[t] = u.kb0;
+      int &np = tile_parts[static_cast<size_t>(u.tile)];
+      if (np != 0 && np != u.nparts) return 18;  // parts disagree on their count
+      np = u.nparts;
+      if (u.nparts > max_parts) max_parts = u.nparts;
+    }
+    if (!it.done(p)) return 19;
+  }
+  for (int64_t i = 0; i < cells; ++i)
+    if (cover[static_cast<size_t>(i)] != 1) return 20;  // k-block missed
+  for (int t = 0; t < p.num_tiles; ++t) {
+    const int np = tile_parts[static_cast<size_t>(t)];
+    for (int q = 0; q < np; ++q) {
+      const size_t i = static_cast<size_t>(t) * kMaxSplit + q;
+      if (part_owner[i] < 0) return 21;  // a part missing
+      if (q > 0 && part_kb0[i] <= part_kb0[i - 1]) return 22;  // parts out of k order
+    }
+  }
+  stats[0] = p.num_tiles;
+  stats[1] = kb;
+  stats[2] = p.dp_tiles;
+  stats[3] = p.sk_share;
+  stats[4] = p.sk_ctas;
+  stats[5] = sch.splits ? 1 : 0;
+  stats[6] = max_parts;
+  stats[7] = clusters;
+  return GEMM_OK;
+}

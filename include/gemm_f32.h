@@ -289,6 +289,39 @@ int gemm_f32_poll_device_status(void *stream);
  */
 int gemm_f32_selftest_wait_timeout(int64_t timeout_ns, void *stream);
 
+/* Kinds of tensor-core launch for gemm_f32_schedule_check. */
+typedef enum {
+    GEMM_SCHEDULE_EXACT_PAIR = 0,  /* 3xTF32 on CTA pairs (TMA-fed, exact mode) */
+    GEMM_SCHEDULE_TF32_PAIR = 1,   /* one TF32 pass on CTA pairs (TMA-fed) */
+    GEMM_SCHEDULE_EXACT_LSU = 2,   /* 3xTF32 on one SM per tile, plain loads */
+    GEMM_SCHEDULE_TF32_LSU = 3     /* one TF32 pass on one SM per tile, plain loads */
+} gemm_f32_schedule_kind;
+
+/*
+ * gemm_f32_schedule_check -- host-only self-check of the tile scheduler; no
+ * GPU or CUDA call. For an M x N x K problem on `workers` clusters (CTA pairs,
+ * or SMs for the plain-load kind), builds the schedule the library launches
+ * with and walks every cluster's work list with the kernels' own code. It
+ * checks that:
+ *   - every k-block of every output tile is computed exactly once;
+ *   - a whole-tile unit spans the tile's k range;
+ *   - the parts of a split tile are numbered 0 .. nparts - 1 in k order, at
+ *     most 8 of them;
+ *   - each part's partial-sum slot belongs to its own cluster and no slot is
+ *     shared.
+ *   M, N, K     >= 1 and below 2^31; tiles x k-blocks at most 2^26
+ *   workers     1 .. 4096
+ *   kind        a gemm_f32_schedule_kind
+ *   stats       host array of 8 int64 (written on success): unit tiles,
+ *               k-blocks per tile, whole tiles, stream-K share, stream-K
+ *               clusters, 1 if some tile is split, most parts of one tile,
+ *               clusters launched
+ * Returns GEMM_OK; GEMM_ERR_INVALID_ARG for bad arguments; otherwise a code
+ * from 10 up that names the check that failed (see its definition).
+ */
+int gemm_f32_schedule_check(int64_t M, int64_t N, int64_t K, int64_t workers, int kind,
+                            int64_t *stats);
+
 #ifdef __cplusplus
 }
 #endif

@@ -9,7 +9,7 @@ import pytest
 EXPECTED = {
     "gemm_f32", "gemm_f32_ex", "gemm_f32_select", "gemm_f32_host", "gemm_f32_status_string",
     "gemm_f32_poll_device_status", "gemm_f32_selftest_wait_timeout", "gemm_f32_noalloc",
-    "gemm_f32_general", "reduce_f32_sum", "gemm_f32_measure_peaks",
+    "gemm_f32_general", "reduce_f32_sum", "gemm_f32_measure_peaks", "gemm_f32_schedule_check",
 }
 
 # Fake, never dereferenced, 256-byte aligned "device" addresses for host-only paths.
