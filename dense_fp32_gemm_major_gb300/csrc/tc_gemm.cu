@@ -2,18 +2,18 @@
 //
 // C[M x N] = A[M x K] * B[K x N], all row-major fp32.
 //
-// Formulation. kind::tf32 MMAs need both operands K-major (k contiguous). A
-// (row-major M x K) already is; B (row-major K x N) is N-contiguous. Each
-// output tile is therefore computed transposed,
+// Formulation. Each output tile is computed transposed,
 //
 //     D = C_tile^T  (128 n x 256 m)  =  B_tile^T (128 n x K)  *  A_tile^T (K x 256 m),
 //
-// with B_tile^T as the MMA's A operand (in TMEM, lane = n, one 32-bit column
-// per k, where threads write it; or an MN-major shared-memory tile, the
-// 32-byte-atom swizzle, in the one-pass pair kernel) and the A tile, staged
-// K-major, as the MMA's B operand in shared memory. The accumulator D lives in TMEM with lane = n and
-// column = m, so each epilogue store writes 32 consecutive columns of one row
-// of C (a coalesced 128-byte segment).
+// with B_tile^T as the MMA's A operand and the A tile (K-major when A is
+// stored M x K) as its B operand in shared memory. B_tile^T sits in TMEM
+// (lane = n, one 32-bit column per k) where threads write it, or in shared
+// memory as an MN-major tile (B stored K x N: the 32-byte-atom swizzle, the
+// one MN-major layout kind::tf32 multiplies from) in the one-pass pair
+// kernel. The accumulator D lives in TMEM with lane = n and column = m, so
+// each epilogue store writes 32 consecutive columns of one row of C (a
+// coalesced 128-byte segment).
 //
 // Kernels (warp-specialised, persistent, one CTA per SM, grouped raster, the
 // same work list, epilogue and split-tile sum):
@@ -96,7 +96,8 @@ struct TcParams {
   // -- one for the first and one for the last unit of the cluster's chunk,
   // the only units that can be parts of a split tile.
   float *sk_partials;
-  unsigned *sk_counters;   // split tiles: parts finished so far per (tile, rank), zeroed before launch
+  // Split tiles: parts finished so far per (tile, rank), zeroed before launch.
+  unsigned *sk_counters;
   float alpha, beta;       // C = alpha * A op(B) + beta * C (beta == 0: C is not read)
   // Pair kernel: the MN-major A (B) tile comes as one copy of four 32-element
   // chunks through a 3-D tensor map (rows a multiple of 32), else as four.
@@ -318,7 +319,8 @@ __device__ __forceinline__ void epilogue_fixup(const TcParams &p, int sk_tile, u
       if (gm >= M) continue;
       float *dst = C + static_cast<long long>(gm) * ldc + gn;
       if (vec_ok && gn + 3 < N) {
-        float4 v = make_float4(alpha * acc[j].x, alpha * acc[j].y, alpha * acc[j].z, alpha * acc[j].w);
+        float4 v = make_float4(alpha * acc[j].x, alpha * acc[j].y, alpha * acc[j].z,
+                               alpha * acc[j].w);
         if (beta != 0.0f) {
           const float4 c = *reinterpret_cast<const float4 *>(dst);
           v.x += beta * c.x;
@@ -828,7 +830,7 @@ struct PairConfig {
 
 // Shared-memory descriptor of k-step kk of an operand tile: K-major rows of
 // 128 bytes (8-row swizzle atoms 1024 bytes apart, a k-step 32 bytes along
-// the row), or MN-major chunks of 32 mn (kMnChunkBytes apart, 4-row groups
+// the row), or MN-major chunks of 32 mn (BK * 128 bytes apart, 4-row groups
 // 512 bytes apart, a k-step of 8 rows 1024 bytes on).
 template <int BK, bool MN>
 __device__ __forceinline__ uint64_t pair_operand_desc(uint32_t base, int kk) {
@@ -1067,7 +1069,7 @@ struct PairExactConfig {
   static constexpr int kXformWarp0 = 6;
   static constexpr int kXformParts = XW / 4;                     // per TMEM lane quadrant
   static constexpr int kThreads = 32 * (kXformWarp0 + XW);
-  static constexpr uint32_t kIdesc = idesc_tf32(2 * kTN, kTM);   // both operands K-major
+  static constexpr uint32_t kIdesc = idesc_tf32(2 * kTN, kTM);   // A from TMEM, B K-major
   static_assert(kAStageBytes % 1024 == 0 && kBRingOffset % 1024 == 0,
                 "swizzled A stages keep 1024-byte alignment");
   static_assert(XW % 4 == 0 && BK % kXformParts == 0 && (BK / kXformParts) % 4 == 0,
@@ -1327,7 +1329,8 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
           }
         } else {
           // Column n = 32 quad + lane of the row-major tile.
-          const float *bs = reinterpret_cast<const float *>(bslot) + part * kW * kTN + quad * 32 + lane;
+          const float *bs =
+              reinterpret_cast<const float *>(bslot) + part * kW * kTN + quad * 32 + lane;
 #pragma unroll
           for (int k = 0; k < kW; ++k) v[k] = bs[k * kTN];
         }
@@ -1349,7 +1352,8 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
           break;
         }
         float4 *raw = reinterpret_cast<float4 *>(tiles + a.idx * Cfg::kAStageBytes);
-        float4 *lo = reinterpret_cast<float4 *>(tiles + a.idx * Cfg::kAStageBytes + Cfg::kALoOffset);
+        float4 *lo =
+            reinterpret_cast<float4 *>(tiles + a.idx * Cfg::kAStageBytes + Cfg::kALoOffset);
 #pragma unroll
         for (int i = xt; i < Cfg::kABytes / 16; i += 32 * XW) {
           const float4 x = raw[i];
@@ -2041,7 +2045,8 @@ int tc_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream) {
 // device image: every GPU that loads the library keeps these bytes until the
 // process exits, and all calls share them.
 
-static __device__ __align__(256) unsigned char g_gemm_noalloc_scratch[GEMM_F32_NOALLOC_SCRATCH_BYTES];
+static __device__ __align__(256) unsigned char
+    g_gemm_noalloc_scratch[GEMM_F32_NOALLOC_SCRATCH_BYTES];
 
 namespace gemm {
 namespace {
