@@ -23,6 +23,7 @@ namespace {
 using gemm::GemmArgs;
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;  // sizes and leading dimensions < 2^31
+constexpr int64_t kMaxSpan = int64_t{1} << 44;  // elements one matrix may span
 
 struct DeviceInfo {
   bool probed = false;
@@ -61,11 +62,16 @@ bool ranges_overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
   return a0 < b1 && b0 < a1;
 }
 
-// Byte range [lo, hi) touched by a rows x cols row-major matrix with pitch ld.
+// Elements spanned by a rows x cols row-major matrix with pitch ld. With
+// every argument in [1, 2^31) the product stays below 2^62.
+int64_t matrix_span(int64_t rows, int64_t cols, int64_t ld) { return (rows - 1) * ld + cols; }
+
+// Byte range [lo, hi) touched by a rows x cols row-major matrix with pitch ld
+// (its span checked against kMaxSpan first, so the byte count cannot wrap).
 void matrix_range(const void *p, int64_t rows, int64_t cols, int64_t ld, uintptr_t *lo,
                   uintptr_t *hi) {
   *lo = reinterpret_cast<uintptr_t>(p);
-  *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * 4);
+  *hi = *lo + static_cast<uintptr_t>(matrix_span(rows, cols, ld)) * 4;
 }
 
 // Host-only validation. Returns kOk, or an error; *noop is set when there is
@@ -90,8 +96,12 @@ int validate(const GemmArgs &a, int mode, bool *noop) {
     return gemm::kOk;
   }
   if (a.C == nullptr || reinterpret_cast<uintptr_t>(a.C) % 4 != 0) return gemm::kErrInvalidArg;
+  if (matrix_span(a.M, a.N, a.ldc) > kMaxSpan) return gemm::kErrInvalidArg;
   if (a.K > 0) {
     if (a.A == nullptr || a.B == nullptr) return gemm::kErrInvalidArg;
+    if (matrix_span(a_rows, a_cols, a.lda) > kMaxSpan ||
+        matrix_span(b_rows, b_cols, a.ldb) > kMaxSpan)
+      return gemm::kErrInvalidArg;
     if (reinterpret_cast<uintptr_t>(a.A) % 4 != 0 || reinterpret_cast<uintptr_t>(a.B) % 4 != 0)
       return gemm::kErrInvalidArg;
     uintptr_t c0, c1, x0, x1;
@@ -289,25 +299,34 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
   if (chunk < 1024) chunk = 1024;
   if ((M + chunk - 1) / chunk > kHostMaxChunks) chunk = (M + kHostMaxChunks - 1) / kHostMaxChunks;
   const int nchunks = static_cast<int>((M + chunk - 1) / chunk);
+  // On an error once copies are queued, wait for all queued work before
+  // returning, so that no copy reads or writes the caller's buffers after
+  // the call has returned.
+  auto drain = [&hs](int code) {
+    cudaStreamSynchronize(hs.h2d);
+    cudaStreamSynchronize(hs.stream);
+    cudaStreamSynchronize(hs.d2h);
+    return code;
+  };
   if (K > 0 && cudaMemcpy2DAsync(dB, dldb * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice,
                                  hs.h2d) != cudaSuccess)
-    return gemm::kErrLaunch;
+    return drain(gemm::kErrLaunch);
   for (int c = 0; c < nchunks; ++c) {
     const int64_t r0 = c * chunk, rows = (M - r0 < chunk) ? M - r0 : chunk;
     if (K > 0 && cudaMemcpy2DAsync(dA + r0 * dlda, dlda * 4, A + r0 * lda, lda * 4, K * 4, rows,
                                    cudaMemcpyHostToDevice, hs.h2d) != cudaSuccess)
-      return gemm::kErrLaunch;
+      return drain(gemm::kErrLaunch);
     if (cudaEventRecord(hs.a_in[c], hs.h2d) != cudaSuccess ||
         cudaStreamWaitEvent(hs.stream, hs.a_in[c], 0) != cudaSuccess)
-      return gemm::kErrLaunch;
+      return drain(gemm::kErrLaunch);
     const GemmArgs d{rows, N, K, dA + r0 * dlda, dlda, dB, dldb, dC + r0 * dldc, dldc};
     st = run(d, mode, GEMM_KERNEL_AUTO, hs.stream);
-    if (st != gemm::kOk) return st;
+    if (st != gemm::kOk) return drain(st);
     if (cudaEventRecord(hs.c_done[c], hs.stream) != cudaSuccess ||
         cudaStreamWaitEvent(hs.d2h, hs.c_done[c], 0) != cudaSuccess ||
         cudaMemcpy2DAsync(C + r0 * ldc, ldc * 4, dC + r0 * dldc, dldc * 4, N * 4, rows,
                           cudaMemcpyDeviceToHost, hs.d2h) != cudaSuccess)
-      return gemm::kErrLaunch;
+      return drain(gemm::kErrLaunch);
   }
   if (cudaStreamSynchronize(hs.d2h) != cudaSuccess) return gemm::kErrLaunch;
   return gemm::tc_poll_status(hs.stream);

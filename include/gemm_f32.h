@@ -93,7 +93,8 @@ typedef enum {
  *             must not overlap A or B (GEMM_ERR_ALIAS)
  *   mode      a gemm_f32_mode
  *   stream    cudaStream_t as void*
- * Sizes and leading dimensions must stay below 2^31 elements.
+ * Sizes and leading dimensions must stay below 2^31 elements, and the span
+ * of each matrix, (rows - 1) x ld + cols elements, at most 2^44.
  * Returns a gemm_f32_status. Stream-ordered and non-blocking.
  */
 int gemm_f32(int64_t M, int64_t N, int64_t K,
@@ -207,7 +208,8 @@ int gemm_f32_select(int64_t M, int64_t N, int64_t K,
  * differs. Same size, leading-dimension, mode and alias rules as gemm_f32
  * (alias checked on the host ranges). Device-side leading dimensions are
  * padded to multiples of 4 so the TMA-fed kernels apply at any K and N.
- * Calls on one device are serialised by a lock.
+ * Calls on one device are serialised by a lock. On every return, success
+ * or error, no copy the call queued still reads or writes the host buffers.
  */
 int gemm_f32_host(int64_t M, int64_t N, int64_t K,
                   const float *A, int64_t lda,

@@ -41,6 +41,9 @@ def test_status_strings(gemm_lib):
     dict(A=0), dict(B=0), dict(C=0),                   # null with non-zero extents
     dict(A=PA + 2), dict(C=PC + 1),                    # not 4-byte aligned
     dict(M=1 << 31), dict(lda=1 << 31),                # beyond the 2^31 element limit
+    dict(M=(1 << 31) - 1, ldc=(1 << 31) - 1),          # spans beyond 2^44 elements
+    dict(M=(1 << 31) - 1, lda=(1 << 31) - 1),
+    dict(K=(1 << 31) - 1, lda=(1 << 31) - 1, ldb=(1 << 31) - 1),
 ])
 def test_invalid_arguments_rejected_before_any_cuda_call(gemm_lib, args):
     a = dict(M=16, N=32, K=64, A=PA, lda=64, B=PB, ldb=32, C=PC, ldc=32, mode=0)
