@@ -193,13 +193,29 @@ def _kernel(kernel) -> int:
     return KERNELS[kernel] if isinstance(kernel, str) else int(kernel)
 
 
-def _check_operand(t, name):
+def _check_rows(shape, row_stride, col_stride, name):
+    """A matrix the library can address as (pointer, leading dimension): unit
+    column stride and rows that do not overlap (strides in elements). Views
+    that break either rule (expanded, transposed or reversed ones) would make
+    the library read or write outside the matrix, so they are refused."""
+    rows, cols = int(shape[0]), int(shape[1])
+    if rows == 0 or cols == 0:
+        return
+    if cols > 1 and col_stride != 1:
+        raise ValueError(f"{name} must be row-major (unit column stride)")
+    if rows > 1 and row_stride < cols:
+        raise ValueError(f"{name} has overlapping or reversed rows (row stride {row_stride} "
+                         f"for {cols} columns)")
+
+
+def _check_operand(t, name, device=None):
     import torch
 
     if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda or t.dim() != 2:
         raise TypeError(f"{name} must be a 2-D float32 CUDA tensor")
-    if t.shape[1] > 1 and t.stride(1) != 1:
-        raise ValueError(f"{name} must be row-major (unit column stride)")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the other operands on {device}")
+    _check_rows(t.shape, t.stride(0), t.stride(1), name)
 
 
 def _ld(t) -> int:
@@ -216,7 +232,7 @@ def matmul(a, b, mode="exact", out=None, kernel="auto", stream=None):
     import torch
 
     _check_operand(a, "a")
-    _check_operand(b, "b")
+    _check_operand(b, "b", a.device)
     m, k = a.shape
     k2, n = b.shape
     if k != k2:
@@ -224,7 +240,7 @@ def matmul(a, b, mode="exact", out=None, kernel="auto", stream=None):
     if out is None:
         out = torch.empty((m, n), dtype=torch.float32, device=a.device)
     else:
-        _check_operand(out, "out")
+        _check_operand(out, "out", a.device)
         if tuple(out.shape) != (m, n):
             raise ValueError("out has the wrong shape")
     if stream is None:
@@ -249,7 +265,7 @@ def gemm(a, b, out=None, alpha=1.0, beta=0.0, transa=False, transb=False, mode="
     import torch
 
     _check_operand(a, "a")
-    _check_operand(b, "b")
+    _check_operand(b, "b", a.device)
     m, k = (a.shape[1], a.shape[0]) if transa else tuple(a.shape)
     k2, n = (b.shape[1], b.shape[0]) if transb else tuple(b.shape)
     if k != k2:
@@ -259,7 +275,7 @@ def gemm(a, b, out=None, alpha=1.0, beta=0.0, transa=False, transb=False, mode="
             raise ValueError("beta != 0 needs out")
         out = torch.empty((m, n), dtype=torch.float32, device=a.device)
     else:
-        _check_operand(out, "out")
+        _check_operand(out, "out", a.device)
         if tuple(out.shape) != (m, n):
             raise ValueError("out has the wrong shape")
     if stream is None:
@@ -284,6 +300,9 @@ def vector_sum(x, groups=0, out=None, stream=None):
         raise TypeError("x must be a contiguous 1-D float32 CUDA tensor")
     if out is None:
         out = torch.empty(1, dtype=torch.float32, device=x.device)
+    elif (not isinstance(out, torch.Tensor) or out.dtype != torch.float32
+          or out.device != x.device or out.numel() < 1):
+        raise TypeError("out must be a float32 tensor of at least one element on x's device")
     if stream is None:
         stream = torch.cuda.current_stream(x.device).cuda_stream
     with torch.cuda.device(x.device):
@@ -293,19 +312,34 @@ def vector_sum(x, groups=0, out=None, stream=None):
     return out
 
 
+def _check_host(x, name):
+    import numpy as np
+
+    if not isinstance(x, np.ndarray) or x.dtype != np.float32 or x.ndim != 2:
+        raise TypeError(f"{name} must be a 2-D float32 numpy array")
+    if x.strides[0] % 4 or x.strides[1] % 4:
+        raise ValueError(f"{name}'s strides are not whole elements")
+    _check_rows(x.shape, x.strides[0] // 4, x.strides[1] // 4, name)
+
+
 def matmul_host(a, b, mode="exact", out=None):
     """C = A x B for host numpy float32 arrays through gemm_f32_host (blocking)."""
     import numpy as np
 
-    for x, name in ((a, "a"), (b, "b")):
-        if not isinstance(x, np.ndarray) or x.dtype != np.float32 or x.ndim != 2 or x.strides[1] != 4:
-            raise TypeError(f"{name} must be a row-major 2-D float32 numpy array")
+    _check_host(a, "a")
+    _check_host(b, "b")
     m, k = a.shape
     k2, n = b.shape
     if k != k2:
         raise ValueError("inner dimensions differ")
     if out is None:
         out = np.empty((m, n), dtype=np.float32)
+    else:
+        _check_host(out, "out")
+        if out.shape != (m, n):
+            raise ValueError("out has the wrong shape")
+        if not out.flags.writeable:
+            raise ValueError("out is read-only")
     ld = lambda x: max(x.strides[0] // 4, x.shape[1], 1) if x.shape[0] > 1 else max(x.shape[1], 1)
     st = gemm_f32_host(m, n, k, a.ctypes.data, ld(a), b.ctypes.data, ld(b), out.ctypes.data,
                        ld(out), _mode(mode))
