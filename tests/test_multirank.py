@@ -68,3 +68,4 @@ def test_reference_arm_is_rank0_only(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     bench.run_reference(Args(), rank=1)
     assert capsys.readouterr().out == ""
+
