@@ -133,15 +133,16 @@ def pin_integer_selftest(gemm):
     # A[i] = (i mod 7) - 3 over m x k, B[i] = (i mod 5) - 2 over k x n, m, n, k = 32, 24, 16;
     # all values are small integers, so the result is exact
     m, n, k = 32, 24, 16
-    av = [(i % 7) - 3 for i in range(m * k)]
-    bv = [(i % 5) - 2 for i in range(k * n)]
-    a = np.array(av, dtype=np.float32).reshape(m, k)
-    b = np.array(bv, dtype=np.float32).reshape(k, n)
-    c64, _ = gemm(a, b)
-    for r in range(m):
-        for q in range(n):
-            if c64[r, q] != sum(av[r * k + p] * bv[p * n + q] for p in range(k)):
-                return "integer self-test"
+    # element (row, col) of each operand takes the pattern at its row-major
+    # linear index
+    a_int = [[(row * k + col) % 7 - 3 for col in range(k)] for row in range(m)]
+    b_int = [[(row * n + col) % 5 - 2 for col in range(n)] for row in range(k)]
+    c64, _ = gemm(np.array(a_int, dtype=np.float32), np.array(b_int, dtype=np.float32))
+    # the product in Python integers (exact)
+    b_cols = list(zip(*b_int))
+    want = [[sum(x * y for x, y in zip(a_row, b_col)) for b_col in b_cols] for a_row in a_int]
+    if not np.array_equal(c64, np.array(want, dtype=np.float64)):
+        return "integer self-test"
     return None
 
 
