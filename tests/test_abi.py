@@ -3,6 +3,7 @@ header declares, and validates arguments and picks kernels on the host
 before touching CUDA."""
 
 import ctypes
+import os
 
 import pytest
 
@@ -200,3 +201,37 @@ def test_missing_library_fails_loudly(gemm_lib, monkeypatch, tmp_path):
     monkeypatch.setattr(g, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         g.gemm_f32(1, 1, 1, PA, 1, PB, 1, PC, 1, 0, 0)
+
+
+def test_headers_compile_and_link_as_c(gemm_lib, tmp_path):
+    # The boundary is a C ABI: the public headers must compile as strict C99
+    # and a C program must link against the library and call it (host-only
+    # entry points here, so no GPU is needed).
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not installed")
+    src = tmp_path / "abi.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include "gemm_f32.h"
+#include "reduce_f32.h"
+int main(void) {
+  int64_t stats[8];
+  int st = gemm_f32_schedule_check(4096, 4096, 4096, 76, GEMM_SCHEDULE_EXACT_PAIR, stats);
+  int sel = gemm_f32_select(64, 64, 64, (const float *)0x10000000, 64,
+                            (const float *)0x20000000, 64, (float *)0x30000000, 64,
+                            GEMM_F32_EXACT, GEMM_KERNEL_AUTO);
+  printf("%d %lld %d %s\n", st, (long long)stats[0], sel, gemm_f32_status_string(GEMM_ERR_ALIAS));
+  return 0;
+}
+''')
+    lib_dir = os.path.dirname(gemm_lib.LIB_PATH)
+    exe = tmp_path / "abi"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", gemm_lib.INCLUDE_DIR, str(src), "-L", lib_dir, "-lgemm_f32",
+                    f"-Wl,-rpath,{lib_dir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert out == ["0", "256", str(gemm_lib.KERNEL_TC_TMA), "GEMM_ERR_ALIAS"]
