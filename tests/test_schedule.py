@@ -62,3 +62,20 @@ def test_schedule_check_rejects_bad_arguments(gemm_lib):
     for args in bad:
         st, _ = gemm_lib.gemm_f32_schedule_check(*args)
         assert st == gemm_lib.ERR_INVALID_ARG, args
+
+
+def test_partition_random_shapes_and_worker_counts(gemm_lib):
+    # seeded random sizes (log-uniform up to 2^15 per side, so at most 2^25
+    # tile k-blocks, inside the check's enumeration limit) on worker counts
+    # from 1 to 152, all four launch kinds
+    import numpy as np
+
+    rng = np.random.default_rng(20261202)
+    for i in range(2000):
+        m, n, k = (int(x) for x in np.exp2(rng.uniform(0, 15, 3)).astype(np.int64))
+        w = int(rng.integers(1, 153))
+        kind = KINDS[i % 4]
+        st, stats = gemm_lib.gemm_f32_schedule_check(m, n, k, w, kind)
+        assert st == gemm_lib.OK, f"{kind} {m}x{n}x{k} on {w}: check {st}"
+        assert stats["clusters"] <= w
+        assert stats["max_parts"] <= 8
