@@ -41,9 +41,14 @@ WORKLOADS = {
 WORKLOAD = WORKLOADS["c4"]
 M = N = K = 4096
 FLUSH_BYTES = 256 << 20
-TF32_PER_BF16 = 1.1 / 2.25          # nominal dense TF32 : BF16 tensor rate
-SMS = 152
+# Nominal dense tensor rates of one GB300: TF32 1.1 PFLOP/s, BF16 2.25 PFLOP/s
+# (without 2:4 sparsity). Their ratio turns the measured bf16 peak into the
+# TF32 denominator.
+TF32_PER_BF16 = 1.1 / 2.25
 FP32_LANES_PER_SM = 128
+# Workloads timed in the configs leg besides the benchmark's own, and the
+# steps each takes (8192 x 11008 x 4096 runs 2 ms per exact call).
+CONFIG_LEG = (("c1", 50), ("c2", 50), ("c3", 50), ("c4", 50), ("c5a", 50), ("c5b", 10))
 
 
 def parse_args():
@@ -417,8 +422,9 @@ def main():
     ms_per_step = total_ms / args.steps
 
     pk = peaks()
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     tf32_peak = pk["bf16"] * TF32_PER_BF16
-    alu_peak = SMS * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+    alu_peak = sms * FP32_LANES_PER_SM * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
     if args.layout != "nn" and kernel != g.KERNEL_SIMT:
         # A stored transposed reaches the TMA-fed 3xTF32 kernel through a
         # transposed copy (the TF32 pair kernel reads it as it is)
@@ -431,7 +437,7 @@ def main():
         roofline = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(alu_peak, 1),
                     "unit": "TFLOP/s", "frac": round(achieved / alu_peak, 4), "traffic": traffic,
                     "kernel": kernel_name,
-                    "peak_source": f"{SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x "
+                    "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x "
                                    f"{pk['sm_max_mhz']:.0f} MHz"}
     else:
         mult = 3 if args.mode == "exact" else 1  # 3xTF32: three TF32 MMAs per fp32 multiply-add
@@ -440,7 +446,7 @@ def main():
                     "unit": "TFLOP/s", "frac": round(achieved / tf32_peak, 4), "traffic": traffic,
                     "kernel": kernel_name,
                     "peak_source": f"{pk['source']} bf16 burst {pk['bf16']} TFLOP/s x nominal "
-                                   f"TF32/BF16 ratio {TF32_PER_BF16:.4f}",
+                                   f"dense TF32/BF16 ratio 1.1/2.25 = {TF32_PER_BF16:.4f}",
                     "achieved_counts": f"{mult} x 2MNK TF32 flops"}
 
     extras = {}
@@ -483,15 +489,60 @@ def main():
         extras["library_reference"] = lib_ref
         # context, not a denominator: what the TF32 tensor pipe and the FP32
         # FMA pipe deliver to MMA-only / FFMA-only probe kernels here
-        pst, ptf32, pfp32 = g.gemm_f32_measure_peaks()
+        pst, ptf32, pfp32, ptf32_mhz, pfp32_mhz = g.gemm_f32_measure_peaks()
         if pst == g.OK:
-            probe = {"tf32_mma_tflops": round(ptf32, 1), "fp32_fma_tflops": round(pfp32, 1),
-                     "note": "probe kernels (gemm_f32_measure_peaks); the roofline fractions "
-                             "stay against the measured bf16 peak x the nominal ratio"}
+            probe = {"tf32_mma_tflops": round(ptf32, 1), "tf32_sm_mhz": round(ptf32_mhz),
+                     "fp32_fma_tflops": round(pfp32, 1), "fp32_sm_mhz": round(pfp32_mhz),
+                     "note": "probe kernels (gemm_f32_measure_peaks): operands non-zero, SM "
+                             "clock measured inside each kernel (clock64 ticks / globaltimer); "
+                             "the roofline fractions stay against the measured bf16 peak x the "
+                             "nominal ratio"}
             extras["probe_peaks"] = probe
-            pk_ctx = pfp32 if roofline["bound"] == "alu" else ptf32
+            pk_ctx, pk_mhz = (pfp32, pfp32_mhz) if roofline["bound"] == "alu" else (ptf32, ptf32_mhz)
             roofline["probe_peak"] = round(pk_ctx, 1)
+            roofline["probe_sm_mhz"] = round(pk_mhz)
             roofline["frac_of_probe_peak"] = round(roofline["achieved"] / pk_ctx, 4)
+            if clocks and clocks.get("sm_mhz") and pk_mhz > 0:
+                # flops per SM clock against the probe's flops per SM clock:
+                # the kernel at the median clock sampled over its timed steps
+                roofline["frac_of_probe_peak_per_clock"] = round(
+                    (roofline["achieved"] / clocks["sm_mhz"]) / (pk_ctx / pk_mhz), 4)
+        else:
+            ptf32 = None
+        # every workload of the benchmark table in both tensor-core modes:
+        # fewer steps, same protocol (L2 flushed between steps), through gemm_f32
+        configs = {}
+        for cname, csteps in CONFIG_LEG:
+            ca, cb, ccfg = synth.config_operands(cname)
+            cm, cn, ck = ccfg["M"], ccfg["N"], ccfg["K"]
+            xa, xb = torch.from_numpy(ca).cuda(), torch.from_numpy(cb).cuda()
+            xc = torch.empty((cm, cn), dtype=torch.float32, device="cuda")
+            cflops = 2.0 * cm * cn * ck
+            entry = {"workload": WORKLOADS[cname], "M": cm, "N": cn, "K": ck}
+            for mname, mcode, mult in (("exact", g.EXACT, 3), ("tf32", g.TF32, 1)):
+                def cfn(mcode=mcode):
+                    st = g.gemm_f32(cm, cn, ck, xa.data_ptr(), ck, xb.data_ptr(), cn, xc.data_ptr(),
+                                    cn, mcode, sptr)
+                    if st != g.OK:
+                        raise g.GemmError(st)
+                xc.fill_(float("nan"))
+                ts, _ = time_steps(torch, cfn, csteps, 5, flush, stream)
+                ms = statistics.mean(ts)
+                ach = mult * cflops / (ms / 1e3) / 1e12
+                mk = g.gemm_f32_select(cm, cn, ck, xa.data_ptr(), ck, xb.data_ptr(), cn,
+                                       xc.data_ptr(), cn, mcode, g.KERNEL_AUTO)
+                entry[mname] = {
+                    "value": round(cflops / (ms / 1e3) / 1e9, 1), "unit": "GFLOP/s",
+                    "us_per_call": round(ms * 1e3, 2),
+                    "us_per_call_median": round(statistics.median(ts) * 1e3, 2),
+                    "steps": csteps, "kernel": kernel_label(g, mk, mname),
+                    "achieved_tflops": round(ach, 2), "achieved_counts": f"{mult} x 2MNK TF32 flops",
+                    "frac": round(ach / tf32_peak, 4),
+                    "frac_of_probe_peak": round(ach / ptf32, 4) if ptf32 else None,
+                    "all_finite": bool(torch.isfinite(xc).all().item())}
+            configs[cname] = entry
+            del xa, xb, xc
+        extras["configs"] = configs
         # the pages' second workload: the per-group tree reduction of 2^26 fp32
         # values (two dispatches), HBM-bound; the vector (256 MiB) exceeds L2,
         # so steps run back to back without a flush

@@ -78,13 +78,14 @@ def _load():
     lib.reduce_f32_sum.restype = i32
     lib.gemm_f32_status_string.argtypes = [i32]
     lib.gemm_f32_status_string.restype = ctypes.c_char_p
-    lib.gemm_f32_measure_peaks.argtypes = [ctypes.POINTER(ctypes.c_double),
-                                           ctypes.POINTER(ctypes.c_double)]
+    lib.gemm_f32_measure_peaks.argtypes = [ctypes.POINTER(ctypes.c_double)] * 4
     lib.gemm_f32_measure_peaks.restype = i32
     lib.gemm_f32_poll_device_status.argtypes = [p]
     lib.gemm_f32_poll_device_status.restype = i32
     lib.gemm_f32_selftest_wait_timeout.argtypes = [i64, p]
     lib.gemm_f32_selftest_wait_timeout.restype = i32
+    lib.gemm_f32_selftest_stalled_gemm.argtypes = sig + [i32, i64, p]
+    lib.gemm_f32_selftest_stalled_gemm.restype = i32
     lib.gemm_f32_schedule_check.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.gemm_f32_schedule_check.restype = i32
     _lib = lib
@@ -155,11 +156,14 @@ def gemm_f32_status_string(status: int) -> str:
 
 
 def gemm_f32_measure_peaks():
-    """(status, tf32_tflops, fp32_tflops) from the MMA-only and FFMA-only
-    probe kernels on the current device."""
+    """(status, tf32_tflops, fp32_tflops, tf32_sm_mhz, fp32_sm_mhz) from the
+    MMA-only and FFMA-only probe kernels on the current device: each rate and
+    the median SM clock its kernel ran at."""
     t, f = ctypes.c_double(0.0), ctypes.c_double(0.0)
-    st = _load().gemm_f32_measure_peaks(ctypes.byref(t), ctypes.byref(f))
-    return st, t.value, f.value
+    tc, fc = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    st = _load().gemm_f32_measure_peaks(ctypes.byref(t), ctypes.byref(f), ctypes.byref(tc),
+                                        ctypes.byref(fc))
+    return st, t.value, f.value, tc.value, fc.value
 
 
 def gemm_f32_poll_device_status(stream=0) -> int:
@@ -168,6 +172,12 @@ def gemm_f32_poll_device_status(stream=0) -> int:
 
 def gemm_f32_selftest_wait_timeout(timeout_ns: int, stream=0) -> int:
     return _load().gemm_f32_selftest_wait_timeout(timeout_ns, stream or None)
+
+
+def gemm_f32_selftest_stalled_gemm(M, N, K, A, lda, B, ldb, C, ldc, mode, timeout_ns,
+                                   stream=0) -> int:
+    return _load().gemm_f32_selftest_stalled_gemm(M, N, K, A, lda, B, ldb, C, ldc, mode,
+                                                  timeout_ns, stream or None)
 
 
 SCHEDULE_KINDS = {"exact_pair": 0, "tf32_pair": 1, "exact_lsu": 2, "tf32_lsu": 3}

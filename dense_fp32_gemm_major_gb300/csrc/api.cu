@@ -396,14 +396,17 @@ const char *gemm_f32_status_string(int status) {
   }
 }
 
-int gemm_f32_measure_peaks(double *tf32_tflops, double *fp32_tflops) {
-  if (tf32_tflops == nullptr || fp32_tflops == nullptr) return GEMM_ERR_INVALID_ARG;
+int gemm_f32_measure_peaks(double *tf32_tflops, double *fp32_tflops, double *tf32_sm_mhz,
+                           double *fp32_sm_mhz) {
+  if (tf32_tflops == nullptr || fp32_tflops == nullptr || tf32_sm_mhz == nullptr ||
+      fp32_sm_mhz == nullptr)
+    return GEMM_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   const int st = current_device(&dev, &sms);
   if (st != gemm::kOk) return st;
   cudaStream_t s = nullptr;
   if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return GEMM_ERR_LAUNCH;
-  const int r = gemm::probe_peaks(sms, tf32_tflops, fp32_tflops, s);
+  const int r = gemm::probe_peaks(sms, tf32_tflops, fp32_tflops, tf32_sm_mhz, fp32_sm_mhz, s);
   cudaStreamDestroy(s);
   return r;
 }
@@ -421,6 +424,23 @@ int gemm_f32_selftest_wait_timeout(int64_t timeout_ns, void *stream) {
   const int st = current_device(&dev, &sms);
   if (st != gemm::kOk) return st;
   return gemm::tc_selftest_wait_timeout(timeout_ns, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_f32_selftest_stalled_gemm(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                   const float *B, int64_t ldb, float *C, int64_t ldc, int mode,
+                                   int64_t timeout_ns, void *stream) {
+  if (timeout_ns < 1000000 || timeout_ns > 10000000000LL) return GEMM_ERR_INVALID_ARG;
+  if (mode != GEMM_F32_EXACT && mode != GEMM_F32_TF32) return GEMM_ERR_INVALID_ARG;
+  const GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
+  bool noop = false;
+  int st = validate(a, mode, &noop);
+  if (st != gemm::kOk) return st;
+  if (noop) return GEMM_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  st = current_device(&dev, &sms);
+  if (st != gemm::kOk) return st;
+  return gemm::tc_selftest_stalled_gemm(a, mode == GEMM_F32_EXACT, timeout_ns, sms,
+                                        static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -83,8 +83,10 @@ int pack_rows_launch(const PackJob &first, const PackJob &second, int sm_count,
                      cudaStream_t stream);
 
 // Rates of the TF32 tensor pipe (MMA-only kernel) and of the FP32 FMA pipe
-// (FFMA-only kernel) on sm_count SMs, in TFLOP/s. Blocking.
-int probe_peaks(int sm_count, double *tf32_tflops, double *fp32_tflops, cudaStream_t stream);
+// (FFMA-only kernel) on sm_count SMs, in TFLOP/s, and the median SM clock
+// (MHz) each kernel's CTAs ran at. Blocking.
+int probe_peaks(int sm_count, double *tf32_tflops, double *fp32_tflops, double *tf32_mhz,
+                double *fp32_mhz, cudaStream_t stream);
 
 // SIMT FP32 GEMM. Requires K >= 1, M >= 1, N >= 1.
 int simt_launch(const GemmArgs &a, cudaStream_t stream);
@@ -94,5 +96,11 @@ int tc_poll_status(cudaStream_t stream);
 
 // Bounded-wait self-test (see gemm_f32_selftest_wait_timeout).
 int tc_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream);
+
+// Abort-path self-test (see gemm_f32_selftest_stalled_gemm): the TMA-fed pair
+// kernel of the mode with its producers stopping after one k-block; returns
+// the device status read after the launch.
+int tc_selftest_stalled_gemm(const GemmArgs &a, bool exact, int64_t timeout_ns, int sm_count,
+                             cudaStream_t stream);
 
 }  // namespace gemm

@@ -103,6 +103,10 @@ struct TcParams {
   // chunks through a 3-D tensor map (rows a multiple of 32), else as four.
   int a_one_copy, b_one_copy;
   unsigned long long timeout_ns;
+  // Failure-detection self-test only: the pair kernels' producer issues no
+  // copy after this many k-blocks, so the other roles' bounded waits run out
+  // and the abort path runs. -1 (never stop) in every other launch.
+  int stall_kb;
 };
 
 // One unit of work of a CTA: k-blocks [kb0, kb1) of unit tile `tile`.
@@ -904,6 +908,7 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
     // ---------------------------------------------------------- producer --
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, armed = 0, armed_parity = 0;
+      int issued = 0;
       bool ok = true;
       UnitIter it(p);
       WorkUnit u;
@@ -913,6 +918,10 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
         const int m0 = mb * kTM + static_cast<int>(rank) * Cfg::kHalfRows;
         const int n0 = nb * kTN;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          if (issued++ == p.stall_kb) {  // self-test: stop feeding the pipeline
+            ok = false;
+            break;
+          }
           if (!mbar_wait_bounded(&sh->empty[stage], phase ^ 1, p.timeout_ns, abort,
                                  &g_tc_status)) {
             ok = false;
@@ -1167,6 +1176,7 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
       RingPos<AST> a;
       RingPos<BST> b;
       uint32_t armed = 0, armed_parity = 0, barmed = 0, barmed_parity = 0;
+      int issued = 0;
       bool ok = true;
       UnitIter it(p);
       WorkUnit u;
@@ -1176,6 +1186,10 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
         const int m0 = mb * kTM + static_cast<int>(rank) * Cfg::kHalfRows;
         const int n0 = nb * kTN;
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
+          if (issued++ == p.stall_kb) {  // self-test: stop feeding the pipeline
+            ok = false;
+            break;
+          }
           if (!mbar_wait_bounded(&sh->empty[a.idx], a.phase ^ 1, p.timeout_ns, abort,
                                  &g_tc_status)) {
             ok = false;
@@ -1730,6 +1744,7 @@ struct LaunchPlan {
     set_tiles(p, a.M, a.N, a.K, BK, CL);
     // Generous: a stage takes microseconds; one tile's mainloop about K * 25 ns.
     p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
+    p.stall_kb = -1;
     // Workers: clusters that can be resident at once (the placement of CTA
     // pairs may leave some SMs unpaired).
     static int workers_cached[64] = {};
@@ -2032,6 +2047,36 @@ int tc_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream) {
   selftest_wait_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(timeout_ns));
   if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
   return tc_poll_status(stream);
+}
+
+namespace {
+
+// One launch of a TMA-fed pair kernel whose producers stop after their first
+// k-block, with every wait limited to timeout_ns. Only problems without split
+// tiles (no workspace) are accepted.
+template <class Plan>
+int stalled_launch(const GemmArgs &a, int64_t timeout_ns, int sm_count, cudaStream_t stream) {
+  Plan plan;
+  int st = plan.prepare(a, sm_count);
+  if (st != kOk) return st;
+  if (plan.counter_bytes > 0) return kErrInvalidArg;
+  plan.p.timeout_ns = static_cast<unsigned long long>(timeout_ns);
+  plan.p.stall_kb = 1;
+  st = plan.launch(stream);
+  if (st != kOk) return st;
+  return tc_poll_status(stream);
+}
+
+}  // namespace
+
+int tc_selftest_stalled_gemm(const GemmArgs &a, bool exact, int64_t timeout_ns, int sm_count,
+                             cudaStream_t stream) {
+  if (!tc_tma_direct(a) || a.opb || a.K < 2 * 32) return kErrInvalidArg;
+  if (exact)
+    return stalled_launch<LaunchPlan<kPairExactBK, kPairExactStages, true, false, 2, false, false,
+                                     kPairExactBSlots, true>>(a, timeout_ns, sm_count, stream);
+  return stalled_launch<LaunchPlan<32, kPairStages, false, false, 2, false, false, 0, true>>(
+      a, timeout_ns, sm_count, stream);
 }
 
 }  // namespace gemm

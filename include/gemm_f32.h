@@ -245,8 +245,17 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K,
  * few counters (under 39 MiB on a 152-SM GB300, whatever the shape), so on
  * such a device every valid problem fits; the check guards larger devices.
  *
- * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
+ * Set-up. The array belongs to the library's tensor-core code module, which
+ * the CUDA runtime places in device memory when it first needs it on a
+ * device: with CUDA's lazy module loading (the default) that is the first
+ * tensor-core call of any entry point, or the first gemm_f32_noalloc call,
+ * whose set-up also looks up the array's device address (with that device
+ * current). So make one gemm_f32_noalloc call on each device before handing
+ * device memory to another allocator and before any stream capture, or set
+ * CUDA_MODULE_LOADING=EAGER so that the array is placed when the context is
+ * created. The address is kept for the life of the process: calls after
+ * cudaDeviceReset on that device are not supported.
+ *
  * Every call on a device uses the same array and leaves its contents behind;
  * the call itself clears what must start at zero. Calls whose work overlaps
  * on the GPU (different streams, or different host threads) race on the
@@ -261,13 +270,17 @@ int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K,
 /*
  * gemm_f32_measure_peaks -- measurement helper, not part of any computation:
  * runs an MMA-only kernel (tcgen05.mma kind::tf32, 128 x 256 x 8, operands
- * resident in shared memory, one CTA per SM) and an FFMA-only kernel
- * (independent fused multiply-add chains, 1024 threads per SM) on the
- * current device and returns the rates they reach, in TFLOP/s, through the
- * two pointers (host memory). Blocking; takes a fraction of a second. The
+ * resident in shared memory and filled with non-zero values, one CTA per SM)
+ * and an FFMA-only kernel (independent fused multiply-add chains, 1024
+ * threads per SM) on the current device and returns, through the four
+ * pointers (host memory), the rates they reach in TFLOP/s and the median SM
+ * clock in MHz each kernel's CTAs ran at (SM clock ticks over wall time,
+ * measured inside the kernel), so that a rate can be compared with another
+ * measured at a different clock. Blocking; takes a fraction of a second. The
  * pages have no counterpart: they time their kernels against no peak.
  */
-int gemm_f32_measure_peaks(double *tf32_tflops, double *fp32_tflops);
+int gemm_f32_measure_peaks(double *tf32_tflops, double *fp32_tflops,
+                           double *tf32_sm_mhz, double *fp32_sm_mhz);
 
 /* gemm_f32_status_string -- static, NUL-terminated name of a status code. */
 const char *gemm_f32_status_string(int status);
@@ -290,6 +303,35 @@ int gemm_f32_poll_device_status(void *stream);
  * the mechanism works). The context stays usable afterwards.
  */
 int gemm_f32_selftest_wait_timeout(int64_t timeout_ns, void *stream);
+
+/*
+ * gemm_f32_selftest_stalled_gemm -- failure-detection self-test of the GEMM
+ * kernels' own abort path. Runs the TMA-fed CTA-pair kernel of `mode`
+ * (GEMM_F32_EXACT: 3xTF32; GEMM_F32_TF32: one TF32 pass) on C = A x B with
+ * every pipeline wait limited to `timeout_ns` (1e6 .. 1e10), and with its
+ * producers stopping after their first k-block: they issue no further copy
+ * and no arrival, and wait (bounded) for the copies they did issue, so
+ * nothing they started is still in flight. The MMA, transform and epilogue
+ * roles then wait for k-blocks that never come; their waits run out, record
+ * GEMM_ERR_TIMEOUT in the device status word and raise the CTA's abort flag;
+ * every role leaves its loop, the MMAs issued so far complete, both CTAs of
+ * each pair meet at the cluster barrier, TMEM is freed and the kernel
+ * returns. Synchronises `stream` and returns what
+ * gemm_f32_poll_device_status then reads (GEMM_ERR_TIMEOUT when the abort
+ * path works); C's contents are unspecified afterwards. The context stays
+ * usable.
+ *   M, N, K, A, lda, B, ldb, C, ldc   as for gemm_f32, with K >= 64 (two
+ *             k-blocks), A and B 16-byte aligned with pitches that are
+ *             multiples of 4, and a problem whose output tiles are not split
+ *             between SMs (M x N of at most one 256 x 256 tile per CTA pair),
+ *             else GEMM_ERR_INVALID_ARG.
+ * The pages have no counterpart: their kernels have no waits that can fail.
+ */
+int gemm_f32_selftest_stalled_gemm(int64_t M, int64_t N, int64_t K,
+                                   const float *A, int64_t lda,
+                                   const float *B, int64_t ldb,
+                                   float *C, int64_t ldc,
+                                   int mode, int64_t timeout_ns, void *stream);
 
 /* Kinds of tensor-core launch for gemm_f32_schedule_check. */
 typedef enum {

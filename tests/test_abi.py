@@ -11,6 +11,7 @@ EXPECTED = {
     "gemm_f32", "gemm_f32_ex", "gemm_f32_select", "gemm_f32_host", "gemm_f32_status_string",
     "gemm_f32_poll_device_status", "gemm_f32_selftest_wait_timeout", "gemm_f32_noalloc",
     "gemm_f32_general", "reduce_f32_sum", "gemm_f32_measure_peaks", "gemm_f32_schedule_check",
+    "gemm_f32_selftest_stalled_gemm",
 }
 
 # Fake, never dereferenced, 256-byte aligned "device" addresses for host-only paths.
@@ -181,7 +182,7 @@ def test_measure_peaks_without_gpu_fails_cleanly(gemm_lib):
 
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
-    st, _, _ = gemm_lib.gemm_f32_measure_peaks()
+    st, _, _, _, _ = gemm_lib.gemm_f32_measure_peaks()
     assert st in (gemm_lib.ERR_LAUNCH, gemm_lib.ERR_UNSUPPORTED_DEVICE)
 
 
@@ -235,3 +236,14 @@ int main(void) {
                     f"-Wl,-rpath,{lib_dir}", "-o", str(exe)], check=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
     assert out == ["0", "256", str(gemm_lib.KERNEL_TC_TMA), "GEMM_ERR_ALIAS"]
+
+
+def test_stalled_gemm_self_test_validates_on_the_host(gemm_lib):
+    # argument errors come back before any CUDA call: limit out of range,
+    # a mode without a pair kernel, bad sizes
+    g = gemm_lib
+    args = (512, 512, 256, PA, 256, PB, 512, PC, 512)
+    assert g.gemm_f32_selftest_stalled_gemm(*args, g.EXACT, 10, 0) == g.ERR_INVALID_ARG
+    assert g.gemm_f32_selftest_stalled_gemm(*args, g.EXACT_SIMT, 20_000_000, 0) == g.ERR_INVALID_ARG
+    assert g.gemm_f32_selftest_stalled_gemm(512, 512, 256, PA, 255, PB, 512, PC, 512, g.TF32,
+                                            20_000_000, 0) == g.ERR_INVALID_ARG

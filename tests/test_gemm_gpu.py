@@ -302,11 +302,17 @@ def test_host_entry_point_long_k(g):
 def test_probe_peaks_are_plausible(g):
     # MMA-only and FFMA-only probe kernels: rates between half and twice the
     # nominal GB300 figures (1.1 PFLOP/s dense TF32; 152 SMs x 128 lanes x 2
-    # flops x 2.07 GHz = 80.5 TFLOP/s FP32)
-    st, tf32, fp32 = g.gemm_f32_measure_peaks()
+    # flops x 2.07 GHz = 80.5 TFLOP/s FP32), SM clocks at most the maximum
+    # (2070 MHz, a little slack for the two clocks' rounding), and the FP32
+    # rate within 10 % of what 128 lanes per SM give at the clock it reports
+    st, tf32, fp32, tf32_mhz, fp32_mhz = g.gemm_f32_measure_peaks()
     assert st == g.OK, g.gemm_f32_status_string(st)
     assert 550.0 < tf32 < 2200.0, tf32
     assert 40.0 < fp32 < 161.0, fp32
+    assert 500.0 < tf32_mhz < 2100.0 and 500.0 < fp32_mhz < 2100.0, (tf32_mhz, fp32_mhz)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    at_clock = sms * 128 * 2 * fp32_mhz * 1e6 / 1e12
+    assert 0.9 * at_clock < fp32 < 1.1 * at_clock, (fp32, at_clock)
 
 
 def test_bounded_wait_times_out_cleanly(g):
@@ -318,6 +324,32 @@ def test_bounded_wait_times_out_cleanly(g):
     c, _ = run(g, a, b, "exact", "tc_tma")
     c64, s = oracle.gemm(a, b)
     check_within_bound(c, c64, s, 64, "exact", "after timeout self-test")
+
+
+@pytest.mark.parametrize("mode", ["exact", "tf32"])
+def test_pair_kernel_abort_path(g, mode):
+    # the pair kernel's producers stop after one k-block, so its other roles'
+    # waits (limit 20 ms) run out: the kernel must report the timeout, let
+    # what it issued finish, free TMEM and return, leaving the context usable
+    m, n, k = 512, 512, 256  # four 256 x 256 tiles, each whole on one pair
+    a, b = operands(m, n, k, "uniform", seed=11)
+    da, db = to_dev(a), to_dev(b)
+    dc = torch.zeros((m, n), device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    st = g.gemm_f32_selftest_stalled_gemm(m, n, k, da.data_ptr(), k, db.data_ptr(), n,
+                                          dc.data_ptr(), n, g.MODES[mode], 20_000_000, s)
+    assert st == g.ERR_TIMEOUT, g.gemm_f32_status_string(st)
+    assert g.gemm_f32_poll_device_status(s) == g.OK
+    # a problem with split tiles (512 x 512 x 4096: every tile split in both
+    # modes) is refused before anything runs: it would need a workspace
+    la = torch.zeros((m, 4096), device="cuda")
+    lb = torch.zeros((4096, n), device="cuda")
+    assert g.gemm_f32_selftest_stalled_gemm(m, n, 4096, la.data_ptr(), 4096, lb.data_ptr(), n,
+                                            dc.data_ptr(), n, g.MODES[mode], 20_000_000,
+                                            s) == g.ERR_INVALID_ARG
+    c, _ = run(g, a, b, mode, "tc_tma")
+    c64, sc = oracle.gemm(a, b)
+    check_within_bound(c, c64, sc, k, mode, f"{mode} after the stalled pair kernel")
 
 
 # ---------------------------------------------------------- full sizes --
@@ -344,12 +376,13 @@ def test_config_full_comparison(g, cfg, mode):
     check_within_bound(out, c64, s, c["K"], mode, f"{cfg} {mode}")
 
 
-@pytest.mark.parametrize("mode", ["exact", "tf32"])
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("cfg", ["c4", "c5b"])
 def test_config_full_size(g, cfg, mode):
     # full-size workload in the benchmark's launch configuration (dense leading
     # dimensions, default kernel choice, torch's current stream), every element
-    # against the fp64 oracle
+    # against the fp64 oracle; exact_simt is the FP32 FMA kernel the benchmark
+    # also times at 4096^3
     a, b, c = config_operands(cfg)
     out, _ = run(g, a, b, mode)
     assert np.isfinite(out).all()
