@@ -182,12 +182,12 @@ def gemm_f32_selftest_stalled_gemm(M, N, K, A, lda, B, ldb, C, ldc, mode, timeou
 
 SCHEDULE_KINDS = {"exact_pair": 0, "tf32_pair": 1, "exact_lsu": 2, "tf32_lsu": 3}
 SCHEDULE_STATS = ("tiles", "k_blocks", "whole_tiles", "sk_share", "sk_clusters", "splits",
-                  "max_parts", "clusters")
+                  "max_parts", "clusters", "cluster_split")
 
 
 def gemm_f32_schedule_check(m: int, n: int, k: int, workers: int, kind):
     """Host-only check of the tile schedule (no GPU): (status, stats dict)."""
-    stats = (ctypes.c_int64 * 8)()
+    stats = (ctypes.c_int64 * len(SCHEDULE_STATS))()
     kind = SCHEDULE_KINDS[kind] if isinstance(kind, str) else int(kind)
     st = _load().gemm_f32_schedule_check(m, n, k, workers, kind, stats)
     return st, dict(zip(SCHEDULE_STATS, list(stats)))

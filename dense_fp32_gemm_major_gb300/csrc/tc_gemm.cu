@@ -70,6 +70,7 @@ constexpr int kTM = 256;        // rows of C per tile   (MMA N)
 constexpr int kTN = 128;        // columns of C per tile (MMA M = TMEM lanes)
 constexpr int kUmmaK = 8;       // K per tcgen05.mma of kind::tf32
 constexpr int kGroupM = 8;      // m-blocks per raster group
+constexpr int kClusterSplitMax = 4;  // pairs per cluster: 8 CTAs, the portable cluster size
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 0;    // D: columns [0, 256) (and [256, 512) when double-buffered)
 constexpr uint32_t kBtCol = 256;   // B^T stage buffers from column 256 (B stored K x N)
@@ -107,6 +108,11 @@ struct TcParams {
   // copy after this many k-blocks, so the other roles' bounded waits run out
   // and the abort path runs. -1 (never stop) in every other launch.
   int stall_kb;
+  // Pair kernels on problems with fewer unit tiles than CTA pairs: ks > 1
+  // pairs of one cluster share each unit tile, pair q of the cluster taking
+  // the q-th of ks contiguous k-slices, and sum their partial tiles through
+  // distributed shared memory (cluster_split_sum). 1 otherwise.
+  int ks;
 };
 
 // One unit of work of a CTA: k-blocks [kb0, kb1) of unit tile `tile`.
@@ -227,6 +233,20 @@ struct UnitIter {
   __device__ explicit UnitIter(const TcParams &p)
       : UnitIter(p, static_cast<int>(blockIdx.x) / p.cl, static_cast<int>(gridDim.x) / p.cl) {}
   __host__ __device__ bool next(const TcParams &p, WorkUnit &u) {
+    if (p.ks > 1) {
+      // One k-slice of one unit tile: pair c takes slice c % ks of tile c / ks.
+      if (dp_next < 0) return false;
+      const int q = c % p.ks;
+      u.tile = c / p.ks;
+      u.kb0 = (q * p.num_k_blocks) / p.ks;
+      u.kb1 = ((q + 1) * p.num_k_blocks) / p.ks;
+      u.sk_tile = -1;
+      u.part = q;
+      u.nparts = p.ks;
+      u.slot = -1;
+      dp_next = -1;
+      return true;
+    }
     if (dp_next < p.dp_tiles) {
       u.tile = dp_next;
       u.kb0 = 0;
@@ -257,6 +277,7 @@ struct UnitIter {
   }
   // True when no unit follows the one last returned by next().
   __host__ __device__ bool done(const TcParams &p) const {
+    if (p.ks > 1) return dp_next < 0;
     return dp_next >= p.dp_tiles && sk_pos >= sk_end;
   }
 };
@@ -335,6 +356,117 @@ __device__ __forceinline__ void epilogue_fixup(const TcParams &p, int sk_tile, u
         *reinterpret_cast<float4 *>(dst) = v;
       } else {
         const float e[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (gn + i < N) dst[i] = beta != 0.0f ? alpha * e[i] + beta * dst[i] : alpha * e[i];
+      }
+    }
+  }
+}
+
+// float4s per thread and partial in flight in cluster_split_sum (a probe
+// read 96 KiB from three other SMs' shared memory in 2.7 us with 8, 4.2 us
+// with 4 and 4.4 us with 1; inside the GEMM 4 and 8 time the same).
+constexpr int kClusterSumBatch = 8;
+
+// Shared::cluster address of `addr` (this CTA's shared memory) in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  return remote;
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// The final sum of a cluster-split tile (TcParams::ks > 1), run by all
+// nthreads threads of every CTA once each CTA's k-slice partial sits in its
+// shared memory at part ([m][n], kTN floats per row) and a cluster barrier
+// has made them visible. The CTAs of rank r (0, 1) in the ks pairs hold the
+// same 128 n x 256 m output tile; pair q's CTA sums m rows [q kTM / ks,
+// (q + 1) kTM / ks) of it over the ks partials, added in pair order 0 .. ks-1
+// (so results do not depend on timing), scales by alpha, adds beta C and
+// stores C with row and column guards. Its own partial is read from shared
+// memory, the others through distributed shared memory, BATCH float4s per
+// thread and partial in flight (the sum is bound by the latency of those
+// reads).
+template <int BATCH>
+__device__ __forceinline__ void cluster_split_sum(const TcParams &p, const float *part,
+                                                  uint32_t crank, int tid, int nthreads) {
+  const int ks = p.ks;
+  const uint32_t r = crank & 1u, q = crank >> 1;
+  int mb, nb;
+  tile_coords(p, (static_cast<int>(blockIdx.x) >> 1) / ks, r, mb, nb);
+  const int row0 = (static_cast<int>(q) * kTM) / ks, row1 = ((static_cast<int>(q) + 1) * kTM) / ks;
+  constexpr int kRowVec = kTN / 4;
+  const int nvec = (row1 - row0) * kRowVec;
+  const float4 *local = reinterpret_cast<const float4 *>(part) + row0 * kRowVec;
+  const uint32_t base = smem_addr(local);
+  const int M = p.M, N = p.N;
+  const long long ldc = p.ldc;
+  float *__restrict__ const C = p.C;
+  const float alpha = p.alpha, beta = p.beta;
+  const bool vec_ok = (ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0);
+#pragma unroll 1
+  for (int f0 = tid; f0 < nvec; f0 += nthreads * BATCH) {
+    float4 acc[BATCH];
+#pragma unroll
+    for (int j = 0; j < kClusterSplitMax; ++j) {
+      if (j >= ks) break;
+      float4 v[BATCH];
+      if (static_cast<uint32_t>(j) == q) {
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+          const int f = f0 + b * nthreads;
+          v[b] = f < nvec ? local[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      } else {
+        const uint32_t src = cluster_map(base, 2u * static_cast<uint32_t>(j) + r);
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+          const int f = f0 + b * nthreads;
+          v[b] = f < nvec ? ld_cluster_f4(src + static_cast<uint32_t>(f) * 16u)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < BATCH; ++b) {
+        if (j == 0) {
+          acc[b] = v[b];
+        } else {
+          acc[b].x += v[b].x;
+          acc[b].y += v[b].y;
+          acc[b].z += v[b].z;
+          acc[b].w += v[b].w;
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+      const int f = f0 + b * nthreads;
+      if (f >= nvec) continue;
+      const int gm = mb * kTM + row0 + f / kRowVec, gn = nb * kTN + (f % kRowVec) * 4;
+      if (gm >= M) continue;
+      float *dst = C + static_cast<long long>(gm) * ldc + gn;
+      if (vec_ok && gn + 3 < N) {
+        float4 o = make_float4(alpha * acc[b].x, alpha * acc[b].y, alpha * acc[b].z,
+                               alpha * acc[b].w);
+        if (beta != 0.0f) {
+          const float4 c = *reinterpret_cast<const float4 *>(dst);
+          o.x += beta * c.x;
+          o.y += beta * c.y;
+          o.z += beta * c.z;
+          o.w += beta * c.w;
+        }
+        *reinterpret_cast<float4 *>(dst) = o;
+      } else {
+        const float e[4] = {acc[b].x, acc[b].y, acc[b].z, acc[b].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           if (gn + i < N) dst[i] = beta != 0.0f ? alpha * e[i] + beta * dst[i] : alpha * e[i];
@@ -489,14 +621,18 @@ __device__ __forceinline__ void stage_cols_lsu(uint8_t *tile, int lo_offset, con
 // of the CTA's work list out of TMEM (lane = n, column = m) and either store
 // it to C or, for a part of a split tile, to its partial-sum slot; the last
 // part to finish sums all parts in order. PAIR: the accumulator's empty
-// barrier belongs to the even CTA of the pair, which issues the MMAs of both.
-template <int ACC_BUFS, int EPI_WARP0, bool PAIR, class Shared>
+// barrier belongs to the even CTA of the pair (cluster rank pb), which issues
+// the MMAs of both. CS (cluster split): the CTA's one accumulator is a k-slice
+// of a tile shared by the pairs of its cluster; it goes to this CTA's shared
+// memory at part_smem ([m][n], kTN floats per row) for cluster_split_sum.
+template <int ACC_BUFS, int EPI_WARP0, bool PAIR, bool CS = false, class Shared>
 __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uint32_t tmem,
                                               uint32_t warp, uint32_t lane, uint32_t rank,
-                                              volatile int *abort) {
-  auto release_acc = [](uint64_t *bar) {
+                                              volatile int *abort, uint32_t pb = 0,
+                                              float *part_smem = nullptr) {
+  auto release_acc = [pb](uint64_t *bar) {
     if (PAIR)
-      mbar_arrive_cluster(bar, 0);
+      mbar_arrive_cluster(bar, pb);
     else
       mbar_arrive(bar);
   };
@@ -515,7 +651,23 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
     const int gn = nb * kTN + n_loc;
     const bool n_ok = gn < p.N;
     const uint32_t t_lane = tmem + ((quad * 32) << 16) + kAccCol + acc * kTM;
-    if (u.nparts == 1) {
+    if constexpr (CS) {
+      float *dst = part_smem + n_loc;
+#pragma unroll 1
+      for (int c = 0; c < kTM / 32; c += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_load_32cols(t_lane + c * 32, r0);
+        tmem_load_32cols(t_lane + (c + 1) * 32, r1);
+        tmem_load_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[(c * 32 + j) * kTN] = __uint_as_float(r0[j]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dst[(c * 32 + 32 + j) * kTN] = __uint_as_float(r1[j]);
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) release_acc(&sh->acc_empty[acc]);
+    } else if (u.nparts == 1) {
       // Whole tile: straight to C, two 32-column chunks per TMEM load wait.
       auto store_chunk = [&](int c, const uint32_t (&r)[32]) {
         const int gm0 = mb * kTM + c * 32;
@@ -861,7 +1013,11 @@ __device__ __forceinline__ void pair_load_operand(uint8_t *dst, const CUtensorMa
   }
 }
 
-template <int BK, int STAGES, bool OPA, bool OPB>
+//
+// CS: a cluster holds p.ks pairs that share one unit tile (TcParams::ks);
+// the pair of a CTA is its cluster rank with bit 0 cleared (pb), and its rank
+// within the pair is bit 0.
+template <int BK, int STAGES, bool OPA, bool OPB, bool CS = false>
 __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
     tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
@@ -874,7 +1030,10 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
 
   const uint32_t warp = warp_index();
   const uint32_t lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t rank = CS ? (crank & 1u) : crank;  // rank within the pair
+  const uint32_t pb = CS ? (crank & ~1u) : 0u;      // cluster rank of the pair's even CTA
+  const uint16_t pair_mask = static_cast<uint16_t>(3u << pb);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -928,7 +1087,7 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
             break;
           }
           uint8_t *st = tiles + stage * Cfg::kStageBytes;
-          const uint32_t bar = mbar_cluster_addr(&sh->full[stage], 0);
+          const uint32_t bar = mbar_cluster_addr(&sh->full[stage], pb);
           if (rank == 0) mbar_arrive_expect_tx(&sh->full[stage], 2 * Cfg::kStageBytes);
           pair_load_operand<BK, OPA>(st + Cfg::kAOffset, &tmap_a, bar, m0, kb * BK,
                                      p.a_one_copy != 0);
@@ -977,27 +1136,28 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
             mma_tf32<2>(d_tmem, pair_operand_desc<BK, !OPB>(st + Cfg::kBtOffset, kk),
                         pair_operand_desc<BK, OPA>(st + Cfg::kAOffset, kk), Cfg::kIdesc,
                         (kb != u.kb0 || kk != 0) ? 1u : 0u);
-          mma_commit_multicast<2>(&sh->empty[stage], 3);
+          mma_commit_multicast<2>(&sh->empty[stage], pair_mask);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        mma_commit_multicast<2>(&sh->acc_full[acc], 3);
+        mma_commit_multicast<2>(&sh->acc_full[acc], pair_mask);
         if (++acc == Cfg::kAccBufs) {
           acc = 0;
           acc_phase ^= 1;
         }
       }
       // Every MMA this thread issued completes before TMEM is released.
-      mma_commit_multicast<2>(&sh->drain, 1);
+      mma_commit_multicast<2>(&sh->drain, static_cast<uint16_t>(1u << pb));
       drain_wait(&sh->drain, 0, p.timeout_ns);
     }
     __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue --
-    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, true>(p, sh, tmem, warp, lane, rank, abort);
+    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, true, CS>(p, sh, tmem, warp, lane, rank, abort, pb,
+                                                          reinterpret_cast<float *>(tiles));
   }
 
   // Neither CTA frees its TMEM or leaves while the pair's MMAs, copies or
@@ -1008,6 +1168,15 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
   if (warp == Cfg::kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc<2>(tmem, kTmemCols);
+  }
+  if constexpr (CS) {
+    // Every CTA's k-slice partial is in its shared memory (the barrier above
+    // orders the epilogue's stores): sum them, then keep this CTA's shared
+    // memory alive until the other CTAs of the cluster have read it.
+    if (!sh->abort)
+      cluster_split_sum<kClusterSumBatch>(p, reinterpret_cast<const float *>(tiles), crank,
+                                          threadIdx.x, blockDim.x);
+    cluster_sync();
   }
   if (sh->fix_tile >= 0 && !sh->abort) {
     __threadfence();
@@ -1117,7 +1286,8 @@ struct RingPos {
   }
 };
 
-template <int BK, int AST, int BST, int XW, bool OPB>
+// CS: as for tc_pair_kernel, p.ks pairs per cluster share one unit tile.
+template <int BK, int AST, int BST, int XW, bool OPB, bool CS = false>
 __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThreads, 1)
     tc_pair_exact_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
@@ -1131,7 +1301,10 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
 
   const uint32_t warp = warp_index();
   const uint32_t lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t rank = CS ? (crank & 1u) : crank;  // rank within the pair
+  const uint32_t pb = CS ? (crank & ~1u) : 0u;      // cluster rank of the pair's even CTA
+  const uint16_t pair_mask = static_cast<uint16_t>(3u << pb);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < AST; ++s) {
@@ -1265,20 +1438,20 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
             mma_tf32_ts<2>(d_tmem, bt_hi + kk * kUmmaK, da_lo, Cfg::kIdesc, 1);
             mma_tf32_ts<2>(d_tmem, bt_hi + kk * kUmmaK, da, Cfg::kIdesc, 1);
           }
-          mma_commit_multicast<2>(&sh->empty[a.idx], 3);
-          mma_commit_multicast<2>(&sh->tfree[t.idx], 3);
+          mma_commit_multicast<2>(&sh->empty[a.idx], pair_mask);
+          mma_commit_multicast<2>(&sh->tfree[t.idx], pair_mask);
           a.next();
           t.next();
         }
         if (!ok) break;
-        mma_commit_multicast<2>(&sh->acc_full[acc], 3);
+        mma_commit_multicast<2>(&sh->acc_full[acc], pair_mask);
         if (++acc == Cfg::kAccBufs) {
           acc = 0;
           acc_phase ^= 1;
         }
       }
       // Every MMA this thread issued completes before TMEM is released.
-      mma_commit_multicast<2>(&sh->drain, 1);
+      mma_commit_multicast<2>(&sh->drain, static_cast<uint16_t>(1u << pb));
       drain_wait(&sh->drain, 0, p.timeout_ns);
     } else if (rank == 1 && lane == 0) {
       // ---------------------------------------------- relay (odd CTA) --
@@ -1295,7 +1468,7 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
             ok = false;
             break;
           }
-          mbar_arrive_cluster(&sh->ready[t.idx], 0);
+          mbar_arrive_cluster(&sh->ready[t.idx], pb);
           t.next();
         }
       }
@@ -1303,7 +1476,8 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
     __syncwarp();
   } else if (warp < Cfg::kEpiWarp0 + 4) {
     // --------------------------------------------------------- epilogue --
-    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, true>(p, sh, tmem, warp, lane, rank, abort);
+    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, true, CS>(p, sh, tmem, warp, lane, rank, abort, pb,
+                                                          reinterpret_cast<float *>(tiles));
   } else {
     // --------------------------------------------------------- transform --
     // Warp (quad, part) moves k in [part * W, (part + 1) * W), W = BK / parts,
@@ -1404,6 +1578,12 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
   if (warp == Cfg::kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc<2>(tmem, kTmemCols);
+  }
+  if constexpr (CS) {
+    if (!sh->abort)
+      cluster_split_sum<kClusterSumBatch>(p, reinterpret_cast<const float *>(tiles), crank,
+                                          threadIdx.x, blockDim.x);
+    cluster_sync();
   }
   if (sh->fix_tile >= 0 && !sh->abort) {
     __threadfence();
@@ -1629,9 +1809,11 @@ Schedule schedule_for(const TcParams &p, int workers, int bk, bool exact, bool p
 
 // The kernel a launch plan runs: tc_lsu_kernel, or with PAIR a CTA-pair
 // kernel.
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST, bool PAIR>
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST, bool PAIR,
+          bool CS = false>
 struct KernelOf {
-  static_assert(LSU && CL == 1 && BST == 0, "tc_lsu_kernel: plain-load producers, one SM per tile");
+  static_assert(LSU && CL == 1 && BST == 0 && !CS,
+                "tc_lsu_kernel: plain-load producers, one SM per tile");
   using Cfg = TcConfig<BK, STAGES, EXACT, OPB>;
   static constexpr int kThreads = Cfg::kThreads;
   static constexpr int kSmemBytes =
@@ -1639,44 +1821,73 @@ struct KernelOf {
   static constexpr auto kernel = tc_lsu_kernel<BK, STAGES, EXACT, OPB, OPA>;
 };
 
-template <int BK, int STAGES, bool OPA, bool OPB>
+template <int BK, int STAGES, bool OPA, bool OPB, bool CS>
 struct PairTf32Kernel {
   using Cfg = PairConfig<BK, STAGES, OPA, OPB>;
+  static_assert(Cfg::kTileBytes >= kTM * kTN * 4, "a cluster-split partial fits the stages");
   static constexpr int kThreads = Cfg::kThreads;
   static constexpr int kSmemBytes =
       Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
-  static constexpr auto kernel = tc_pair_kernel<BK, STAGES, OPA, OPB>;
+  static constexpr auto kernel = tc_pair_kernel<BK, STAGES, OPA, OPB, CS>;
 };
 
 // Transform warps per CTA of the 3xTF32 pair kernel (16 time the same).
 constexpr int kPairExactXform = 8;
 
-template <int BK, int AST, int BST, int XW, bool OPB>
+template <int BK, int AST, int BST, int XW, bool OPB, bool CS>
 struct PairExactKernel {
   using Cfg = PairExactConfig<BK, AST, BST, XW, OPB>;
+  static_assert(Cfg::kBRingOffset >= kTM * kTN * 4, "a cluster-split partial fits the A ring");
   static constexpr int kThreads = Cfg::kThreads;
   static constexpr int kSmemBytes =
       Cfg::kTileBytes +
       static_cast<int>(sizeof(PairExactShared<AST, BST, Cfg::kTmemSlots>)) + 1024;
-  static constexpr auto kernel = tc_pair_exact_kernel<BK, AST, BST, XW, OPB>;
+  static constexpr auto kernel = tc_pair_exact_kernel<BK, AST, BST, XW, OPB, CS>;
 };
 
 // PAIR: the CTA-pair kernels, one TF32 pass (every layout) or 3xTF32 (A
 // stored M x K, B in either storage).
 // With EXACT, STAGES counts A stages and BST the B slots.
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST>
-struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true>
-    : std::conditional_t<EXACT, PairExactKernel<BK, STAGES, BST, kPairExactXform, OPB>,
-                         PairTf32Kernel<BK, STAGES, OPA, OPB>> {
+// CS: the cluster-split variant (TcParams::ks pairs per cluster and tile).
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST, bool CS>
+struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true, CS>
+    : std::conditional_t<EXACT, PairExactKernel<BK, STAGES, BST, kPairExactXform, OPB, CS>,
+                         PairTf32Kernel<BK, STAGES, OPA, OPB, CS>> {
   static_assert(!LSU && CL == 2 && (EXACT ? BST > 0 : BST == 0), "the pair kernels are fed by TMA");
   static_assert(!EXACT || !OPA, "3xTF32 pairs: A stored M x K");
 };
 
-// Everything a launch needs except the stream-K workspace.
+// Cluster split (TcParams::ks): worth it only when the k range each pair no
+// longer computes, kb (1 - 1 / ks), outweighs the exchange of partial tiles
+// (a per-CTA timeline at 512^3 and 1024^3: 1.6 us to move the accumulator to
+// shared memory, 3-5 us to read 64-96 KiB of partials from the other CTAs,
+// which distributed shared memory serves at 22-36 GB/s per SM, and two cluster
+// barriers): at least 256 k of 3xTF32 work (about 6 us per pair) or 768 k of
+// one TF32 pass.
+constexpr int kClusterSplitSavedKExact = 256;
+constexpr int kClusterSplitSavedKTf32 = 768;
+
+// Pairs per unit tile for a problem of `tiles` unit tiles of kb k-blocks on
+// `pairs` CTA pairs: as many as there are pairs per tile, up to
+// kClusterSplitMax, if that saves enough k per pair; < 2 means no cluster
+// split (the stream-K schedule applies). Host and device code.
+__host__ __device__ inline int cluster_split_ks(int tiles, int kb, int pairs, int bk, bool exact) {
+  int ks = pairs / (tiles > 0 ? tiles : 1);
+  if (ks > kClusterSplitMax) ks = kClusterSplitMax;
+  if (ks > kb) ks = kb;
+  if (ks < 2) return 1;
+  const long long saved_k = static_cast<long long>(kb) * bk * (ks - 1) / ks;
+  return saved_k >= (exact ? kClusterSplitSavedKExact : kClusterSplitSavedKTf32) ? ks : 1;
+}
+
+// Everything a launch needs except the stream-K workspace. CS: the
+// cluster-split launch of a pair kernel; prepare() sets p.ks = 1 when the
+// problem does not take it, and the caller then launches the plain plan.
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
-          int BST = 0, bool PAIR = false>
+          int BST = 0, bool PAIR = false, bool CS = false>
 struct LaunchPlan {
-  using K = KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR>;
+  static_assert(!CS || PAIR, "cluster split: pair kernels only");
+  using K = KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, CS>;
   TcParams p;
   Schedule sch;
   CUtensorMap map_a, map_b;
@@ -1745,6 +1956,51 @@ struct LaunchPlan {
     // Generous: a stage takes microseconds; one tile's mainloop about K * 25 ns.
     p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
     p.stall_kb = -1;
+    p.ks = 1;
+    p.sk_partials = nullptr;
+    p.sk_counters = nullptr;
+    if constexpr (CS) {
+      // ks pairs per unit tile, if the problem has few enough tiles and all
+      // its clusters of 2 ks CTAs can be resident at once (checked once per
+      // device and ks).
+      int ks = cluster_split_ks(p.num_tiles, p.num_k_blocks, sm_count / 2, BK, EXACT);
+      static int fits[64][kClusterSplitMax + 1] = {};
+      static std::mutex fits_mu;
+      for (; ks >= 2; --ks) {
+        std::lock_guard<std::mutex> g(fits_mu);
+        if (fits[dev][ks] == 0) {
+          cudaLaunchConfig_t qc = {};
+          qc.gridDim = dim3(2 * ks, 1, 1);
+          qc.blockDim = dim3(K::kThreads, 1, 1);
+          qc.dynamicSmemBytes = smem_bytes;
+          cudaLaunchAttribute attr[1];
+          attr[0].id = cudaLaunchAttributeClusterDimension;
+          attr[0].val.clusterDim.x = 2 * ks;
+          attr[0].val.clusterDim.y = 1;
+          attr[0].val.clusterDim.z = 1;
+          qc.attrs = attr;
+          qc.numAttrs = 1;
+          int clusters = 0;
+          if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &qc) != cudaSuccess) {
+            cudaGetLastError();
+            clusters = 0;
+          }
+          fits[dev][ks] = clusters > 0 ? clusters : -1;
+        }
+        if (fits[dev][ks] >= p.num_tiles) break;
+      }
+      if (ks < 2) return kOk;  // p.ks == 1: not taken
+      p.ks = ks;
+      sch.grid = p.num_tiles * ks;  // pairs
+      sch.dp_tiles = 0;
+      sch.sk_share = 1;
+      sch.sk_ctas = 0;
+      sch.splits = false;
+      p.dp_tiles = 0;
+      p.sk_share = 1;
+      p.sk_ctas = 0;
+      return kOk;
+    }
     // Workers: clusters that can be resident at once (the placement of CTA
     // pairs may leave some SMs unpaired).
     static int workers_cached[64] = {};
@@ -1775,8 +2031,6 @@ struct LaunchPlan {
     p.dp_tiles = sch.dp_tiles;
     p.sk_share = sch.sk_share;
     p.sk_ctas = sch.sk_ctas;
-    p.sk_partials = nullptr;
-    p.sk_counters = nullptr;
     const int split_tiles = p.num_tiles - p.dp_tiles;
     if (split_tiles > 0 && sch.splits) {
       counter_bytes = (static_cast<size_t>(split_tiles) * CL * 4 + 255) / 256 * 256;
@@ -1799,7 +2053,7 @@ struct LaunchPlan {
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.x = CS ? CL * p.ks : CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -1844,6 +2098,13 @@ int workspace_pool(int dev, cudaMemPool_t *out) {
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
           int BST = 0, bool PAIR = false>
 int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
+  if constexpr (PAIR) {
+    // Few unit tiles: pairs of one cluster share each tile (no workspace).
+    LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, true> cs;
+    const int cst = cs.prepare(a, sm_count);
+    if (cst != kOk) return cst;
+    if (cs.p.ks > 1) return cs.launch(stream);
+  }
   LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR> plan;
   int st = plan.prepare(a, sm_count);
   if (st != kOk) return st;
@@ -2129,6 +2390,13 @@ int launch_variant_noalloc(const GemmArgs &a, int sm_count, cudaStream_t stream)
   void *scratch = nullptr;
   int st = noalloc_scratch(dev, &scratch);
   if (st != kOk) return st;
+  if constexpr (PAIR) {
+    // A cluster split needs no workspace at all.
+    LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, false, BST, PAIR, true> cs;
+    st = cs.prepare(a, sm_count);
+    if (st != kOk) return st;
+    if (cs.p.ks > 1) return cs.launch(stream);
+  }
   LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, false, BST, PAIR> plan;
   st = plan.prepare(a, sm_count);
   if (st != kOk) return st;
@@ -2181,8 +2449,42 @@ extern "C" int gemm_f32_schedule_check(int64_t M, int64_t N, int64_t K, int64_t 
   const int bk = kernel_kind == 0 ? kPairExactBK : (kernel_kind == 2 ? 16 : 32);
   TcParams p = {};
   set_tiles(p, M, N, K, bk, pair ? 2 : 1);
+  p.ks = 1;
   const int64_t cells = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
   if (cells > (int64_t{1} << 26)) return GEMM_ERR_INVALID_ARG;  // keep the check's memory small
+  const int ks = pair ? cluster_split_ks(p.num_tiles, p.num_k_blocks, static_cast<int>(workers), bk,
+                                         exact)
+                      : 1;
+  if (ks >= 2) {
+    // Cluster split: pair c takes k-slice c % ks of unit tile c / ks; the
+    // slices of a tile cover its k range once, in pair order, none empty.
+    p.ks = ks;
+    const int kb = p.num_k_blocks, pairs = p.num_tiles * ks;
+    std::vector<int> next_kb(static_cast<size_t>(p.num_tiles), 0);
+    for (int c = 0; c < pairs; ++c) {
+      UnitIter it(p, c, pairs);
+      WorkUnit u;
+      if (!it.next(p, u)) return 23;  // a pair without work
+      if (u.tile < 0 || u.tile >= p.num_tiles || u.kb0 >= u.kb1 || u.kb1 > kb) return 10;
+      if (u.part != c % ks || u.nparts != ks) return 14;
+      int &at = next_kb[static_cast<size_t>(u.tile)];
+      if (u.kb0 != at) return at > u.kb0 ? 11 : 20;  // covered twice / k-block missed
+      at = u.kb1;
+      if (it.next(p, u) || !it.done(p)) return 19;  // more than one unit
+    }
+    for (int t = 0; t < p.num_tiles; ++t)
+      if (next_kb[static_cast<size_t>(t)] != kb) return 20;
+    stats[0] = p.num_tiles;
+    stats[1] = kb;
+    stats[2] = 0;
+    stats[3] = 0;
+    stats[4] = 0;
+    stats[5] = 0;
+    stats[6] = ks;
+    stats[7] = pairs;
+    stats[8] = ks;
+    return GEMM_OK;
+  }
   const Schedule sch = schedule_for(p, static_cast<int>(workers), bk, exact, pair);
   p.dp_tiles = sch.dp_tiles;
   p.sk_share = sch.sk_share;
@@ -2239,5 +2541,6 @@ extern "C" int gemm_f32_schedule_check(int64_t M, int64_t N, int64_t K, int64_t 
   stats[5] = sch.splits ? 1 : 0;
   stats[6] = max_parts;
   stats[7] = clusters;
+  stats[8] = 1;
   return GEMM_OK;
 }

@@ -352,14 +352,22 @@ typedef enum {
  *   - the parts of a split tile are numbered 0 .. nparts - 1 in k order, at
  *     most 8 of them;
  *   - each part's partial-sum slot belongs to its own cluster and no slot is
- *     shared.
+ *     shared;
+ *   - for the pair kinds, when there are at most half as many unit tiles as
+ *     pairs (the cluster split: 2 to 4 pairs of one cluster take contiguous
+ *     k-slices of one unit tile and sum them in shared memory, with no
+ *     workspace), that each pair has exactly one non-empty slice and the
+ *     slices of a tile follow each other in pair order. (On a GPU the
+ *     library also lowers the pairs per tile until all the clusters fit on
+ *     the device at once, which this host-only check cannot see.)
  *   M, N, K     >= 1 and below 2^31; tiles x k-blocks at most 2^26
  *   workers     1 .. 4096
  *   kind        a gemm_f32_schedule_kind
- *   stats       host array of 8 int64 (written on success): unit tiles,
+ *   stats       host array of 9 int64 (written on success): unit tiles,
  *               k-blocks per tile, whole tiles, stream-K share, stream-K
- *               clusters, 1 if some tile is split, most parts of one tile,
- *               clusters launched
+ *               clusters, 1 if some tile is split through the workspace,
+ *               most parts of one tile, clusters (pairs or SMs) launched,
+ *               pairs per tile in a cluster split (1: none)
  * Returns GEMM_OK; GEMM_ERR_INVALID_ARG for bad arguments; otherwise a code
  * from 10 up that names the check that failed (see its definition).
  */

@@ -220,7 +220,7 @@ def test_headers_compile_and_link_as_c(gemm_lib, tmp_path):
 #include "gemm_f32.h"
 #include "reduce_f32.h"
 int main(void) {
-  int64_t stats[8];
+  int64_t stats[9];
   int st = gemm_f32_schedule_check(4096, 4096, 4096, 76, GEMM_SCHEDULE_EXACT_PAIR, stats);
   int sel = gemm_f32_select(64, 64, 64, (const float *)0x10000000, 64,
                             (const float *)0x20000000, 64, (float *)0x30000000, 64,

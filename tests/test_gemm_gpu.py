@@ -184,10 +184,15 @@ def test_ragged_sweep(g):
     (512, 512, 1024),     # 4 pair tiles, each split (3xTF32)
     (200, 100, 8000),     # one ragged tile, split in both modes
     (512, 512, 4096),     # 8 tiles, each split in both modes
+    (2048, 1280, 2048),   # 40 pair tiles on 76 pairs: every tile split through the
+                          # workspace (3xTF32; tf32: dealt whole)
+    (1280, 2048, 8192),   # 40 pair tiles, split in both modes
 ])
 def test_stream_k_splits(g, mode, kernel, m, n, k):
     # tiles whose k range is shared by several CTAs: partial sums through the
-    # workspace, summed by the last contributor in part order
+    # workspace, summed by the last contributor in part order (the TMA-fed
+    # pair kernels split tiles inside a cluster instead when there are at most
+    # half as many tiles as pairs, which the small shapes here exercise)
     a, b = operands(m, n, k, "normal", seed=m + 3 * n + k)
     c, _ = run(g, a, b, mode, kernel)
     rows = np.unique(np.concatenate([np.arange(0, m, max(1, m // 97)), [m - 1]]))
@@ -200,6 +205,37 @@ def test_stream_k_splits(g, mode, kernel, m, n, k):
     assert np.array_equal(ci[rows].astype(np.float64), ci64)
     c2, _ = run(g, a, b, mode, kernel)
     assert np.array_equal(c.view(np.uint32), c2.view(np.uint32)), "split tiles not deterministic"
+
+
+@pytest.mark.parametrize("mode,m,n,k", [
+    ("exact", 512, 512, 512),     # 4 tiles, 4 pairs per tile
+    ("exact", 1000, 1531, 776),   # 24 ragged tiles, 3 pairs per tile: clusters of 6
+    ("exact", 129, 257, 520),     # 2 ragged tiles, k not a multiple of the k-block
+    ("exact", 300, 700, 2000),    # 6 ragged tiles, k slices of unequal length
+    ("tf32", 300, 700, 2000),
+    ("exact", 1024, 1024, 1024),  # 16 tiles (4 pairs per tile if 16 clusters of 8 fit)
+    ("tf32", 1024, 1024, 1024),
+    ("tf32", 700, 300, 1100),     # 6 ragged tiles, ragged k
+    ("exact", 256, 128, 4096),    # one tile
+    ("tf32", 256, 128, 4096),
+])
+def test_cluster_split(g, mode, m, n, k):
+    # few unit tiles: pairs of one cluster take k-slices of a tile and sum
+    # them through distributed shared memory, in pair order
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    st, stats = g.gemm_f32_schedule_check(m, n, k, sms // 2, mode + "_pair")
+    assert st == g.OK and stats["cluster_split"] >= 2, stats
+    a, b = operands(m, n, k, "normal", seed=m + 7 * n + k)
+    c, full = run(g, a, b, mode, "tc_tma", ldc=n + 3, c_fill=-777.0)
+    c64, sc = oracle.gemm(a, b)
+    check_within_bound(c, c64, sc, k, mode, f"cluster split {mode} {m}x{n}x{k}")
+    assert np.all(full[:, n:] == -777.0), "write outside C's columns"
+    c2, _ = run(g, a, b, mode, "tc_tma", ldc=n + 3)
+    assert np.array_equal(c.view(np.uint32), c2.view(np.uint32)), "cluster split not deterministic"
+    ai = synth.small_integers((m, k), 17)
+    bi = synth.small_integers((k, n), 18)
+    ci, _ = run(g, ai, bi, mode, "tc_tma")
+    assert np.array_equal(ci.astype(np.float64), oracle.gemm(ai, bi)[0])
 
 
 def test_nan_prefilled_output_fully_written(g):

@@ -45,15 +45,39 @@ def test_benchmark_workloads_schedule(gemm_lib):
     st, s = gemm_lib.gemm_f32_schedule_check(4096, 4096, 4096, 76, "tf32_pair")
     assert st == gemm_lib.OK
     assert (s["whole_tiles"], s["splits"], s["max_parts"]) == (228, 1, 2)
-    # 512^3: 4 tiles of 16 k-blocks, too short to be worth splitting
+    # 512^3: 4 tiles of 16 k-blocks on 76 pairs: four pairs of one cluster
+    # share each tile (k-slices of 4 k-blocks), no workspace
     st, s = gemm_lib.gemm_f32_schedule_check(512, 512, 512, 76, "exact_pair")
     assert st == gemm_lib.OK
-    assert (s["tiles"], s["whole_tiles"], s["splits"]) == (4, 4, 0)
-    # one tile with a long k range: split over as many clusters as keep every
-    # chunk at least 256 k and at most 8 parts on the tile
-    st, s = gemm_lib.gemm_f32_schedule_check(256, 128, 4096, 76, "exact_pair")
+    assert (s["tiles"], s["cluster_split"], s["splits"], s["clusters"]) == (4, 4, 0, 16)
+    # 1024^3: 16 tiles of 32 k-blocks, slices of 8 in both modes
+    for kind in ("exact_pair", "tf32_pair"):
+        st, s = gemm_lib.gemm_f32_schedule_check(1024, 1024, 1024, 76, kind)
+        assert st == gemm_lib.OK
+        assert (s["tiles"], s["cluster_split"], s["clusters"]) == (16, 4, 64), kind
+    # 1000 x 1531 x 777: 24 tiles, three pairs per tile on 76 pairs
+    st, s = gemm_lib.gemm_f32_schedule_check(1000, 1531, 777, 76, "exact_pair")
     assert st == gemm_lib.OK
-    assert s["splits"] == 1 and 2 <= s["max_parts"] <= 8 and s["sk_share"] >= 8
+    assert (s["tiles"], s["cluster_split"], s["clusters"]) == (24, 3, 72)
+    # a split must save each pair at least 256 k of 3xTF32 work or 768 k of
+    # one TF32 pass: one TF32 pass at 512^3 (384 k saved at best) and
+    # 512 x 512 x 256 (192 k) are not split
+    st, s = gemm_lib.gemm_f32_schedule_check(512, 512, 512, 76, "tf32_pair")
+    assert st == gemm_lib.OK and s["cluster_split"] == 1
+    st, s = gemm_lib.gemm_f32_schedule_check(512, 512, 256, 76, "exact_pair")
+    assert st == gemm_lib.OK and s["cluster_split"] == 1
+    # 40 tiles on 76 pairs: more than half as many tiles as pairs, so the
+    # stream-K schedule applies (every tile split through the workspace)
+    st, s = gemm_lib.gemm_f32_schedule_check(2048, 1280, 2048, 76, "exact_pair")
+    assert st == gemm_lib.OK
+    assert (s["tiles"], s["cluster_split"], s["splits"], s["clusters"]) == (40, 1, 1, 76)
+    # one tile with a long k range: four pairs of one cluster
+    st, s = gemm_lib.gemm_f32_schedule_check(256, 128, 4096, 76, "exact_pair")
+    assert st == gemm_lib.OK and s["cluster_split"] == 4
+    # the plain-load kernel never splits within a cluster
+    st, s = gemm_lib.gemm_f32_schedule_check(256, 128, 4096, 152, "exact_lsu")
+    assert st == gemm_lib.OK
+    assert s["cluster_split"] == 1 and s["splits"] == 1 and 2 <= s["max_parts"] <= 8
 
 
 def test_schedule_check_rejects_bad_arguments(gemm_lib):

@@ -28,23 +28,29 @@ pytestmark = pytest.mark.gpu
 
 # (M, N, K, mode, lda padding, schedule kind). A pitch that is not a multiple
 # of 4 floats sends the call to the plain-load kernel (no operand copy may be
-# made without allocating). Workspace of each call on 76 CTA pairs (152 SMs):
-# 17.5, 17.5, 16, 19 and 8 MiB of partial tiles.
+# made without allocating). Each shape has more unit tiles than half the CTA
+# pairs, so its tiles are split through the workspace (problems with fewer
+# tiles split inside a cluster and need none). Workspace of each call on 76
+# CTA pairs (152 SMs): 38, 38, 38, 19 and 8 MiB of partial tiles.
 SEQUENCE = [
-    (512, 768, 2048, "exact", 0, "exact_pair"),    # 3xTF32 pairs, up to 7 parts a tile
-    (512, 768, 2048, "exact", 0, "exact_pair"),    # the same again: counters left counted up
-    (1024, 1024, 4096, "tf32", 0, "tf32_pair"),    # one TF32 pass on pairs, 2 parts a tile
+    (2048, 1280, 2048, "exact", 0, "exact_pair"),  # 3xTF32 pairs: 40 tiles, 3 parts each
+    (2048, 1280, 2048, "exact", 0, "exact_pair"),  # the same again: counters left counted up
+    (1280, 2048, 8192, "tf32", 0, "tf32_pair"),    # one TF32 pass on pairs, 3 parts a tile
     (1000, 1531, 777, "exact", 0, "exact_lsu"),    # lda 777: plain-load 3xTF32 kernel
-    (512, 512, 1024, "exact", 0, "exact_pair"),
+    (2560, 2048, 1024, "exact", 0, "exact_pair"),  # a full wave whole, the rest split
+    (1024, 1024, 1024, "exact", 0, "exact_pair_cs"),  # 16 tiles: split inside clusters,
+    (1024, 1024, 1024, "tf32", 0, "tf32_pair_cs"),    # no workspace at all
 ]
-# One call per kernel with a small workspace (3, 1 and 1.5 MiB) before the
+# One call per kernel with a small workspace (6.5, 2 and 1.5 MiB) before the
 # memory is measured: a first launch may load code, which is not the GEMM
 # allocating, and a pool-backed workspace would then have to grow for the
 # larger workspaces of SEQUENCE.
 WARMUP = [
-    (256, 128, 4096, "exact", 0, "exact_pair"),
-    (256, 128, 4096, "tf32", 0, "tf32_pair"),
+    (3328, 1536, 4096, "exact", 0, "exact_pair"),
+    (3328, 1536, 4096, "tf32", 0, "tf32_pair"),
     (200, 100, 2000, "exact", 3, "exact_lsu"),
+    (512, 512, 512, "exact", 0, "exact_pair_cs"),
+    (512, 512, 512, "tf32", 0, "tf32_pair_cs"),
 ]
 
 
@@ -77,13 +83,18 @@ def _call(g, job, stream):
 
 def test_noalloc_split_tiles_match_oracle_without_allocating(g):
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    # every shape splits tiles between SMs on this device (CTA pairs: the
-    # library runs at most sms / 2 of them, fewer if fewer fit at once)
+    # every shape splits tiles between SMs through the workspace on this
+    # device (CTA pairs: the library runs at most sms / 2 of them, fewer if
+    # fewer fit at once)
     for m, n, k, mode, pad, kind in WARMUP + SEQUENCE:
         workers = sms if kind.endswith("lsu") else sms // 2
-        for w in (workers, workers - 8):
-            st, stats = g.gemm_f32_schedule_check(m, n, k, w, kind)
-            assert st == g.OK and stats["splits"] == 1, (m, n, k, kind, w, stats)
+        for w in (workers, workers - 4):
+            st, stats = g.gemm_f32_schedule_check(m, n, k, w, kind.replace("_cs", ""))
+            if kind.endswith("_cs"):
+                ok = stats["splits"] == 0 and stats["cluster_split"] >= 2
+            else:
+                ok = stats["splits"] == 1 and stats["cluster_split"] == 1
+            assert st == g.OK and ok, (m, n, k, kind, w, stats)
 
     s = torch.cuda.current_stream().cuda_stream
     warm = [_prepare(c, 40 + i) for i, c in enumerate(WARMUP)]
