@@ -181,7 +181,7 @@ constexpr int kHostMaxChunks = 16;
 struct HostState {
   std::mutex mu;
   cudaStream_t stream = nullptr, h2d = nullptr, d2h = nullptr;
-  cudaEvent_t a_in[kHostMaxChunks] = {}, c_done[kHostMaxChunks] = {};
+  cudaEvent_t a_in[kHostMaxChunks] = {}, c_done[kHostMaxChunks] = {}, b_hi = nullptr;
   bool ready = false;
   float *buf = nullptr;
   size_t cap_bytes = 0;
@@ -198,6 +198,8 @@ int host_state_init(HostState &hs) {
     if (cudaEventCreateWithFlags(&hs.a_in[i], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&hs.c_done[i], cudaEventDisableTiming) != cudaSuccess)
       return gemm::kErrLaunch;
+  if (cudaEventCreateWithFlags(&hs.b_hi, cudaEventDisableTiming) != cudaSuccess)
+    return gemm::kErrLaunch;
   hs.ready = true;
   return gemm::kOk;
 }
@@ -292,13 +294,19 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
   // GEMM of this one. Chunks are a quarter of M in whole 256-row tiles and
   // at least 1024 rows: a row chunk is a smaller GEMM that keeps fewer SMs
   // busy (4096^3 as 8 chunks of 512 rows takes 1.5x the time of one call,
-  // as 4 of 1024 rows 1.2x), and B's transfer, which every chunk needs,
-  // comes first whatever the split.
+  // as 4 of 1024 rows 1.2x). Every chunk needs all of B, so B goes first, in
+  // two halves of whole rows around the first chunk of A (when K >= 512):
+  // the first chunk's GEMM runs over the first half of K while the second
+  // half of B is still on its way, then adds the second half (beta = 1), so
+  // that only half of that GEMM waits behind the whole of B.
   int64_t chunk = (M + 3) / 4;
   chunk = (chunk + 255) / 256 * 256;
   if (chunk < 1024) chunk = 1024;
   if ((M + chunk - 1) / chunk > kHostMaxChunks) chunk = (M + kHostMaxChunks - 1) / kHostMaxChunks;
   const int nchunks = static_cast<int>((M + chunk - 1) / chunk);
+  // First half of B: rows [0, k1), a multiple of 32 (whole k-blocks, and a
+  // 16-byte aligned offset into the rows of A); 0 when K is too short.
+  const int64_t k1 = K >= 512 ? (K / 2) / 32 * 32 : 0;
   // On an error once copies are queued, wait for all queued work before
   // returning, so that no copy reads or writes the caller's buffers after
   // the call has returned.
@@ -308,9 +316,11 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
     cudaStreamSynchronize(hs.d2h);
     return code;
   };
-  if (K > 0 && cudaMemcpy2DAsync(dB, dldb * 4, B, ldb * 4, N * 4, K, cudaMemcpyHostToDevice,
-                                 hs.h2d) != cudaSuccess)
-    return drain(gemm::kErrLaunch);
+  auto copy_b_rows = [&](int64_t r0, int64_t rows) {
+    return cudaMemcpy2DAsync(dB + r0 * dldb, dldb * 4, B + r0 * ldb, ldb * 4, N * 4, rows,
+                             cudaMemcpyHostToDevice, hs.h2d);
+  };
+  if (K > 0 && copy_b_rows(0, k1 > 0 ? k1 : K) != cudaSuccess) return drain(gemm::kErrLaunch);
   for (int c = 0; c < nchunks; ++c) {
     const int64_t r0 = c * chunk, rows = (M - r0 < chunk) ? M - r0 : chunk;
     if (K > 0 && cudaMemcpy2DAsync(dA + r0 * dlda, dlda * 4, A + r0 * lda, lda * 4, K * 4, rows,
@@ -319,8 +329,21 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
     if (cudaEventRecord(hs.a_in[c], hs.h2d) != cudaSuccess ||
         cudaStreamWaitEvent(hs.stream, hs.a_in[c], 0) != cudaSuccess)
       return drain(gemm::kErrLaunch);
-    const GemmArgs d{rows, N, K, dA + r0 * dlda, dlda, dB, dldb, dC + r0 * dldc, dldc};
-    st = run(d, mode, GEMM_KERNEL_AUTO, hs.stream);
+    if (c == 0 && k1 > 0) {
+      // The second half of B follows the first chunk of A.
+      if (copy_b_rows(k1, K - k1) != cudaSuccess || cudaEventRecord(hs.b_hi, hs.h2d) != cudaSuccess)
+        return drain(gemm::kErrLaunch);
+      GemmArgs lo{rows, N, k1, dA, dlda, dB, dldb, dC, dldc};
+      st = run(lo, mode, GEMM_KERNEL_AUTO, hs.stream);
+      if (st != gemm::kOk) return drain(st);
+      if (cudaStreamWaitEvent(hs.stream, hs.b_hi, 0) != cudaSuccess) return drain(gemm::kErrLaunch);
+      GemmArgs hi{rows, N, K - k1, dA + k1, dlda, dB + k1 * dldb, dldb, dC, dldc};
+      hi.beta = 1.0f;
+      st = run(hi, mode, GEMM_KERNEL_AUTO, hs.stream);
+    } else {
+      const GemmArgs d{rows, N, K, dA + r0 * dlda, dlda, dB, dldb, dC + r0 * dldc, dldc};
+      st = run(d, mode, GEMM_KERNEL_AUTO, hs.stream);
+    }
     if (st != gemm::kOk) return drain(st);
     if (cudaEventRecord(hs.c_done[c], hs.stream) != cudaSuccess ||
         cudaStreamWaitEvent(hs.d2h, hs.c_done[c], 0) != cudaSuccess ||

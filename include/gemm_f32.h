@@ -202,7 +202,10 @@ int gemm_f32_select(int64_t M, int64_t N, int64_t K,
  * at least 1024 rows): B and then each chunk of A go to the device on
  * one stream, each chunk's GEMM starts when its rows have landed, and its
  * rows of C come back on another stream while later chunks compute, so
- * copies and compute overlap (page-locked host memory copies fastest).
+ * copies and compute overlap (page-locked host memory copies fastest). When
+ * K >= 512, B goes in two halves of whole rows, the second after the first
+ * chunk of A: that chunk's GEMM runs over the first half of K as soon as it
+ * can and adds the second half when it has landed.
  * Results meet the accuracy class of the mode; they may differ in the last
  * bits from one gemm_f32 call on the whole matrices, whose split of the work
  * differs. Same size, leading-dimension, mode and alias rules as gemm_f32
