@@ -50,7 +50,7 @@ WARMUP = [
     (3328, 1536, 4096, "tf32", 0, "tf32_pair"),
     (200, 100, 2000, "exact", 3, "exact_lsu"),
     (512, 512, 512, "exact", 0, "exact_pair_cs"),
-    (512, 512, 512, "tf32", 0, "tf32_pair_cs"),
+    (512, 512, 1024, "tf32", 0, "tf32_pair_cs"),
 ]
 
 
