@@ -2313,19 +2313,29 @@ int tc_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream) {
 namespace {
 
 // One launch of a TMA-fed pair kernel whose producers stop after their first
-// k-block, with every wait limited to timeout_ns. Only problems without split
-// tiles (no workspace) are accepted.
+// k-block, with every wait limited to timeout_ns: the cluster-split variant
+// when the problem takes it, else the plain one, which accepts only problems
+// whose tiles are not split through a workspace.
 template <class Plan>
-int stalled_launch(const GemmArgs &a, int64_t timeout_ns, int sm_count, cudaStream_t stream) {
-  Plan plan;
-  int st = plan.prepare(a, sm_count);
-  if (st != kOk) return st;
-  if (plan.counter_bytes > 0) return kErrInvalidArg;
+int stalled_run(Plan &plan, int64_t timeout_ns, cudaStream_t stream) {
   plan.p.timeout_ns = static_cast<unsigned long long>(timeout_ns);
   plan.p.stall_kb = 1;
-  st = plan.launch(stream);
+  const int st = plan.launch(stream);
   if (st != kOk) return st;
   return tc_poll_status(stream);
+}
+
+template <class CsPlan, class Plan>
+int stalled_launch(const GemmArgs &a, int64_t timeout_ns, int sm_count, cudaStream_t stream) {
+  CsPlan cs;
+  int st = cs.prepare(a, sm_count);
+  if (st != kOk) return st;
+  if (cs.p.ks > 1) return stalled_run(cs, timeout_ns, stream);
+  Plan plan;
+  st = plan.prepare(a, sm_count);
+  if (st != kOk) return st;
+  if (plan.counter_bytes > 0) return kErrInvalidArg;
+  return stalled_run(plan, timeout_ns, stream);
 }
 
 }  // namespace
@@ -2335,8 +2345,11 @@ int tc_selftest_stalled_gemm(const GemmArgs &a, bool exact, int64_t timeout_ns, 
   if (!tc_tma_direct(a) || a.opb || a.K < 2 * 32) return kErrInvalidArg;
   if (exact)
     return stalled_launch<LaunchPlan<kPairExactBK, kPairExactStages, true, false, 2, false, false,
+                                     kPairExactBSlots, true, true>,
+                          LaunchPlan<kPairExactBK, kPairExactStages, true, false, 2, false, false,
                                      kPairExactBSlots, true>>(a, timeout_ns, sm_count, stream);
-  return stalled_launch<LaunchPlan<32, kPairStages, false, false, 2, false, false, 0, true>>(
+  return stalled_launch<LaunchPlan<32, kPairStages, false, false, 2, false, false, 0, true, true>,
+                        LaunchPlan<32, kPairStages, false, false, 2, false, false, 0, true>>(
       a, timeout_ns, sm_count, stream);
 }
 

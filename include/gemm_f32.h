@@ -319,15 +319,18 @@ int gemm_f32_selftest_wait_timeout(int64_t timeout_ns, void *stream);
  * GEMM_ERR_TIMEOUT in the device status word and raise the CTA's abort flag;
  * every role leaves its loop, the MMAs issued so far complete, both CTAs of
  * each pair meet at the cluster barrier, TMEM is freed and the kernel
- * returns. Synchronises `stream` and returns what
- * gemm_f32_poll_device_status then reads (GEMM_ERR_TIMEOUT when the abort
- * path works); C's contents are unspecified afterwards. The context stays
- * usable.
+ * returns. A problem with few output tiles runs on the cluster-split
+ * variant, as gemm_f32 would run it (its CTAs then also skip the sum of the
+ * partial tiles and meet at the second cluster barrier). Synchronises
+ * `stream` and returns what gemm_f32_poll_device_status then reads
+ * (GEMM_ERR_TIMEOUT when the abort path works); C's contents are
+ * unspecified afterwards. The context stays usable.
  *   M, N, K, A, lda, B, ldb, C, ldc   as for gemm_f32, with K >= 64 (two
  *             k-blocks), A and B 16-byte aligned with pitches that are
- *             multiples of 4, and a problem whose output tiles are not split
- *             between SMs (M x N of at most one 256 x 256 tile per CTA pair),
- *             else GEMM_ERR_INVALID_ARG.
+ *             multiples of 4, and a problem whose tiles gemm_f32 would not
+ *             split through its workspace (no more unit tiles than CTA
+ *             pairs, or few enough for the cluster split), else
+ *             GEMM_ERR_INVALID_ARG.
  * The pages have no counterpart: their kernels have no waits that can fail.
  */
 int gemm_f32_selftest_stalled_gemm(int64_t M, int64_t N, int64_t K,

@@ -362,12 +362,19 @@ def test_bounded_wait_times_out_cleanly(g):
     check_within_bound(c, c64, s, 64, "exact", "after timeout self-test")
 
 
-@pytest.mark.parametrize("mode", ["exact", "tf32"])
-def test_pair_kernel_abort_path(g, mode):
+@pytest.mark.parametrize("mode,m,n,k,split", [
+    ("exact", 512, 512, 256, False),    # four 256 x 256 tiles, each whole on one pair
+    ("tf32", 512, 512, 256, False),
+    ("exact", 512, 512, 512, True),     # four pairs of one cluster per tile
+    ("tf32", 1024, 1024, 1024, True),
+])
+def test_pair_kernel_abort_path(g, mode, m, n, k, split):
     # the pair kernel's producers stop after one k-block, so its other roles'
     # waits (limit 20 ms) run out: the kernel must report the timeout, let
     # what it issued finish, free TMEM and return, leaving the context usable
-    m, n, k = 512, 512, 256  # four 256 x 256 tiles, each whole on one pair
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    st, stats = g.gemm_f32_schedule_check(m, n, k, sms // 2, mode + "_pair")
+    assert st == g.OK and (stats["cluster_split"] > 1) == split and stats["splits"] == 0, stats
     a, b = operands(m, n, k, "uniform", seed=11)
     da, db = to_dev(a), to_dev(b)
     dc = torch.zeros((m, n), device="cuda")
@@ -376,16 +383,25 @@ def test_pair_kernel_abort_path(g, mode):
                                           dc.data_ptr(), n, g.MODES[mode], 20_000_000, s)
     assert st == g.ERR_TIMEOUT, g.gemm_f32_status_string(st)
     assert g.gemm_f32_poll_device_status(s) == g.OK
-    # a problem with split tiles (512 x 512 x 4096: every tile split in both
-    # modes) is refused before anything runs: it would need a workspace
-    la = torch.zeros((m, 4096), device="cuda")
-    lb = torch.zeros((4096, n), device="cuda")
-    assert g.gemm_f32_selftest_stalled_gemm(m, n, 4096, la.data_ptr(), 4096, lb.data_ptr(), n,
-                                            dc.data_ptr(), n, g.MODES[mode], 20_000_000,
-                                            s) == g.ERR_INVALID_ARG
     c, _ = run(g, a, b, mode, "tc_tma")
     c64, sc = oracle.gemm(a, b)
     check_within_bound(c, c64, sc, k, mode, f"{mode} after the stalled pair kernel")
+
+
+@pytest.mark.parametrize("mode,m,n,k", [("exact", 2048, 1280, 2048), ("tf32", 1280, 2048, 8192)])
+def test_stalled_gemm_refuses_workspace_splits(g, mode, m, n, k):
+    # 40 unit tiles on 76 pairs: split through the workspace, which the
+    # self-test does not take; refused before anything runs
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    st, stats = g.gemm_f32_schedule_check(m, n, k, sms // 2, mode + "_pair")
+    assert st == g.OK and stats["splits"] == 1, stats
+    la = torch.zeros((m, k), device="cuda")
+    lb = torch.zeros((k, n), device="cuda")
+    dc = torch.zeros((m, n), device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert g.gemm_f32_selftest_stalled_gemm(m, n, k, la.data_ptr(), k, lb.data_ptr(), n,
+                                            dc.data_ptr(), n, g.MODES[mode], 20_000_000,
+                                            s) == g.ERR_INVALID_ARG
 
 
 # ---------------------------------------------------------- full sizes --
