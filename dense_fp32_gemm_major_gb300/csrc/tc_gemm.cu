@@ -113,6 +113,10 @@ struct TcParams {
   // the q-th of ks contiguous k-slices, and sum their partial tiles through
   // distributed shared memory (cluster_split_sum). 1 otherwise.
   int ks;
+  // 1: each cluster takes its stream-K chunk before its whole tiles, so that
+  // the sums of split tiles run in the epilogue while the MMAs go on with
+  // whole tiles; 0: whole tiles first.
+  int sk_first;
 };
 
 // One unit of work of a CTA: k-blocks [kb0, kb1) of unit tile `tile`.
@@ -203,10 +207,11 @@ __device__ __forceinline__ void tile_coords(const TcParams &p, int t, uint32_t r
 }
 
 // The work list of one cluster c (both CTAs of a cluster walk the same list),
-// identical for every role: first the whole unit tiles c, c + clusters, ...
-// below dp_tiles (raster order, so concurrent clusters share operand tiles in
-// L2), then its stream-K chunk (k-blocks [c * share, (c + 1) * share) of the
-// remaining unit tiles, in order, cut at tile boundaries). Every cluster sees
+// identical for every role: the whole unit tiles c, c + clusters, ... below
+// dp_tiles (raster order, so concurrent clusters share operand tiles in L2)
+// and its stream-K chunk (k-blocks [c * share, (c + 1) * share) of the
+// remaining unit tiles, in order, cut at tile boundaries): whole tiles first,
+// or with TcParams::sk_first the chunk first. Every cluster sees
 // the same partition, so the number of clusters contributing to a split tile
 // and each one's part index follow from the chunk boundaries alone.
 // (Host and device code: the host-side self-check gemm_f32_schedule_check
@@ -247,6 +252,10 @@ struct UnitIter {
       dp_next = -1;
       return true;
     }
+    if (p.sk_first) return next_split(p, u) || next_whole(p, u);
+    return next_whole(p, u) || next_split(p, u);
+  }
+  __host__ __device__ bool next_whole(const TcParams &p, WorkUnit &u) {
     if (dp_next < p.dp_tiles) {
       u.tile = dp_next;
       u.kb0 = 0;
@@ -258,6 +267,9 @@ struct UnitIter {
       dp_next += workers;
       return true;
     }
+    return false;
+  }
+  __host__ __device__ bool next_split(const TcParams &p, WorkUnit &u) {
     if (sk_pos < sk_end) {
       const int kbt = p.num_k_blocks;
       const int s = sk_pos / kbt;
@@ -1783,6 +1795,20 @@ Schedule make_schedule(int tiles, int kb, int sms, int min_chunk, bool full_wave
   return s;
 }
 
+// Whether the pair kernels take their stream-K chunk before their whole
+// tiles (TcParams::sk_first). The split-tile sums then run in the epilogue
+// while the MMAs go on with whole tiles, instead of after the last tile. The
+// 3xTF32 kernel gains at every size (4096^3: 394.7 -> 385.8 us,
+// 3328 x 1536 x 4096: 158 -> 144 us, 8192 x 11008 x 4096: -0.6 %). For one
+// TF32 pass, whose copies compete with the sums for L2 bandwidth, it pays
+// only while the tail is a large part of the work (4096^3, three whole
+// waves: 162.5 -> 159.3 us; 3328 x 1536 x 4096, one: 78.5 -> 70.8 us;
+// 8192 x 11008 x 4096, 18: 776 -> 785 us): at most 8 whole waves.
+bool split_chunk_first(const Schedule &sch, int workers, bool exact, bool pair) {
+  if (!pair) return false;
+  return exact || sch.dp_tiles <= 8 * workers;
+}
+
 // Tile counts of a launch: unit tiles of kTM rows x CL * kTN columns, k-blocks
 // of BK.
 void set_tiles(TcParams &p, int64_t M, int64_t N, int64_t K, int bk, int cl) {
@@ -1957,6 +1983,7 @@ struct LaunchPlan {
     p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
     p.stall_kb = -1;
     p.ks = 1;
+    p.sk_first = 0;
     p.sk_partials = nullptr;
     p.sk_counters = nullptr;
     if constexpr (CS) {
@@ -2031,6 +2058,7 @@ struct LaunchPlan {
     p.dp_tiles = sch.dp_tiles;
     p.sk_share = sch.sk_share;
     p.sk_ctas = sch.sk_ctas;
+    p.sk_first = split_chunk_first(sch, workers, EXACT, PAIR) ? 1 : 0;
     const int split_tiles = p.num_tiles - p.dp_tiles;
     if (split_tiles > 0 && sch.splits) {
       counter_bytes = (static_cast<size_t>(split_tiles) * CL * 4 + 255) / 256 * 256;
@@ -2463,6 +2491,7 @@ extern "C" int gemm_f32_schedule_check(int64_t M, int64_t N, int64_t K, int64_t 
   TcParams p = {};
   set_tiles(p, M, N, K, bk, pair ? 2 : 1);
   p.ks = 1;
+  p.sk_first = 0;
   const int64_t cells = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;
   if (cells > (int64_t{1} << 26)) return GEMM_ERR_INVALID_ARG;  // keep the check's memory small
   const int ks = pair ? cluster_split_ks(p.num_tiles, p.num_k_blocks, static_cast<int>(workers), bk,
@@ -2502,6 +2531,7 @@ extern "C" int gemm_f32_schedule_check(int64_t M, int64_t N, int64_t K, int64_t 
   p.dp_tiles = sch.dp_tiles;
   p.sk_share = sch.sk_share;
   p.sk_ctas = sch.sk_ctas;
+  p.sk_first = split_chunk_first(sch, static_cast<int>(workers), exact, pair) ? 1 : 0;
   const int kb = p.num_k_blocks, clusters = sch.grid;
   std::vector<int> cover(static_cast<size_t>(cells), 0);
   std::vector<int> part_owner(static_cast<size_t>(p.num_tiles) * kMaxSplit, -1);
