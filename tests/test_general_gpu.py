@@ -119,8 +119,9 @@ def test_general_integers_bitwise(g, mode, kernel, transa, transb):
                                          ("exact", "tc_lsu")])
 @pytest.mark.parametrize("transa,transb", LAYOUTS)
 def test_general_stream_k_adds_beta_c_once(g, mode, kernel, transa, transb):
-    # few output tiles and a long k range: the schedule splits every tile's k
-    # range over several SMs; beta * C must enter exactly once
+    # few output tiles and a long k range: every tile's k range is split over
+    # several SMs (the TMA-fed pair kernels over the pairs of one cluster, the
+    # plain-load kernel through the workspace); beta * C must enter exactly once
     m, n, k = 256, 384, 6144
     a = synth.small_integers((m, k), 71)
     b = synth.small_integers((k, n), 72)
