@@ -110,8 +110,10 @@ struct TcParams {
   int stall_kb;
   // Pair kernels on problems with fewer unit tiles than CTA pairs: ks > 1
   // pairs of one cluster share each unit tile, pair q of the cluster taking
-  // the q-th of ks contiguous k-slices, and sum their partial tiles through
-  // distributed shared memory (cluster_split_sum). 1 otherwise.
+  // the q-th of ks contiguous k-slices; every CTA writes its partial tile
+  // (its own band of rows to shared memory, the rest to its sk_partials slot)
+  // and, after a cluster barrier, sums its band over the ks partials
+  // (cluster_split_sum). 1 otherwise.
   int ks;
   // 1: each cluster takes its stream-K chunk before its whole tiles, so that
   // the sums of split tiles run in the epilogue while the MMAs go on with
@@ -376,50 +378,44 @@ __device__ __forceinline__ void epilogue_fixup(const TcParams &p, int sk_tile, u
   }
 }
 
-// float4s per thread and partial in flight in cluster_split_sum (a probe
-// read 96 KiB from three other SMs' shared memory in 2.7 us with 8, 4.2 us
-// with 4 and 4.4 us with 1; inside the GEMM 4 and 8 time the same).
+// float4s per thread and partial in flight in cluster_split_sum.
 constexpr int kClusterSumBatch = 8;
 
-// Shared::cluster address of `addr` (this CTA's shared memory) in CTA `rank`.
-__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
-  return remote;
-}
-
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
+// Rows [row0, row1) of the kTM-row tile that pair q of ks sums in a cluster
+// split (the band the CTAs of that pair own).
+__device__ __forceinline__ void cluster_split_band(int ks, int q, int &row0, int &row1) {
+  row0 = (q * kTM) / ks;
+  row1 = ((q + 1) * kTM) / ks;
 }
 
 // The final sum of a cluster-split tile (TcParams::ks > 1), run by all
-// nthreads threads of every CTA once each CTA's k-slice partial sits in its
-// shared memory at part ([m][n], kTN floats per row) and a cluster barrier
-// has made them visible. The CTAs of rank r (0, 1) in the ks pairs hold the
-// same 128 n x 256 m output tile; pair q's CTA sums m rows [q kTM / ks,
-// (q + 1) kTM / ks) of it over the ks partials, added in pair order 0 .. ks-1
-// (so results do not depend on timing), scales by alpha, adds beta C and
-// stores C with row and column guards. Its own partial is read from shared
-// memory, the others through distributed shared memory, BATCH float4s per
-// thread and partial in flight (the sum is bound by the latency of those
-// reads).
+// nthreads threads of every CTA once each CTA of the cluster has written its
+// k-slice partial ([m][n], kTN floats per row) and a cluster barrier has
+// ordered those writes: the rows of its own band in its shared memory at
+// own, the other rows in its slot of sk_partials (slot = CTA index). The
+// CTAs of rank r (0, 1) in the ks pairs hold the same 128 n x 256 m output
+// tile; pair q's CTA sums its band of rows over the ks partials, added in
+// pair order 0 .. ks-1 (so results do not depend on timing), scales by alpha,
+// adds beta C and stores C with row and column guards. The other pairs'
+// partials were written by other SMs, so they are read through L2
+// (ld.global.cg), BATCH float4s per thread and partial in flight.
 template <int BATCH>
-__device__ __forceinline__ void cluster_split_sum(const TcParams &p, const float *part,
+__device__ __forceinline__ void cluster_split_sum(const TcParams &p, const float *own,
                                                   uint32_t crank, int tid, int nthreads) {
   const int ks = p.ks;
   const uint32_t r = crank & 1u, q = crank >> 1;
   int mb, nb;
   tile_coords(p, (static_cast<int>(blockIdx.x) >> 1) / ks, r, mb, nb);
-  const int row0 = (static_cast<int>(q) * kTM) / ks, row1 = ((static_cast<int>(q) + 1) * kTM) / ks;
+  int row0, row1;
+  cluster_split_band(ks, static_cast<int>(q), row0, row1);
   constexpr int kRowVec = kTN / 4;
+  constexpr long long kSlotVec = static_cast<long long>(kTM) * kTN / 4;
+  const float4 *own4 = reinterpret_cast<const float4 *>(own) + row0 * kRowVec;
   const int nvec = (row1 - row0) * kRowVec;
-  const float4 *local = reinterpret_cast<const float4 *>(part) + row0 * kRowVec;
-  const uint32_t base = smem_addr(local);
+  // Slot of the CTA of rank r in pair 0 of this cluster; pair j's is 2 j further.
+  const float4 *base = reinterpret_cast<const float4 *>(p.sk_partials) +
+                       (static_cast<long long>(blockIdx.x) - crank + r) * kSlotVec +
+                       static_cast<long long>(row0) * kRowVec;
   const int M = p.M, N = p.N;
   const long long ldc = p.ldc;
   float *__restrict__ const C = p.C;
@@ -436,15 +432,14 @@ __device__ __forceinline__ void cluster_split_sum(const TcParams &p, const float
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {
           const int f = f0 + b * nthreads;
-          v[b] = f < nvec ? local[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[b] = f < nvec ? own4[f] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       } else {
-        const uint32_t src = cluster_map(base, 2u * static_cast<uint32_t>(j) + r);
+        const float4 *src = base + 2 * j * kSlotVec;
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {
           const int f = f0 + b * nthreads;
-          v[b] = f < nvec ? ld_cluster_f4(src + static_cast<uint32_t>(f) * 16u)
-                          : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[b] = f < nvec ? __ldcg(src + f) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
 #pragma unroll
@@ -635,13 +630,14 @@ __device__ __forceinline__ void stage_cols_lsu(uint8_t *tile, int lo_offset, con
 // part to finish sums all parts in order. PAIR: the accumulator's empty
 // barrier belongs to the even CTA of the pair (cluster rank pb), which issues
 // the MMAs of both. CS (cluster split): the CTA's one accumulator is a k-slice
-// of a tile shared by the pairs of its cluster; it goes to this CTA's shared
-// memory at part_smem ([m][n], kTN floats per row) for cluster_split_sum.
+// of a tile shared by the pairs of its cluster; its rows go ([m][n], kTN
+// floats per row) to this CTA's shared memory at own_smem if they are in the
+// band this CTA sums, else to its slot of sk_partials, for cluster_split_sum.
 template <int ACC_BUFS, int EPI_WARP0, bool PAIR, bool CS = false, class Shared>
 __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uint32_t tmem,
                                               uint32_t warp, uint32_t lane, uint32_t rank,
                                               volatile int *abort, uint32_t pb = 0,
-                                              float *part_smem = nullptr) {
+                                              float *own_smem = nullptr) {
   auto release_acc = [pb](uint64_t *bar) {
     if (PAIR)
       mbar_arrive_cluster(bar, pb);
@@ -664,7 +660,16 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
     const bool n_ok = gn < p.N;
     const uint32_t t_lane = tmem + ((quad * 32) << 16) + kAccCol + acc * kTM;
     if constexpr (CS) {
-      float *dst = part_smem + n_loc;
+      float *slot = p.sk_partials + static_cast<long long>(blockIdx.x) * kTM * kTN + n_loc;
+      float *local = own_smem + n_loc;
+      int row0, row1;
+      cluster_split_band(p.ks, u.part, row0, row1);
+      auto put = [&](int m, uint32_t v) {
+        if (m >= row0 && m < row1)
+          local[m * kTN] = __uint_as_float(v);
+        else
+          slot[m * kTN] = __uint_as_float(v);
+      };
 #pragma unroll 1
       for (int c = 0; c < kTM / 32; c += 2) {
         uint32_t r0[32], r1[32];
@@ -672,9 +677,9 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
         tmem_load_32cols(t_lane + (c + 1) * 32, r1);
         tmem_load_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) dst[(c * 32 + j) * kTN] = __uint_as_float(r0[j]);
+        for (int j = 0; j < 32; ++j) put(c * 32 + j, r0[j]);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) dst[(c * 32 + 32 + j) * kTN] = __uint_as_float(r1[j]);
+        for (int j = 0; j < 32; ++j) put(c * 32 + 32 + j, r1[j]);
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -1182,13 +1187,11 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
     tmem_dealloc<2>(tmem, kTmemCols);
   }
   if constexpr (CS) {
-    // Every CTA's k-slice partial is in its shared memory (the barrier above
-    // orders the epilogue's stores): sum them, then keep this CTA's shared
-    // memory alive until the other CTAs of the cluster have read it.
+    // Every CTA's k-slice partial is in its slot (the cluster barrier above
+    // orders the epilogue's stores before these reads).
     if (!sh->abort)
       cluster_split_sum<kClusterSumBatch>(p, reinterpret_cast<const float *>(tiles), crank,
                                           threadIdx.x, blockDim.x);
-    cluster_sync();
   }
   if (sh->fix_tile >= 0 && !sh->abort) {
     __threadfence();
@@ -1592,10 +1595,11 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
     tmem_dealloc<2>(tmem, kTmemCols);
   }
   if constexpr (CS) {
+    // Every CTA's k-slice partial is in its slot (the cluster barrier above
+    // orders the epilogue's stores before these reads).
     if (!sh->abort)
       cluster_split_sum<kClusterSumBatch>(p, reinterpret_cast<const float *>(tiles), crank,
                                           threadIdx.x, blockDim.x);
-    cluster_sync();
   }
   if (sh->fix_tile >= 0 && !sh->abort) {
     __threadfence();
@@ -1850,7 +1854,7 @@ struct KernelOf {
 template <int BK, int STAGES, bool OPA, bool OPB, bool CS>
 struct PairTf32Kernel {
   using Cfg = PairConfig<BK, STAGES, OPA, OPB>;
-  static_assert(Cfg::kTileBytes >= kTM * kTN * 4, "a cluster-split partial fits the stages");
+  static_assert(Cfg::kTileBytes >= kTM * kTN * 4, "a cluster-split band fits the stages");
   static constexpr int kThreads = Cfg::kThreads;
   static constexpr int kSmemBytes =
       Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
@@ -1863,7 +1867,7 @@ constexpr int kPairExactXform = 8;
 template <int BK, int AST, int BST, int XW, bool OPB, bool CS>
 struct PairExactKernel {
   using Cfg = PairExactConfig<BK, AST, BST, XW, OPB>;
-  static_assert(Cfg::kBRingOffset >= kTM * kTN * 4, "a cluster-split partial fits the A ring");
+  static_assert(Cfg::kBRingOffset >= kTM * kTN * 4, "a cluster-split band fits the A ring");
   static constexpr int kThreads = Cfg::kThreads;
   static constexpr int kSmemBytes =
       Cfg::kTileBytes +
@@ -1885,11 +1889,10 @@ struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true, CS>
 
 // Cluster split (TcParams::ks): worth it only when the k range each pair no
 // longer computes, kb (1 - 1 / ks), outweighs the exchange of partial tiles
-// (a per-CTA timeline at 512^3 and 1024^3: 1.6 us to move the accumulator to
-// shared memory, 3-5 us to read 64-96 KiB of partials from the other CTAs,
-// which distributed shared memory serves at 22-36 GB/s per SM, and two cluster
-// barriers): at least 256 k of 3xTF32 work (about 6 us per pair) or 768 k of
-// one TF32 pass.
+// (about 6 us at 512^3 and 1024^3: moving the accumulator out of TMEM, a
+// cluster barrier, reading 64-96 KiB of the other pairs' partials through L2
+// at about 56 GB/s per SM): at least 256 k of 3xTF32 work (about 6 us per
+// pair) or 768 k of one TF32 pass.
 constexpr int kClusterSplitSavedKExact = 256;
 constexpr int kClusterSplitSavedKTf32 = 768;
 
@@ -2026,6 +2029,8 @@ struct LaunchPlan {
       p.dp_tiles = 0;
       p.sk_share = 1;
       p.sk_ctas = 0;
+      // One kTM x kTN partial slot per CTA, no counters.
+      partial_bytes = static_cast<size_t>(sch.grid) * CL * kTM * kTN * 4;
       return kOk;
     }
     // Workers: clusters that can be resident at once (the placement of CTA
@@ -2066,6 +2071,8 @@ struct LaunchPlan {
     }
     return kOk;
   }
+
+  size_t workspace_bytes() const { return counter_bytes + partial_bytes; }
 
   // Point the schedule at a workspace of counter_bytes + partial_bytes.
   void set_workspace(void *ws) {
@@ -2123,40 +2130,44 @@ int workspace_pool(int dev, cudaMemPool_t *out) {
   return kOk;
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
-          int BST = 0, bool PAIR = false>
-int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
-  if constexpr (PAIR) {
-    // Few unit tiles: pairs of one cluster share each tile (no workspace).
-    LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, true> cs;
-    const int cst = cs.prepare(a, sm_count);
-    if (cst != kOk) return cst;
-    if (cs.p.ks > 1) return cs.launch(stream);
-  }
-  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR> plan;
-  int st = plan.prepare(a, sm_count);
-  if (st != kOk) return st;
-  // Split tiles need a workspace: partial tiles and one counter per split
-  // tile and CTA rank. It comes from the library's stream-ordered pool on the
-  // caller's stream and goes back right after the kernel, so concurrent calls
-  // on other streams never share it.
+// Launch a prepared plan with its workspace (partial tiles, and counters
+// cleared before the kernel) from the library's stream-ordered pool on the
+// caller's stream, returned right after the kernel, so concurrent calls on
+// other streams never share it.
+template <class Plan>
+int launch_pooled(Plan &plan, cudaStream_t stream) {
   void *ws = nullptr;
-  if (plan.counter_bytes > 0) {
+  if (plan.workspace_bytes() > 0) {
     int dev = 0;
     cudaMemPool_t pool = nullptr;
     if (cudaGetDevice(&dev) != cudaSuccess || workspace_pool(dev, &pool) != kOk) return kErrLaunch;
-    if (cudaMallocFromPoolAsync(&ws, plan.counter_bytes + plan.partial_bytes, pool, stream) !=
-        cudaSuccess)
+    if (cudaMallocFromPoolAsync(&ws, plan.workspace_bytes(), pool, stream) != cudaSuccess)
       return kErrLaunch;
-    if (cudaMemsetAsync(ws, 0, plan.counter_bytes, stream) != cudaSuccess) {
+    if (plan.counter_bytes > 0 && cudaMemsetAsync(ws, 0, plan.counter_bytes, stream) != cudaSuccess) {
       cudaFreeAsync(ws, stream);
       return kErrLaunch;
     }
     plan.set_workspace(ws);
   }
-  st = plan.launch(stream);
+  const int st = plan.launch(stream);
   if (ws != nullptr && cudaFreeAsync(ws, stream) != cudaSuccess) return kErrLaunch;
   return st;
+}
+
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
+          int BST = 0, bool PAIR = false>
+int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
+  if constexpr (PAIR) {
+    // Few unit tiles: pairs of one cluster share each tile.
+    LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, true> cs;
+    const int cst = cs.prepare(a, sm_count);
+    if (cst != kOk) return cst;
+    if (cs.p.ks > 1) return launch_pooled(cs, stream);
+  }
+  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR> plan;
+  const int st = plan.prepare(a, sm_count);
+  if (st != kOk) return st;
+  return launch_pooled(plan, stream);
 }
 
 }  // namespace
@@ -2348,7 +2359,7 @@ template <class Plan>
 int stalled_run(Plan &plan, int64_t timeout_ns, cudaStream_t stream) {
   plan.p.timeout_ns = static_cast<unsigned long long>(timeout_ns);
   plan.p.stall_kb = 1;
-  const int st = plan.launch(stream);
+  const int st = launch_pooled(plan, stream);
   if (st != kOk) return st;
   return tc_poll_status(stream);
 }
@@ -2431,26 +2442,28 @@ int launch_variant_noalloc(const GemmArgs &a, int sm_count, cudaStream_t stream)
   void *scratch = nullptr;
   int st = noalloc_scratch(dev, &scratch);
   if (st != kOk) return st;
+  // The same workspace layout gemm_f32 takes from the pool, here inside the
+  // fixed array; problems that need more are refused before anything runs.
+  auto run_in_scratch = [&](auto &plan) {
+    if (plan.workspace_bytes() > 0) {
+      if (plan.workspace_bytes() > GEMM_F32_NOALLOC_SCRATCH_BYTES) return static_cast<int>(kErrInvalidArg);
+      // The counters must start at zero; the previous call left them counted up.
+      if (plan.counter_bytes > 0 && cudaMemsetAsync(scratch, 0, plan.counter_bytes, stream) != cudaSuccess)
+        return static_cast<int>(kErrLaunch);
+      plan.set_workspace(scratch);
+    }
+    return plan.launch(stream);
+  };
   if constexpr (PAIR) {
-    // A cluster split needs no workspace at all.
     LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, false, BST, PAIR, true> cs;
     st = cs.prepare(a, sm_count);
     if (st != kOk) return st;
-    if (cs.p.ks > 1) return cs.launch(stream);
+    if (cs.p.ks > 1) return run_in_scratch(cs);
   }
   LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, false, BST, PAIR> plan;
   st = plan.prepare(a, sm_count);
   if (st != kOk) return st;
-  // The same workspace layout gemm_f32 takes from the pool, here inside the
-  // fixed array; problems that need more are refused before anything runs.
-  if (plan.counter_bytes > 0) {
-    if (plan.counter_bytes + plan.partial_bytes > GEMM_F32_NOALLOC_SCRATCH_BYTES)
-      return kErrInvalidArg;
-    // The counters must start at zero; the previous call left them counted up.
-    if (cudaMemsetAsync(scratch, 0, plan.counter_bytes, stream) != cudaSuccess) return kErrLaunch;
-    plan.set_workspace(scratch);
-  }
-  return plan.launch(stream);
+  return run_in_scratch(plan);
 }
 
 }  // namespace

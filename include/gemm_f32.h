@@ -361,9 +361,10 @@ typedef enum {
  *     shared;
  *   - for the pair kinds, when there are at most half as many unit tiles as
  *     pairs (the cluster split: 2 to 4 pairs of one cluster take contiguous
- *     k-slices of one unit tile and sum them in shared memory, with no
- *     workspace), that each pair has exactly one non-empty slice and the
- *     slices of a tile follow each other in pair order. (On a GPU the
+ *     k-slices of one unit tile and sum them after a cluster barrier, through
+ *     one workspace slot per CTA and no counters), that each pair has
+ *     exactly one non-empty slice and the slices of a tile follow each
+ *     other in pair order. (On a GPU the
  *     library also lowers the pairs per tile until all the clusters fit on
  *     the device at once, which this host-only check cannot see.)
  *   M, N, K     >= 1 and below 2^31; tiles x k-blocks at most 2^26
