@@ -29,6 +29,9 @@ constexpr int kBlocksPerSm = 8;
 // of the combined row range belong to `first`, the rest to `second`.
 __global__ void __launch_bounds__(kThreads)
     pack_rows_kernel(const PackJob first, const PackJob second) {
+  // The GEMM that reads the copies is launched as a programmatic dependent:
+  // let it start its set-up now (it waits for this grid before reading).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long total = first.rows + second.rows;
   for (long long rr = blockIdx.x; rr < total; rr += gridDim.x) {
     const bool in_first = rr < first.rows;

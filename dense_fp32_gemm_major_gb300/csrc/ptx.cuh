@@ -185,6 +185,23 @@ __device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *m
       : "memory");
 }
 
+// ------------------------------------------------- dependent grid launch --
+
+// Wait until every grid this one depends on has completed and its memory
+// operations are visible (a no-op for a grid launched without a programmatic
+// dependency). Every thread that reads or writes global memory the previous
+// grid may touch calls it first.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the grid launched next on the stream as a programmatic dependent to
+// start now; it still waits (grid_dependency_wait) for this grid to finish
+// before it touches memory.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cluster --
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

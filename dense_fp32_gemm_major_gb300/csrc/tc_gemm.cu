@@ -815,6 +815,7 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, OPB>::kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
+  grid_dependency_wait();  // see tc_pair_kernel
 
   if (warp < Cfg::kProdWarps) {
     // ---------------------------------------------------------- producer --
@@ -1079,6 +1080,9 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
   cluster_sync();  // barriers and TMEM of both CTAs set up before either signals the other
   tc_fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
+  // Launched as a programmatic dependent: the set-up above overlapped the
+  // previous grid (an operand copy, say); its results are needed from here on.
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer --
@@ -1357,6 +1361,9 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
   cluster_sync();  // barriers and TMEM of both CTAs set up before either signals the other
   tc_fence_after_sync();
   const uint32_t tmem = sh->tmem_base;
+  // Launched as a programmatic dependent: the set-up above overlapped the
+  // previous grid (an operand copy, say); its results are needed from here on.
+  grid_dependency_wait();
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer --
@@ -1889,11 +1896,13 @@ struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true, CS>
 
 // Cluster split (TcParams::ks): worth it only when the k range each pair no
 // longer computes, kb (1 - 1 / ks), outweighs the exchange of partial tiles
-// (about 6 us at 512^3 and 1024^3: moving the accumulator out of TMEM, a
-// cluster barrier, reading 64-96 KiB of the other pairs' partials through L2
-// at about 56 GB/s per SM): at least 256 k of 3xTF32 work (about 6 us per
-// pair) or 768 k of one TF32 pass.
-constexpr int kClusterSplitSavedKExact = 256;
+// (moving the accumulator out of TMEM, a cluster barrier, reading 64-96 KiB
+// of the other pairs' partials through L2 at about 56 GB/s per SM): at least
+// 128 k of 3xTF32 work or 768 k of one TF32 pass (timed: with 128 k instead
+// of 256, 512 x 512 x 256 20.1 -> 17.5 us, 1024 x 1024 x 256 20.5 -> 17.9 us,
+// 300 x 700 x 300 22.6 -> 18.1 us; one TF32 pass with 384 k instead of 768,
+// 512^3 15.0 -> 16.2 us, 1000 x 1532 x 776 19.4 -> 19.8 us).
+constexpr int kClusterSplitSavedKExact = 128;
 constexpr int kClusterSplitSavedKTf32 = 768;
 
 // Pairs per unit tile for a problem of `tiles` unit tiles of kb k-blocks on
@@ -2086,13 +2095,19 @@ struct LaunchPlan {
     cfg.blockDim = dim3(K::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CS ? CL * p.ks : CL;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    // A programmatic dependent of the previous grid on the stream: the launch
+    // and set-up overlap its tail (the kernels wait for it before they touch
+    // memory). After the operand copies of 1000 x 1531 x 777 (pitches of 777
+    // and 1531 floats): 37.3 -> 34.7 us exact, 29.4 -> 26.7 us tf32.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CS ? CL * p.ks : CL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = CL > 1 ? 1 : 0;
+    cfg.numAttrs = CL > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, K::kernel, map_a, map_b, p) ==
                    cudaSuccess
                ? kOk

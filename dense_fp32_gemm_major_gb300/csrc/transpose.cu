@@ -30,6 +30,9 @@ __global__ void __launch_bounds__(kW * kRowsPerPass)
     transpose_kernel(const float *__restrict__ src, long long lds, int rows, int cols,
                      float *__restrict__ dst, long long ldd, int tiles_c, long long tiles) {
   __shared__ float t[kT][kT + 1];
+  // The GEMM that reads the copy is launched as a programmatic dependent:
+  // let it start its set-up now (it waits for this grid before reading).
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tx = threadIdx.x % kW, ty = threadIdx.x / kW;
   for (long long tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int r0 = static_cast<int>(tile / tiles_c) * kT;

@@ -363,7 +363,7 @@ def test_bounded_wait_times_out_cleanly(g):
 
 
 @pytest.mark.parametrize("mode,m,n,k,split", [
-    ("exact", 512, 512, 256, False),    # four 256 x 256 tiles, each whole on one pair
+    ("exact", 512, 512, 128, False),    # four 256 x 256 tiles, each whole on one pair
     ("tf32", 512, 512, 256, False),
     ("exact", 512, 512, 512, True),     # four pairs of one cluster per tile
     ("tf32", 1024, 1024, 1024, True),

@@ -59,13 +59,15 @@ def test_benchmark_workloads_schedule(gemm_lib):
     st, s = gemm_lib.gemm_f32_schedule_check(1000, 1531, 777, 76, "exact_pair")
     assert st == gemm_lib.OK
     assert (s["tiles"], s["cluster_split"], s["clusters"]) == (24, 3, 72)
-    # a split must save each pair at least 256 k of 3xTF32 work or 768 k of
+    # a split must save each pair at least 128 k of 3xTF32 work or 768 k of
     # one TF32 pass: one TF32 pass at 512^3 (384 k saved at best) and
-    # 512 x 512 x 256 (192 k) are not split
+    # 512 x 512 x 128 (96 k) are not split, 512 x 512 x 256 (192 k) is
     st, s = gemm_lib.gemm_f32_schedule_check(512, 512, 512, 76, "tf32_pair")
     assert st == gemm_lib.OK and s["cluster_split"] == 1
-    st, s = gemm_lib.gemm_f32_schedule_check(512, 512, 256, 76, "exact_pair")
+    st, s = gemm_lib.gemm_f32_schedule_check(512, 512, 128, 76, "exact_pair")
     assert st == gemm_lib.OK and s["cluster_split"] == 1
+    st, s = gemm_lib.gemm_f32_schedule_check(512, 512, 256, 76, "exact_pair")
+    assert st == gemm_lib.OK and s["cluster_split"] == 4
     # 40 tiles on 76 pairs: more than half as many tiles as pairs, so the
     # stream-K schedule applies (every tile split through the workspace)
     st, s = gemm_lib.gemm_f32_schedule_check(2048, 1280, 2048, 76, "exact_pair")
