@@ -11,6 +11,10 @@ argument order; pointers are plain integers, streams are ``cudaStream_t``
 values as integers, 0 = the legacy default stream). ``matmul`` and ``gemm``
 are convenience wrappers over ``gemm_f32_ex`` and ``gemm_f32_general`` for
 torch CUDA tensors.
+
+``checked_library()`` loads libgemm_f32_checked.so, the same library built
+with device-side index checks (see include/gemm_f32.h, "The checked build");
+its handle has the same functions, and the wrappers below take it as ``lib``.
 """
 
 from __future__ import annotations
@@ -21,6 +25,7 @@ import re
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgemm_f32.so")
+LIB_CHECKED_PATH = os.path.join(_PKG, "libgemm_f32_checked.so")
 INCLUDE_DIR = os.path.join(os.path.dirname(_PKG), "include")
 HEADER_PATH = os.path.join(INCLUDE_DIR, "gemm_f32.h")
 HEADERS = [HEADER_PATH, os.path.join(INCLUDE_DIR, "reduce_f32.h")]
@@ -29,7 +34,11 @@ HEADERS = [HEADER_PATH, os.path.join(INCLUDE_DIR, "reduce_f32.h")]
 EXACT, TF32, EXACT_SIMT = 0, 1, 2
 MODES = {"exact": EXACT, "tf32": TF32, "exact_simt": EXACT_SIMT}
 # gemm_f32_status
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_ALIAS = range(6)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_DEVICE, ERR_LAUNCH, ERR_TIMEOUT, ERR_ALIAS, ERR_INDEX = range(7)
+# index-check sites (gemm_f32_take_index_fault)
+SITE_C_STORE, SITE_PARTIAL_WRITE, SITE_PARTIAL_READ, SITE_COUNTER, SITE_BAND = range(1, 6)
+SITE_LOAD_A, SITE_LOAD_B, SITE_COPY_SRC, SITE_COPY_DST = range(6, 10)
+SITE_REDUCE_IN, SITE_REDUCE_PARTIAL, SITE_REDUCE_OUT = range(10, 13)
 # fixed scratch of gemm_f32_noalloc
 NOALLOC_SCRATCH_BYTES = 40 * 1024 * 1024
 # gemm_f32_kernel
@@ -47,17 +56,15 @@ class GemmError(RuntimeError):
 
 
 _lib = None
+_lib_checked = None
 
 
-def _load():
-    global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
+def _open(path):
+    if not os.path.exists(path):
         raise RuntimeError(
-            f"libgemm_f32.so is not built ({LIB_PATH}); run __graft_entry__.build(). "
+            f"{os.path.basename(path)} is not built ({path}); run __graft_entry__.build(). "
             "There is no fallback implementation.")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(path)
     i64, i32, p = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
     sig = [i64, i64, i64, p, i64, p, i64, p, i64]
     lib.gemm_f32.argtypes = sig + [i32, p]
@@ -88,19 +95,44 @@ def _load():
     lib.gemm_f32_selftest_stalled_gemm.restype = i32
     lib.gemm_f32_schedule_check.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.gemm_f32_schedule_check.restype = i32
-    _lib = lib
+    lib.gemm_f32_checked_build.argtypes = []
+    lib.gemm_f32_checked_build.restype = i32
+    ll = ctypes.POINTER(ctypes.c_longlong)
+    lib.gemm_f32_take_index_fault.argtypes = [p, ll, ctypes.POINTER(i32), ll, ll]
+    lib.gemm_f32_take_index_fault.restype = i32
+    lib.gemm_f32_index_site_name.argtypes = [i32]
+    lib.gemm_f32_index_site_name.restype = ctypes.c_char_p
+    lib.gemm_f32_selftest_index_check.argtypes = sig + [i32, i32, p]
+    lib.gemm_f32_selftest_index_check.restype = i32
     return lib
 
 
-def reload():
-    """Drop the cached handle (after a rebuild) and load the library again."""
+def _load():
     global _lib
+    if _lib is None:
+        _lib = _open(LIB_PATH)
+    return _lib
+
+
+def reload():
+    """Drop the cached handles (after a rebuild) and load the library again."""
+    global _lib, _lib_checked
     _lib = None
+    _lib_checked = None
     return _load()
 
 
 def library():
     return _load()
+
+
+def checked_library():
+    """The index-checked build (libgemm_f32_checked.so): same functions as
+    library(); slower, for debugging and the index-check tests."""
+    global _lib_checked
+    if _lib_checked is None:
+        _lib_checked = _open(LIB_CHECKED_PATH)
+    return _lib_checked
 
 
 def declared_symbols() -> list[str]:
@@ -178,6 +210,31 @@ def gemm_f32_selftest_stalled_gemm(M, N, K, A, lda, B, ldb, C, ldc, mode, timeou
                                    stream=0) -> int:
     return _load().gemm_f32_selftest_stalled_gemm(M, N, K, A, lda, B, ldb, C, ldc, mode,
                                                   timeout_ns, stream or None)
+
+
+def gemm_f32_checked_build(lib=None) -> int:
+    return (lib or _load()).gemm_f32_checked_build()
+
+
+def gemm_f32_take_index_fault(stream=0, lib=None):
+    """(status, count, site, offset, extent): the index-check record since the
+    last call, reset (checked build; count is always 0 in the regular one)."""
+    count, off, ext = ctypes.c_longlong(0), ctypes.c_longlong(0), ctypes.c_longlong(0)
+    site = ctypes.c_int(0)
+    st = (lib or _load()).gemm_f32_take_index_fault(stream or None, ctypes.byref(count),
+                                                   ctypes.byref(site), ctypes.byref(off),
+                                                   ctypes.byref(ext))
+    return st, count.value, site.value, off.value, ext.value
+
+
+def gemm_f32_index_site_name(site: int, lib=None) -> str:
+    return (lib or _load()).gemm_f32_index_site_name(site).decode()
+
+
+def gemm_f32_selftest_index_check(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel=KERNEL_AUTO,
+                                  stream=0, lib=None) -> int:
+    return (lib or _load()).gemm_f32_selftest_index_check(M, N, K, A, lda, B, ldb, C, ldc, mode,
+                                                         kernel, stream or None)
 
 
 SCHEDULE_KINDS = {"exact_pair": 0, "tf32_pair": 1, "exact_lsu": 2, "tf32_lsu": 3}

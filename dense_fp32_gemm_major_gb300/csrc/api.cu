@@ -206,6 +206,33 @@ int host_state_init(HostState &hs) {
 
 int64_t round_up4(int64_t x) { return (x + 3) / 4 * 4; }
 
+// Checked build: the index-check records of every kernel translation unit
+// (read after the caller synchronised). Returns the total count of recorded
+// violations (-1 if a record could not be read), *first the first record of
+// the first unit that has one; clear: reset the records.
+long long take_index_faults(bool clear, gemm::IndexFault *first) {
+  if (!GEMM_F32_INDEX_CHECKS) {
+    if (first != nullptr) *first = gemm::IndexFault{0u, 0, 0, 0};
+    return 0;
+  }
+  int (*const takers[])(gemm::IndexFault *, bool) = {
+      gemm::tc_index_fault_take, gemm::simt_index_fault_take, gemm::pack_index_fault_take,
+      gemm::transpose_index_fault_take, gemm::reduce_index_fault_take};
+  long long total = 0;
+  bool have = false;
+  for (auto take : takers) {
+    gemm::IndexFault f = {0u, 0, 0, 0};
+    if (take(&f, clear) != gemm::kOk) return -1;
+    total += f.count;
+    if (f.count > 0 && !have) {
+      have = true;
+      if (first != nullptr) *first = f;
+    }
+  }
+  if (!have && first != nullptr) *first = gemm::IndexFault{0u, 0, 0, 0};
+  return total;
+}
+
 }  // namespace
 
 extern "C" {
@@ -414,6 +441,8 @@ const char *gemm_f32_status_string(int status) {
       return "GEMM_ERR_TIMEOUT";
     case GEMM_ERR_ALIAS:
       return "GEMM_ERR_ALIAS";
+    case GEMM_ERR_INDEX:
+      return "GEMM_ERR_INDEX";
     default:
       return "GEMM_ERR_UNKNOWN";
   }
@@ -438,7 +467,79 @@ int gemm_f32_poll_device_status(void *stream) {
   int dev = 0, sms = 0;
   const int st = current_device(&dev, &sms);
   if (st != gemm::kOk) return st;
-  return gemm::tc_poll_status(static_cast<cudaStream_t>(stream));
+  const int tst = gemm::tc_poll_status(static_cast<cudaStream_t>(stream));
+  if (tst != gemm::kOk || !GEMM_F32_INDEX_CHECKS) return tst;
+  // Checked build: a recorded index violation, left for take_index_fault.
+  if (take_index_faults(false, nullptr) > 0) return GEMM_ERR_INDEX;
+  return gemm::kOk;
+}
+
+int gemm_f32_checked_build(void) { return GEMM_F32_INDEX_CHECKS ? 1 : 0; }
+
+int gemm_f32_take_index_fault(void *stream, long long *count, int *site, long long *offset,
+                              long long *extent) {
+  if (count == nullptr || site == nullptr || offset == nullptr || extent == nullptr)
+    return GEMM_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  const int st = current_device(&dev, &sms);
+  if (st != gemm::kOk) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return GEMM_ERR_LAUNCH;
+  gemm::IndexFault first = {0u, 0, 0, 0};
+  const long long n = take_index_faults(true, &first);
+  if (n < 0) return GEMM_ERR_LAUNCH;
+  *count = n;
+  *site = first.site;
+  *offset = first.offset;
+  *extent = first.extent;
+  return GEMM_OK;
+}
+
+const char *gemm_f32_index_site_name(int site) {
+  switch (site) {
+    case gemm::kSiteNone:
+      return "none";
+    case gemm::kSiteCStore:
+      return "C store";
+    case gemm::kSitePartialWrite:
+      return "partial slot write";
+    case gemm::kSitePartialRead:
+      return "partial slot read";
+    case gemm::kSiteCounter:
+      return "split-tile counter";
+    case gemm::kSiteBand:
+      return "cluster-split band (shared memory)";
+    case gemm::kSiteLoadA:
+      return "A load";
+    case gemm::kSiteLoadB:
+      return "B load";
+    case gemm::kSiteCopySrc:
+      return "operand copy source";
+    case gemm::kSiteCopyDst:
+      return "operand copy destination";
+    case gemm::kSiteReduceIn:
+      return "reduction input";
+    case gemm::kSiteReducePartial:
+      return "reduction partial";
+    case gemm::kSiteReduceOut:
+      return "reduction output";
+    default:
+      return "unknown";
+  }
+}
+
+int gemm_f32_selftest_index_check(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                  const float *B, int64_t ldb, float *C, int64_t ldc, int mode,
+                                  int kernel, void *stream) {
+  if (!GEMM_F32_INDEX_CHECKS) return GEMM_ERR_INVALID_ARG;  // nothing to check in this build
+  GemmArgs a{M, N, K, A, lda, B, ldb, C, ldc};
+  bool noop = false;
+  int st = validate(a, mode, &noop);
+  if (st != gemm::kOk) return st;
+  if (noop || M < 2 || K < 1) return GEMM_ERR_INVALID_ARG;
+  // C declared one row short: every access to its last row fails the check.
+  a.c_extent = gemm::matrix_extent(M - 1, N, ldc);
+  return run(a, mode, kernel, static_cast<cudaStream_t>(stream));
 }
 
 int gemm_f32_selftest_wait_timeout(int64_t timeout_ns, void *stream) {

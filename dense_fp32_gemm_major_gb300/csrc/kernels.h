@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "checks.cuh"
+
 namespace gemm {
 
 // C = alpha * op(A) op(B) + beta * C, row-major. opa = 0: A is M x K (pitch
@@ -22,7 +24,15 @@ struct GemmArgs {
   int opa = 0;
   float alpha = 1.0f;
   float beta = 0.0f;
+  // Extent of C in elements that the kernels' index checks hold stores to
+  // (checked build); -1: the extent of the M x N matrix, (M - 1) ldc + N.
+  int64_t c_extent = -1;
 };
+
+// The extent index checks use for C.
+inline long long c_extent_of(const GemmArgs &a) {
+  return a.c_extent >= 0 ? a.c_extent : matrix_extent(a.M, a.N, a.ldc);
+}
 
 // Status codes (values of gemm_f32_status).
 enum : int {
@@ -32,6 +42,7 @@ enum : int {
   kErrLaunch = 3,
   kErrTimeout = 4,
   kErrAlias = 5,
+  kErrIndex = 6,
 };
 
 // True when A and B as given can be described by TMA tensor maps: A not
@@ -76,6 +87,9 @@ struct PackJob {
   int64_t lds = 0, rows = 0, cols = 0;
   float *dst = nullptr;
   int64_t ldd = 0;
+  // Declared extents (elements) of src and dst for the index checks; set by
+  // pack_rows_launch from the shape.
+  int64_t src_extent = 0, dst_extent = 0;
 };
 
 // Both jobs in one launch on `stream`.
@@ -102,5 +116,14 @@ int tc_selftest_wait_timeout(int64_t timeout_ns, cudaStream_t stream);
 // the device status read after the launch.
 int tc_selftest_stalled_gemm(const GemmArgs &a, bool exact, int64_t timeout_ns, int sm_count,
                              cudaStream_t stream);
+
+// Checked build: read (and with clear, reset) the index-check record of
+// each translation unit (see checks.cuh); the caller has synchronised the
+// device. In the regular build they return an empty record.
+int tc_index_fault_take(IndexFault *out, bool clear);
+int simt_index_fault_take(IndexFault *out, bool clear);
+int pack_index_fault_take(IndexFault *out, bool clear);
+int transpose_index_fault_take(IndexFault *out, bool clear);
+int reduce_index_fault_take(IndexFault *out, bool clear);
 
 }  // namespace gemm

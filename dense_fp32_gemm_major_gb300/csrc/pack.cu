@@ -40,20 +40,29 @@ __global__ void __launch_bounds__(kThreads)
     const float *s = j.src + r * j.lds;
     float *d = j.dst + r * j.ldd;
     const int cols = static_cast<int>(j.cols);
+    // Index checks of the checked build (checks.cuh); nothing in the regular one.
+    auto load = [&](int cc) {
+      return index_ok(kSiteCopySrc, r * j.lds + cc, 1, j.src_extent) ? __ldg(s + cc) : 0.0f;
+    };
+    auto store = [&](int cc, float v) {
+      if (index_ok(kSiteCopyDst, r * j.ldd + cc, 1, j.dst_extent)) d[cc] = v;
+    };
     int c = threadIdx.x;
     for (; c + 3 * kThreads < cols; c += 4 * kThreads) {
-      const float v0 = __ldg(s + c), v1 = __ldg(s + c + kThreads), v2 = __ldg(s + c + 2 * kThreads),
-                  v3 = __ldg(s + c + 3 * kThreads);
-      d[c] = v0;
-      d[c + kThreads] = v1;
-      d[c + 2 * kThreads] = v2;
-      d[c + 3 * kThreads] = v3;
+      const float v0 = load(c), v1 = load(c + kThreads), v2 = load(c + 2 * kThreads),
+                  v3 = load(c + 3 * kThreads);
+      store(c, v0);
+      store(c + kThreads, v1);
+      store(c + 2 * kThreads, v2);
+      store(c + 3 * kThreads, v3);
     }
-    for (; c < cols; c += kThreads) d[c] = __ldg(s + c);
+    for (; c < cols; c += kThreads) store(c, load(c));
   }
 }
 
 }  // namespace
+
+GEMM_INDEX_FAULT_TAKE(pack_index_fault_take)
 
 int pack_rows_launch(const PackJob &first, const PackJob &second, int sm_count,
                      cudaStream_t stream) {
@@ -63,6 +72,10 @@ int pack_rows_launch(const PackJob &first, const PackJob &second, int sm_count,
   PackJob a = first, b = second;
   if (a.rows <= 0 || a.cols <= 0) a.rows = 0;
   if (b.rows <= 0 || b.cols <= 0) b.rows = 0;
+  for (PackJob *j : {&a, &b}) {
+    j->src_extent = matrix_extent(j->rows, j->cols, j->lds);
+    j->dst_extent = matrix_extent(j->rows, j->cols, j->ldd);
+  }
   const long long cap = static_cast<long long>(sm_count > 0 ? sm_count : 1) * kBlocksPerSm;
   const unsigned grid = static_cast<unsigned>(total < cap ? total : cap);
   pack_rows_kernel<<<grid, kThreads, 0, stream>>>(a, b);

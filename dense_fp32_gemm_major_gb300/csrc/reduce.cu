@@ -64,7 +64,8 @@ __device__ __forceinline__ float block_sum(float v) {
 // i goes to thread i mod T.
 template <bool VEC>
 __global__ void __launch_bounds__(kThreads)
-    reduce_partials_kernel(const float *__restrict__ x, long long n, float *__restrict__ partials) {
+    reduce_partials_kernel(const float *__restrict__ x, long long n, float *__restrict__ partials,
+                           int groups) {
   // Let the second dispatch be scheduled now; it waits for this grid to
   // finish (and its writes to land) before it reads the partials.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -78,7 +79,9 @@ __global__ void __launch_bounds__(kThreads)
     for (; i + (kUnroll - 1) * T < n4; i += kUnroll * T) {
       float4 v[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) v[u] = __ldcs(x4 + i + u * T);
+      for (int u = 0; u < kUnroll; ++u)
+        v[u] = index_ok(kSiteReduceIn, 4 * (i + u * T), 4, n) ? __ldcs(x4 + i + u * T)
+                                                             : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         a0 += v[u].x;
@@ -88,27 +91,31 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     for (; i < n4; i += T) {
-      const float4 v = __ldcs(x4 + i);
+      const float4 v = index_ok(kSiteReduceIn, 4 * i, 4, n) ? __ldcs(x4 + i)
+                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
       a0 += v.x;
       a1 += v.y;
       a2 += v.z;
       a3 += v.w;
     }
-    if (t < n - 4 * n4) a0 += x[4 * n4 + t];
+    if (t < n - 4 * n4 && index_ok(kSiteReduceIn, 4 * n4 + t, 1, n)) a0 += x[4 * n4 + t];
   } else {
     long long i = t;
+    auto load = [&](long long j) {
+      return index_ok(kSiteReduceIn, j, 1, n) ? __ldcs(x + j) : 0.0f;
+    };
     for (; i + 3 * T < n; i += 4 * T) {
-      const float v0 = __ldcs(x + i), v1 = __ldcs(x + i + T), v2 = __ldcs(x + i + 2 * T),
-                  v3 = __ldcs(x + i + 3 * T);
+      const float v0 = load(i), v1 = load(i + T), v2 = load(i + 2 * T), v3 = load(i + 3 * T);
       a0 += v0;
       a1 += v1;
       a2 += v2;
       a3 += v3;
     }
-    for (; i < n; i += T) a0 += __ldcs(x + i);
+    for (; i < n; i += T) a0 += load(i);
   }
   const float s = block_sum((a0 + a1) + (a2 + a3));
-  if (threadIdx.x == 0) partials[blockIdx.x] = s;
+  if (threadIdx.x == 0 && index_ok(kSiteReducePartial, blockIdx.x, 1, groups))
+    partials[blockIdx.x] = s;
 }
 
 // The second dispatch: one CTA sums the G partials (partial g to thread
@@ -119,12 +126,15 @@ __global__ void __launch_bounds__(kThreads)
   // that grid has completed and its partials are visible.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   float a = 0.0f;
-  for (int g = threadIdx.x; g < groups; g += kThreads) a += partials[g];
+  for (int g = threadIdx.x; g < groups; g += kThreads)
+    if (index_ok(kSiteReducePartial, g, 1, groups)) a += partials[g];
   const float s = block_sum(a);
   if (threadIdx.x == 0) *out = s;
 }
 
 }  // namespace
+
+GEMM_INDEX_FAULT_TAKE(reduce_index_fault_take)
 
 int reduce_default_groups(int sm_count) { return 4 * (sm_count > 0 ? sm_count : 1); }
 
@@ -134,9 +144,9 @@ int reduce_launch(int64_t n, const float *x, float *out, int groups, float *part
     return cudaMemsetAsync(out, 0, sizeof(float), stream) == cudaSuccess ? kOk : kErrLaunch;
   }
   if (reinterpret_cast<uintptr_t>(x) % 16 == 0)
-    reduce_partials_kernel<true><<<groups, kThreads, 0, stream>>>(x, n, partials);
+    reduce_partials_kernel<true><<<groups, kThreads, 0, stream>>>(x, n, partials, groups);
   else
-    reduce_partials_kernel<false><<<groups, kThreads, 0, stream>>>(x, n, partials);
+    reduce_partials_kernel<false><<<groups, kThreads, 0, stream>>>(x, n, partials, groups);
   if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
   // The second dispatch as a programmatic dependent launch: its launch
   // overlaps the tail of the first grid instead of following its completion.

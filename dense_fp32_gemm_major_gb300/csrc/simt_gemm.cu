@@ -58,6 +58,8 @@ struct SimtParams {
   long long ldc;
   float alpha, beta;
   int tiles_m, tiles_n;
+  // Extents in elements of A, B and C for the checked build's index checks.
+  long long a_extent, b_extent, c_extent;
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -113,21 +115,27 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int row = warp * 16 + j * 4 + (lane >> 3), kk = lane & 7;
-          const bool in = m0 + row < p.M && k0 + kk < p.K;
-          const float *src = in ? p.A + static_cast<long long>(m0 + row) * p.lda + k0 + kk : p.A;
+          const long long off = static_cast<long long>(m0 + row) * p.lda + k0 + kk;
+          const bool in = m0 + row < p.M && k0 + kk < p.K &&
+                          index_ok(kSiteLoadA, off, 1, p.a_extent);
+          const float *src = in ? p.A + off : p.A;
           copy4(as + ((h * 8 + kk) * kPitch + row) * 4, src, in);
         }
       } else if constexpr (VEC) {
         const int kk = tid >> 5, col = lane * 4;
-        const bool in = k0 + kk < p.K && m0 + col < p.M;
-        const float *src = in ? p.A + static_cast<long long>(k0 + kk) * p.lda + m0 + col : p.A;
+        const long long off = static_cast<long long>(k0 + kk) * p.lda + m0 + col;
+        const bool in = k0 + kk < p.K && m0 + col < p.M &&
+                        index_ok(kSiteLoadA, off, 4, p.a_extent);
+        const float *src = in ? p.A + off : p.A;
         copy16(as + ((h * 8 + kk) * kPitch + col) * 4, src, in);
       } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int kk = tid >> 5, col = lane + 32 * j;
-          const bool in = k0 + kk < p.K && m0 + col < p.M;
-          const float *src = in ? p.A + static_cast<long long>(k0 + kk) * p.lda + m0 + col : p.A;
+          const long long off = static_cast<long long>(k0 + kk) * p.lda + m0 + col;
+          const bool in = k0 + kk < p.K && m0 + col < p.M &&
+                          index_ok(kSiteLoadA, off, 1, p.a_extent);
+          const float *src = in ? p.A + off : p.A;
           copy4(as + ((h * 8 + kk) * kPitch + col) * 4, src, in);
         }
       }
@@ -135,21 +143,27 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int col = warp * 16 + j * 4 + (lane >> 3), kk = lane & 7;
-          const bool in = n0 + col < p.N && k0 + kk < p.K;
-          const float *src = in ? p.B + static_cast<long long>(n0 + col) * p.ldb + k0 + kk : p.B;
+          const long long off = static_cast<long long>(n0 + col) * p.ldb + k0 + kk;
+          const bool in = n0 + col < p.N && k0 + kk < p.K &&
+                          index_ok(kSiteLoadB, off, 1, p.b_extent);
+          const float *src = in ? p.B + off : p.B;
           copy4(bs + ((h * 8 + kk) * kPitch + col) * 4, src, in);
         }
       } else if constexpr (VEC) {
         const int kk = tid >> 5, col = lane * 4;
-        const bool in = k0 + kk < p.K && n0 + col < p.N;
-        const float *src = in ? p.B + static_cast<long long>(k0 + kk) * p.ldb + n0 + col : p.B;
+        const long long off = static_cast<long long>(k0 + kk) * p.ldb + n0 + col;
+        const bool in = k0 + kk < p.K && n0 + col < p.N &&
+                        index_ok(kSiteLoadB, off, 4, p.b_extent);
+        const float *src = in ? p.B + off : p.B;
         copy16(bs + ((h * 8 + kk) * kPitch + col) * 4, src, in);
       } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int kk = tid >> 5, col = lane + 32 * j;
-          const bool in = k0 + kk < p.K && n0 + col < p.N;
-          const float *src = in ? p.B + static_cast<long long>(k0 + kk) * p.ldb + n0 + col : p.B;
+          const long long off = static_cast<long long>(k0 + kk) * p.ldb + n0 + col;
+          const bool in = k0 + kk < p.K && n0 + col < p.N &&
+                          index_ok(kSiteLoadB, off, 1, p.b_extent);
+          const float *src = in ? p.B + off : p.B;
           copy4(bs + ((h * 8 + kk) * kPitch + col) * 4, src, in);
         }
       }
@@ -202,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
 #pragma unroll
       for (int j = 0; j < 4; ++j) v[j] = p.alpha * acc[i][h * 4 + j];
       if (VEC) {
-        if (col < p.N) {
+        if (col < p.N && ptr_ok(kSiteCStore, crow + col, 4, p.C, p.c_extent)) {
           float4 *dst = reinterpret_cast<float4 *>(crow + col);
           if (p.beta != 0.0f) {
             const float4 c = *dst;
@@ -216,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 2) simt_gemm_kernel(const SimtParams
       } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (col + j < p.N) {
+          if (col + j < p.N && ptr_ok(kSiteCStore, crow + col + j, 1, p.C, p.c_extent)) {
             if (p.beta != 0.0f) v[j] += p.beta * crow[col + j];
             crow[col + j] = v[j];
           }
@@ -249,6 +263,8 @@ int launch_variant(const SimtParams &p, dim3 grid, cudaStream_t stream) {
 
 }  // namespace
 
+GEMM_INDEX_FAULT_TAKE(simt_index_fault_take)
+
 int simt_launch(const GemmArgs &a, cudaStream_t stream) {
   SimtParams p;
   p.M = static_cast<int>(a.M);
@@ -262,6 +278,9 @@ int simt_launch(const GemmArgs &a, cudaStream_t stream) {
   p.ldc = a.ldc;
   p.alpha = a.alpha;
   p.beta = a.beta;
+  p.a_extent = a.opa ? matrix_extent(a.K, a.M, a.lda) : matrix_extent(a.M, a.K, a.lda);
+  p.b_extent = a.opb ? matrix_extent(a.N, a.K, a.ldb) : matrix_extent(a.K, a.N, a.ldb);
+  p.c_extent = c_extent_of(a);
   p.tiles_m = static_cast<int>((a.M + kTile - 1) / kTile);
   p.tiles_n = static_cast<int>((a.N + kTile - 1) / kTile);
   const long long blocks = static_cast<long long>(p.tiles_m) * p.tiles_n;

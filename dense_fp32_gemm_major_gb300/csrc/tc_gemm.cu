@@ -119,6 +119,10 @@ struct TcParams {
   // the sums of split tiles run in the epilogue while the MMAs go on with
   // whole tiles; 0: whole tiles first.
   int sk_first;
+  // Extents in elements of A, B, C and the workspace's partial slots and
+  // counters, which the checked build's index checks hold every plain
+  // access to (checks.cuh).
+  long long a_extent, b_extent, c_extent, partial_extent, counter_extent;
 };
 
 // One unit of work of a CTA: k-blocks [kb0, kb1) of unit tile `tile`.
@@ -330,7 +334,9 @@ __device__ __forceinline__ void epilogue_fixup(const TcParams &p, int sk_tile, u
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int f = f0 + tid + nthreads * j;
-      acc[j] = f < kVec ? __ldcg(base + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+      acc[j] = f < kVec && ptr_ok(kSitePartialRead, base + f, 4, p.sk_partials, p.partial_extent)
+                   ? __ldcg(base + f)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll 1
     for (int q = 1; q < nparts; ++q) {
@@ -339,7 +345,9 @@ __device__ __forceinline__ void epilogue_fixup(const TcParams &p, int sk_tile, u
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const int f = f0 + tid + nthreads * j;
-        v[j] = f < kVec ? __ldcg(src + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[j] = f < kVec && ptr_ok(kSitePartialRead, src + f, 4, p.sk_partials, p.partial_extent)
+                   ? __ldcg(src + f)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
@@ -358,6 +366,7 @@ __device__ __forceinline__ void epilogue_fixup(const TcParams &p, int sk_tile, u
       if (gm >= M) continue;
       float *dst = C + static_cast<long long>(gm) * ldc + gn;
       if (vec_ok && gn + 3 < N) {
+        if (!ptr_ok(kSiteCStore, dst, 4, C, p.c_extent)) continue;
         float4 v = make_float4(alpha * acc[j].x, alpha * acc[j].y, alpha * acc[j].z,
                                alpha * acc[j].w);
         if (beta != 0.0f) {
@@ -372,7 +381,8 @@ __device__ __forceinline__ void epilogue_fixup(const TcParams &p, int sk_tile, u
         const float e[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          if (gn + i < N) dst[i] = beta != 0.0f ? alpha * e[i] + beta * dst[i] : alpha * e[i];
+          if (gn + i < N && ptr_ok(kSiteCStore, dst + i, 1, C, p.c_extent))
+            dst[i] = beta != 0.0f ? alpha * e[i] + beta * dst[i] : alpha * e[i];
       }
     }
   }
@@ -432,14 +442,18 @@ __device__ __forceinline__ void cluster_split_sum(const TcParams &p, const float
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {
           const int f = f0 + b * nthreads;
-          v[b] = f < nvec ? own4[f] : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[b] = f < nvec && index_ok(kSiteBand, (row0 * kRowVec + f) * 4LL, 4, kTM * kTN)
+                     ? own4[f]
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       } else {
         const float4 *src = base + 2 * j * kSlotVec;
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {
           const int f = f0 + b * nthreads;
-          v[b] = f < nvec ? __ldcg(src + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+          v[b] = f < nvec && ptr_ok(kSitePartialRead, src + f, 4, p.sk_partials, p.partial_extent)
+                     ? __ldcg(src + f)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
         }
       }
 #pragma unroll
@@ -462,6 +476,7 @@ __device__ __forceinline__ void cluster_split_sum(const TcParams &p, const float
       if (gm >= M) continue;
       float *dst = C + static_cast<long long>(gm) * ldc + gn;
       if (vec_ok && gn + 3 < N) {
+        if (!ptr_ok(kSiteCStore, dst, 4, C, p.c_extent)) continue;
         float4 o = make_float4(alpha * acc[b].x, alpha * acc[b].y, alpha * acc[b].z,
                                alpha * acc[b].w);
         if (beta != 0.0f) {
@@ -476,7 +491,8 @@ __device__ __forceinline__ void cluster_split_sum(const TcParams &p, const float
         const float e[4] = {acc[b].x, acc[b].y, acc[b].z, acc[b].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          if (gn + i < N) dst[i] = beta != 0.0f ? alpha * e[i] + beta * dst[i] : alpha * e[i];
+          if (gn + i < N && ptr_ok(kSiteCStore, dst + i, 1, C, p.c_extent))
+            dst[i] = beta != 0.0f ? alpha * e[i] + beta * dst[i] : alpha * e[i];
       }
     }
   }
@@ -561,7 +577,8 @@ __device__ __forceinline__ void stage_a_value(uint8_t *stage, int lo_offset, uin
 template <int BK, bool EXACT, int ROWS>
 __device__ __forceinline__ void stage_rows_lsu(uint8_t *tile, int lo_offset, const float *src,
                                                long long ld, int r0, int limit_r, int k0, int K,
-                                               uint32_t warp, uint32_t lane, int row_bytes) {
+                                               uint32_t warp, uint32_t lane, int row_bytes,
+                                               int site, long long extent) {
   constexpr int kRowsPerInstr = 32 / BK;
   constexpr int kSteps = ROWS / (4 * kRowsPerInstr);
   constexpr int kChunk = kSteps < 32 ? kSteps : 32;  // loads in flight per lane
@@ -576,7 +593,8 @@ __device__ __forceinline__ void stage_rows_lsu(uint8_t *tile, int lo_offset, con
     for (int i = 0; i < kChunk; ++i) {
       const int row = (chunk * kChunk + i) * 4 * kRowsPerInstr + warp * kRowsPerInstr + r_in;
       const int gr = r0 + row;
-      v[i] = (gr < limit_r && gk < K) ? __ldg(src + static_cast<long long>(gr) * ld + gk) : 0.0f;
+      const long long off = static_cast<long long>(gr) * ld + gk;
+      v[i] = (gr < limit_r && gk < K && index_ok(site, off, 1, extent)) ? __ldg(src + off) : 0.0f;
     }
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
@@ -596,7 +614,8 @@ __device__ __forceinline__ void stage_rows_lsu(uint8_t *tile, int lo_offset, con
 template <int BK, bool EXACT, int ROWS>
 __device__ __forceinline__ void stage_cols_lsu(uint8_t *tile, int lo_offset, const float *src,
                                                long long ld, int r0, int limit_r, int k0, int K,
-                                               uint32_t warp, uint32_t lane, int row_bytes) {
+                                               uint32_t warp, uint32_t lane, int row_bytes,
+                                               int site, long long extent) {
   constexpr int kRowGroups = ROWS / 8;
   constexpr int kPerWarp = kRowGroups * (BK / 4) / 4;
   constexpr int kChunk = kPerWarp < 16 ? kPerWarp : 16;  // loads in flight per lane
@@ -612,7 +631,8 @@ __device__ __forceinline__ void stage_cols_lsu(uint8_t *tile, int lo_offset, con
       const int row = (g % kRowGroups) * 8 + r_in;
       const int k = (g / kRowGroups) * 4 + k_in;
       const int gr = r0 + row, gk = k0 + k;
-      v[i] = (gr < limit_r && gk < K) ? __ldg(src + static_cast<long long>(gk) * ld + gr) : 0.0f;
+      const long long off = static_cast<long long>(gk) * ld + gr;
+      v[i] = (gr < limit_r && gk < K && index_ok(site, off, 1, extent)) ? __ldg(src + off) : 0.0f;
     }
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
@@ -665,10 +685,13 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
       int row0, row1;
       cluster_split_band(p.ks, u.part, row0, row1);
       auto put = [&](int m, uint32_t v) {
-        if (m >= row0 && m < row1)
-          local[m * kTN] = __uint_as_float(v);
-        else
+        if (m >= row0 && m < row1) {
+          if (index_ok(kSiteBand, m * kTN + n_loc, 1, kTM * kTN))
+            local[m * kTN] = __uint_as_float(v);
+        } else if (ptr_ok(kSitePartialWrite, slot + m * kTN, 1, p.sk_partials,
+                          p.partial_extent)) {
           slot[m * kTN] = __uint_as_float(v);
+        }
       };
 #pragma unroll 1
       for (int c = 0; c < kTM / 32; c += 2) {
@@ -691,20 +714,24 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
         if (gm0 >= p.M || !n_ok) return;
         float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
         const int rows = min(32, p.M - gm0);
+        // Index checks (checked build): each element's offset in C.
+        auto c_ok = [&](int j) {
+          return ptr_ok(kSiteCStore, dst + static_cast<long long>(j) * p.ldc, 1, p.C, p.c_extent);
+        };
         if (p.alpha == 1.0f && p.beta == 0.0f) {
           if (rows == 32) {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+              if (c_ok(j)) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (j < rows) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+              if (j < rows && c_ok(j)) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
           }
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < rows) {
+            if (j < rows && c_ok(j)) {
               float *d = dst + static_cast<long long>(j) * p.ldc;
               *d = scale_out(p, __uint_as_float(r[j]), d);
             }
@@ -739,18 +766,24 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
         tmem_load_wait();
         float *dst = slot + (c * 32) * kTN + n_loc;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) dst[j * kTN] = __uint_as_float(r0[j]);
+        for (int j = 0; j < 32; ++j)
+          if (ptr_ok(kSitePartialWrite, dst + j * kTN, 1, p.sk_partials, p.partial_extent))
+            dst[j * kTN] = __uint_as_float(r0[j]);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) dst[(32 + j) * kTN] = __uint_as_float(r1[j]);
+        for (int j = 0; j < 32; ++j)
+          if (ptr_ok(kSitePartialWrite, dst + (32 + j) * kTN, 1, p.sk_partials, p.partial_extent))
+            dst[(32 + j) * kTN] = __uint_as_float(r1[j]);
       }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) release_acc(&sh->acc_empty[acc]);
       __threadfence();
       named_barrier_sync(1, 128);
-      if (warp == EPI_WARP0 && lane == 0)
-        sh->sk_last = atomicAdd(&p.sk_counters[u.sk_tile * p.cl + rank], 1u) ==
-                      static_cast<unsigned>(u.nparts - 1);
+      if (warp == EPI_WARP0 && lane == 0) {
+        const long long ci = static_cast<long long>(u.sk_tile) * p.cl + rank;
+        sh->sk_last = index_ok(kSiteCounter, ci, 1, p.counter_extent) &&
+                      atomicAdd(&p.sk_counters[ci], 1u) == static_cast<unsigned>(u.nparts - 1);
+      }
       named_barrier_sync(1, 128);
       if (sh->sk_last) {
         if (it.done(p)) {
@@ -840,22 +873,25 @@ __global__ void __launch_bounds__(TcConfig<BK, STAGES, EXACT, OPB>::kThreads, 1)
         const int k0 = kb * BK;
         if (OPA)
           stage_cols_lsu<BK, EXACT, kTM>(st, Cfg::kALoOffset, p.A, p.lda, m0, p.M, k0, p.K, warp,
-                                         lane, Cfg::kRowBytes);
+                                         lane, Cfg::kRowBytes, kSiteLoadA, p.a_extent);
         else
           stage_rows_lsu<BK, EXACT, kTM>(st, Cfg::kALoOffset, p.A, p.lda, m0, p.M, k0, p.K, warp,
-                                         lane, Cfg::kRowBytes);
+                                         lane, Cfg::kRowBytes, kSiteLoadA, p.a_extent);
         if (OPB) {
           // B stored N x K: its tile is staged K-major, like A's.
           stage_rows_lsu<BK, EXACT, kTN>(st + Cfg::kBOffset, Cfg::kBLoOffset - Cfg::kBOffset, p.B,
-                                         p.ldb, n0, p.N, k0, p.K, warp, lane, Cfg::kRowBytes);
+                                         p.ldb, n0, p.N, k0, p.K, warp, lane, Cfg::kRowBytes,
+                                         kSiteLoadB, p.b_extent);
         } else {
           const int gn = n0 + quad * 32 + lane;
           float v[BK];
 #pragma unroll
-          for (int k = 0; k < BK; ++k)
-            v[k] = (gn < p.N && k0 + k < p.K)
-                       ? __ldg(p.B + static_cast<long long>(k0 + k) * p.ldb + gn)
+          for (int k = 0; k < BK; ++k) {
+            const long long off = static_cast<long long>(k0 + k) * p.ldb + gn;
+            v[k] = (gn < p.N && k0 + k < p.K && index_ok(kSiteLoadB, off, 1, p.b_extent))
+                       ? __ldg(p.B + off)
                        : 0.0f;
+          }
           const uint32_t col = tmem + ((quad * 32) << 16) + kBtCol + stage * Cfg::kBtColsPerStage;
           bt_to_tmem<BK, EXACT>(col, col + BK, v);
         }
@@ -1990,6 +2026,11 @@ struct LaunchPlan {
     p.ldc = a.ldc;
     p.alpha = a.alpha;
     p.beta = a.beta;
+    p.a_extent = a.opa ? matrix_extent(a.K, a.M, a.lda) : matrix_extent(a.M, a.K, a.lda);
+    p.b_extent = a.opb ? matrix_extent(a.N, a.K, a.ldb) : matrix_extent(a.K, a.N, a.ldb);
+    p.c_extent = c_extent_of(a);
+    p.partial_extent = 0;
+    p.counter_extent = 0;
     set_tiles(p, a.M, a.N, a.K, BK, CL);
     // Generous: a stage takes microseconds; one tile's mainloop about K * 25 ns.
     p.timeout_ns = 2000000000ull + static_cast<unsigned long long>(a.K) * 2000ull;
@@ -2087,6 +2128,8 @@ struct LaunchPlan {
   void set_workspace(void *ws) {
     p.sk_counters = static_cast<unsigned *>(ws);
     p.sk_partials = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + counter_bytes);
+    p.counter_extent = static_cast<long long>(counter_bytes / 4);
+    p.partial_extent = static_cast<long long>(partial_bytes / 4);
   }
 
   int launch(cudaStream_t stream) {
@@ -2348,6 +2391,8 @@ int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_
   }
   return launch_variant<32, 6, false, true, 1, false>(a, sm_count, stream);
 }
+
+GEMM_INDEX_FAULT_TAKE(tc_index_fault_take)
 
 int tc_poll_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return kErrLaunch;

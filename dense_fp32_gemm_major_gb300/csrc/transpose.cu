@@ -28,7 +28,8 @@ constexpr int kBlocksPerSm = 32;  // grid cap: up to one tile per CTA at the usu
 
 __global__ void __launch_bounds__(kW * kRowsPerPass)
     transpose_kernel(const float *__restrict__ src, long long lds, int rows, int cols,
-                     float *__restrict__ dst, long long ldd, int tiles_c, long long tiles) {
+                     float *__restrict__ dst, long long ldd, int tiles_c, long long tiles,
+                     long long src_extent, long long dst_extent) {
   __shared__ float t[kT][kT + 1];
   // The GEMM that reads the copy is launched as a programmatic dependent:
   // let it start its set-up now (it waits for this grid before reading).
@@ -43,7 +44,10 @@ __global__ void __launch_bounds__(kW * kRowsPerPass)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int r = r0 + ty + i * kRowsPerPass, c = c0 + tx + h * kW;
-        v[i][h] = (r < rows && c < cols) ? __ldg(src + static_cast<long long>(r) * lds + c) : 0.0f;
+        const long long off = static_cast<long long>(r) * lds + c;
+        v[i][h] = (r < rows && c < cols && index_ok(kSiteCopySrc, off, 1, src_extent))
+                      ? __ldg(src + off)
+                      : 0.0f;
       }
 #pragma unroll
     for (int i = 0; i < kT / kRowsPerPass; ++i)
@@ -55,14 +59,17 @@ __global__ void __launch_bounds__(kW * kRowsPerPass)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c = c0 + ty + i * kRowsPerPass, r = r0 + tx + h * kW;  // dst row c, column r
-        if (c < cols && r < rows)
-          dst[static_cast<long long>(c) * ldd + r] = t[tx + h * kW][ty + i * kRowsPerPass];
+        const long long off = static_cast<long long>(c) * ldd + r;
+        if (c < cols && r < rows && index_ok(kSiteCopyDst, off, 1, dst_extent))
+          dst[off] = t[tx + h * kW][ty + i * kRowsPerPass];
       }
     __syncthreads();
   }
 }
 
 }  // namespace
+
+GEMM_INDEX_FAULT_TAKE(transpose_index_fault_take)
 
 int transpose_launch(const float *src, int64_t lds, int64_t rows, int64_t cols, float *dst,
                      int64_t ldd, int sm_count, cudaStream_t stream) {
@@ -73,7 +80,8 @@ int transpose_launch(const float *src, int64_t lds, int64_t rows, int64_t cols, 
   const unsigned grid = static_cast<unsigned>(tiles < cap ? tiles : cap);
   transpose_kernel<<<grid, kW * kRowsPerPass, 0, stream>>>(
       src, lds, static_cast<int>(rows), static_cast<int>(cols), dst, ldd,
-      static_cast<int>(tiles_c), tiles);
+      static_cast<int>(tiles_c), tiles, matrix_extent(rows, cols, lds),
+      matrix_extent(cols, rows, ldd));
   return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 

@@ -71,7 +71,8 @@ typedef enum {
     GEMM_ERR_UNSUPPORTED_DEVICE = 2,  /* current device is not compute capability 10.3 */
     GEMM_ERR_LAUNCH = 3,              /* a CUDA launch or API call failed */
     GEMM_ERR_TIMEOUT = 4,             /* a device-side pipeline wait ran out of time */
-    GEMM_ERR_ALIAS = 5                /* C overlaps A or B */
+    GEMM_ERR_ALIAS = 5,               /* C overlaps A or B */
+    GEMM_ERR_INDEX = 6                /* checked build: a device-side index check failed */
 } gemm_f32_status;
 
 /* Kernel choice for gemm_f32_ex. */
@@ -292,9 +293,64 @@ const char *gemm_f32_status_string(int status);
  * gemm_f32_poll_device_status -- synchronise `stream`, then return and clear
  * the device status word of the current device (GEMM_OK if no kernel has
  * recorded an error since the last poll). Returns GEMM_ERR_LAUNCH if the
- * synchronisation itself fails.
+ * synchronisation itself fails. In the checked build (below) it returns
+ * GEMM_ERR_INDEX when no wait has timed out but an index check has failed
+ * since the last gemm_f32_take_index_fault; the record stays for that call.
  */
 int gemm_f32_poll_device_status(void *stream);
+
+/*
+ * The checked build. libgemm_f32_checked.so exports the same functions as
+ * libgemm_f32.so, compiled with device-side index checks: before every
+ * global-memory access that a kernel addresses with its own index
+ * arithmetic -- plain loads of A and B, stores and beta reads of C, the
+ * partial-sum slots and counters of split tiles, the operand copies, the
+ * reduction -- it compares the element offset with the extent the call
+ * declared for that buffer ((rows - 1) x pitch + columns for a matrix, the
+ * allocation for a library workspace). A failed check skips the access (no
+ * fault, no trap; the kernel carries on) and counts it; the first one of
+ * each kernel source file is recorded. TMA copies are bounded by their
+ * tensor maps in hardware and need no check. The checks cost time; the
+ * regular library has none (index checks compile to nothing).
+ *
+ * gemm_f32_checked_build -- 1 in the checked build, 0 in the regular one.
+ */
+int gemm_f32_checked_build(void);
+
+/*
+ * gemm_f32_take_index_fault -- synchronise `stream`, then read and reset the
+ * index-check records of the current device: *count = failed checks since
+ * the last call, and the first recorded one's *site (a GEMM_F32 site code,
+ * see gemm_f32_index_site_name), element *offset and declared *extent (all
+ * 0 when *count is 0). Always *count = 0 in the regular build. Returns
+ * GEMM_OK, GEMM_ERR_INVALID_ARG for a null output pointer, GEMM_ERR_LAUNCH
+ * if the synchronisation or a read fails. Outputs are host pointers.
+ */
+int gemm_f32_take_index_fault(void *stream, long long *count, int *site, long long *offset,
+                              long long *extent);
+
+/* gemm_f32_index_site_name -- static, NUL-terminated name of an index-check
+ * site code (1 C store, 2 partial slot write, 3 partial slot read, 4
+ * split-tile counter, 5 cluster-split band in shared memory, 6 A load, 7 B
+ * load, 8 operand copy source, 9 operand copy destination, 10 reduction
+ * input, 11 reduction partial, 12 reduction output). */
+const char *gemm_f32_index_site_name(int site);
+
+/*
+ * gemm_f32_selftest_index_check -- self-test of the checked build's index
+ * checks. Runs gemm_f32_ex(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel,
+ * stream) with C declared one row short to the kernels' checks (extent
+ * (M - 2) x ldc + N elements instead of (M - 1) x ldc + N), so every store
+ * to C's last row fails its check and is skipped: that row keeps its
+ * previous contents and gemm_f32_take_index_fault reports a C-store site.
+ * Every access it makes stays inside the M x N matrix passed, which must be
+ * valid memory as for gemm_f32. Requires M >= 2 and K >= 1; returns what
+ * the launch returns, GEMM_ERR_INVALID_ARG for bad arguments and always in
+ * the regular build (nothing to check there).
+ */
+int gemm_f32_selftest_index_check(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                  const float *B, int64_t ldb, float *C, int64_t ldc, int mode,
+                                  int kernel, void *stream);
 
 /*
  * gemm_f32_selftest_wait_timeout -- failure-detection self-test. Launches one

@@ -22,3 +22,14 @@ def gemm_lib():
     _build.build_library()
     g.reload()
     return g
+
+
+@pytest.fixture(scope="session")
+def checked_lib(gemm_lib):
+    """The index-checked build, libgemm_f32_checked.so (a ctypes handle with
+    the same functions as the regular library)."""
+    from dense_fp32_gemm_major_gb300 import _build
+
+    _build.build_all()
+    gemm_lib.reload()
+    return gemm_lib.checked_library()

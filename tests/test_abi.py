@@ -11,7 +11,8 @@ EXPECTED = {
     "gemm_f32", "gemm_f32_ex", "gemm_f32_select", "gemm_f32_host", "gemm_f32_status_string",
     "gemm_f32_poll_device_status", "gemm_f32_selftest_wait_timeout", "gemm_f32_noalloc",
     "gemm_f32_general", "reduce_f32_sum", "gemm_f32_measure_peaks", "gemm_f32_schedule_check",
-    "gemm_f32_selftest_stalled_gemm",
+    "gemm_f32_selftest_stalled_gemm", "gemm_f32_checked_build", "gemm_f32_take_index_fault",
+    "gemm_f32_index_site_name", "gemm_f32_selftest_index_check",
 }
 
 # Fake, never dereferenced, 256-byte aligned "device" addresses for host-only paths.
@@ -30,7 +31,7 @@ def test_library_exports_every_declared_symbol(gemm_lib):
 
 def test_status_strings(gemm_lib):
     names = ["GEMM_OK", "GEMM_ERR_INVALID_ARG", "GEMM_ERR_UNSUPPORTED_DEVICE", "GEMM_ERR_LAUNCH",
-             "GEMM_ERR_TIMEOUT", "GEMM_ERR_ALIAS"]
+             "GEMM_ERR_TIMEOUT", "GEMM_ERR_ALIAS", "GEMM_ERR_INDEX"]
     for code, name in enumerate(names):
         assert gemm_lib.gemm_f32_status_string(code) == name
     assert gemm_lib.gemm_f32_status_string(99) == "GEMM_ERR_UNKNOWN"
@@ -247,3 +248,56 @@ def test_stalled_gemm_self_test_validates_on_the_host(gemm_lib):
     assert g.gemm_f32_selftest_stalled_gemm(*args, g.EXACT_SIMT, 20_000_000, 0) == g.ERR_INVALID_ARG
     assert g.gemm_f32_selftest_stalled_gemm(512, 512, 256, PA, 255, PB, 512, PC, 512, g.TF32,
                                             20_000_000, 0) == g.ERR_INVALID_ARG
+
+
+def test_checked_library_exports_every_declared_symbol(gemm_lib, checked_lib):
+    for name in gemm_lib.declared_symbols():
+        assert hasattr(checked_lib, name), f"{name} not exported by the checked build"
+    assert gemm_lib.gemm_f32_checked_build() == 0
+    assert gemm_lib.gemm_f32_checked_build(lib=checked_lib) == 1
+
+
+def test_index_site_names(gemm_lib, checked_lib):
+    g = gemm_lib
+    expected = {g.SITE_C_STORE: "C store", g.SITE_PARTIAL_WRITE: "partial slot write",
+                g.SITE_PARTIAL_READ: "partial slot read", g.SITE_COUNTER: "split-tile counter",
+                g.SITE_LOAD_A: "A load", g.SITE_LOAD_B: "B load",
+                g.SITE_COPY_SRC: "operand copy source", g.SITE_COPY_DST: "operand copy destination",
+                g.SITE_REDUCE_IN: "reduction input", g.SITE_REDUCE_PARTIAL: "reduction partial",
+                g.SITE_REDUCE_OUT: "reduction output"}
+    for lib in (None, checked_lib):
+        for code, name in expected.items():
+            assert g.gemm_f32_index_site_name(code, lib=lib) == name
+        assert g.gemm_f32_index_site_name(g.SITE_BAND, lib=lib).startswith("cluster-split band")
+        assert g.gemm_f32_index_site_name(0, lib=lib) == "none"
+        assert g.gemm_f32_index_site_name(99, lib=lib) == "unknown"
+
+
+def test_index_check_entry_points_validate_on_the_host(gemm_lib, checked_lib):
+    g = gemm_lib
+    args = (64, 64, 64, PA, 64, PB, 64, PC, 64, g.EXACT)
+    # the regular build has no checks: its self-test refuses before any CUDA call
+    assert g.gemm_f32_selftest_index_check(*args) == g.ERR_INVALID_ARG
+    # the checked build validates as gemm_f32 does, and wants M >= 2, K >= 1
+    assert g.gemm_f32_selftest_index_check(1, 64, 64, PA, 64, PB, 64, PC, 64, g.EXACT,
+                                           lib=checked_lib) == g.ERR_INVALID_ARG
+    assert g.gemm_f32_selftest_index_check(64, 64, 64, PA, 63, PB, 64, PC, 64, g.EXACT,
+                                           lib=checked_lib) == g.ERR_INVALID_ARG
+    assert g.gemm_f32_selftest_index_check(64, 64, 64, PA, 64, PB, 64, PA, 64, g.EXACT,
+                                           lib=checked_lib) == g.ERR_ALIAS
+    # null outputs are refused before the device is touched
+    for lib in (g.library(), checked_lib):
+        assert lib.gemm_f32_take_index_fault(None, None, None, None, None) == g.ERR_INVALID_ARG
+
+
+def test_checked_build_without_gpu_fails_cleanly(gemm_lib, checked_lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    g = gemm_lib
+    st = g.gemm_f32_selftest_index_check(64, 64, 64, PA, 64, PB, 64, PC, 64, g.EXACT,
+                                         lib=checked_lib)
+    assert st in (g.ERR_LAUNCH, g.ERR_UNSUPPORTED_DEVICE)
+    st, count, _, _, _ = g.gemm_f32_take_index_fault(lib=checked_lib)
+    assert st in (g.ERR_LAUNCH, g.ERR_UNSUPPORTED_DEVICE) and count == 0
