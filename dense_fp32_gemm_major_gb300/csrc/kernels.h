@@ -57,6 +57,36 @@ bool tc_tma_direct(const GemmArgs &a);
 // K >= 1, M >= 1, N >= 1.
 int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_t stream);
 
+// Words of a streamed launch, in device memory (see TcParams::stream_*).
+// Rows of A and of C go in groups of `group` rows of unit tiles
+// (kStreamRows rows of the matrices each): a_ready[i] = epoch once group i's
+// rows of A have landed; b_ready[0] = epoch once B's rows [0, 32 kb_split)
+// have, and b_ready[1] once the rest have; c_done[i] counts the CTAs that
+// stored their part of a unit tile of group i of C (zeroed before the
+// launch; the group is complete at tc_stream_done_target(N, its rows of unit
+// tiles)).
+struct StreamFeed {
+  const unsigned *a_ready = nullptr;
+  const unsigned *b_ready = nullptr;
+  unsigned *c_done = nullptr;
+  unsigned epoch = 0;
+  int kb_split = 0;
+  int group = 1;
+};
+constexpr int kStreamRows = 256;     // rows of A and of C per row of unit tiles
+constexpr int kStreamKBlock = 32;    // k per k-block of kb_split
+inline unsigned tc_stream_done_target(int64_t N, int64_t tile_rows) {
+  // two CTAs per 256-column unit tile
+  return static_cast<unsigned>(2 * ((N + 255) / 256) * tile_rows);
+}
+
+// One persistent launch of the TMA-fed 3xTF32 pair kernel over whole unit
+// tiles in row-major order, its producers waiting on feed's words before
+// copying operands and its epilogue counting the stored tiles per group. A
+// (M x K) and B (K x N), not stored transposed, must be tc_tma_direct; K >= 1.
+int tc_launch_streamed(const GemmArgs &a, const StreamFeed &feed, int sm_count,
+                       cudaStream_t stream);
+
 // tc_launch with the stream-K workspace in the library's fixed scratch array
 // (no allocation, so no operand copies: with lsu = false the operands must
 // be tc_tma_direct). Returns kErrInvalidArg if the problem needs more scratch

@@ -119,6 +119,26 @@ struct TcParams {
   // the sums of split tiles run in the epilogue while the MMAs go on with
   // whole tiles; 0: whole tiles first.
   int sk_first;
+  // Height, in unit tiles, of the raster groups that order the tiles: kGroupM
+  // (concurrent clusters share operand tiles in L2), or 1 (plain row-major
+  // order) for a streamed launch.
+  int group_m;
+  // Streamed launch (operands arriving while the kernel runs; null pointers
+  // otherwise). Rows of unit tiles go in groups of stream_group, one word
+  // each. Before its first copy of A rows of unit-tile row mb a producer
+  // waits until stream_a_ready[mb / stream_group] == stream_epoch; before
+  // copying a k-block below stream_kb_split, until stream_b_ready[0] ==
+  // stream_epoch, and for one at or above it until stream_b_ready[1] ==
+  // stream_epoch. The host's copy stream writes these words once the copies
+  // they cover have completed. After storing a whole unit tile, each CTA
+  // adds 1 to stream_c_done[mb / stream_group], so a group is in C when its
+  // counter reaches cl * num_nu_blocks times its rows of unit tiles; a CTA
+  // that gives up raises every counter to the largest value, so the host's
+  // waits for C always end.
+  const unsigned *stream_a_ready, *stream_b_ready;
+  unsigned *stream_c_done;
+  unsigned stream_epoch;
+  int stream_kb_split, stream_group;
   // Extents in elements of A, B, C and the workspace's partial slots and
   // counters, which the checked build's index checks hold every plain
   // access to (checks.cuh).
@@ -203,13 +223,70 @@ struct alignas(8) TcShared {
 // tiles of the unit tile.
 __device__ __forceinline__ void tile_coords(const TcParams &p, int t, uint32_t rank, int &mb,
                                             int &nb) {
-  const int group_tiles = kGroupM * p.num_nu_blocks;
+  const int group_tiles = p.group_m * p.num_nu_blocks;
   const int g = t / group_tiles;
-  const int first_m = g * kGroupM;
-  const int gm = min(p.num_m_blocks - first_m, kGroupM);
+  const int first_m = g * p.group_m;
+  const int gm = min(p.num_m_blocks - first_m, p.group_m);
   const int r = t - g * group_tiles;
   mb = first_m + r % gm;
   nb = (r / gm) * p.cl + static_cast<int>(rank);
+}
+
+// Bounded wait of a streamed launch until the word at `flag` equals `want`:
+// the host's copy stream writes it (a stream memory operation, executed by
+// the GPU's front end, not by an SM) once the copies before it have
+// completed. The acquire load orders those copies' data before the caller's
+// later reads, and the proxy fence before its TMA copies of them. On timeout
+// the wait records kStatusTimeout and raises the CTA's abort flag.
+__device__ __noinline__ bool stream_flag_wait(const unsigned *flag, unsigned want,
+                                              unsigned long long timeout_ns,
+                                              volatile int *abort) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v == want) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    if (*abort) return false;
+    if (it == 0) {
+      t0 = global_timer_ns();
+    } else if (global_timer_ns() - t0 > timeout_ns) {
+      *abort = 1;
+      atomicCAS(&g_tc_status, 0, kStatusTimeout);
+      return false;
+    }
+    __nanosleep(256);
+  }
+}
+
+// A producer's waits in a streamed launch (TcParams::stream_*): the row of
+// unit tiles of A before a tile's copies, each half of B's k range before
+// its first k-block. Nothing to wait for in any other launch.
+struct StreamGate {
+  bool b_have[2] = {false, false};
+  __device__ __forceinline__ bool tile(const TcParams &p, int mb, volatile int *abort) {
+    return p.stream_a_ready == nullptr ||
+           stream_flag_wait(&p.stream_a_ready[mb / p.stream_group], p.stream_epoch, p.timeout_ns,
+                            abort);
+  }
+  __device__ __forceinline__ bool kblock(const TcParams &p, int kb, volatile int *abort) {
+    if (p.stream_b_ready == nullptr) return true;
+    const int h = kb < p.stream_kb_split ? 0 : 1;
+    if (!b_have[h])
+      b_have[h] = stream_flag_wait(&p.stream_b_ready[h], p.stream_epoch, p.timeout_ns, abort);
+    return b_have[h];
+  }
+};
+
+// A streamed launch whose CTA gave up: raise every done counter to the
+// largest value, so that the host's copies of C (waiting on the counters) go
+// ahead and the call returns the recorded error.
+__device__ __forceinline__ void stream_release(const TcParams &p, bool aborted) {
+  if (p.stream_c_done == nullptr || !aborted || threadIdx.x != 0) return;
+  const int words = (p.num_m_blocks + p.stream_group - 1) / p.stream_group;
+  for (int r = 0; r < words; ++r) atomicMax(&p.stream_c_done[r], 0xffffffffu);
 }
 
 // The work list of one cluster c (both CTAs of a cluster walk the same list),
@@ -750,6 +827,13 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) release_acc(&sh->acc_empty[acc]);
+      if (p.stream_c_done != nullptr) {
+        // Streamed launch: count the tile once the four warps' stores are
+        // visible to the host's copy of C.
+        __threadfence();
+        named_barrier_sync(1, 128);
+        if (warp == EPI_WARP0 && lane == 0) atomicAdd(&p.stream_c_done[mb / p.stream_group], 1u);
+      }
     } else {
       // Split tile: write this part's partial sums ([m][n], pitch kTN) to
       // its slot and free the accumulator; the last part to finish sums all
@@ -1409,6 +1493,7 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
       uint32_t armed = 0, armed_parity = 0, barmed = 0, barmed_parity = 0;
       int issued = 0;
       bool ok = true;
+      StreamGate gate;
       UnitIter it(p);
       WorkUnit u;
       while (ok && it.next(p, u)) {
@@ -1416,8 +1501,16 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
         tile_coords(p, u.tile, rank, mb, nb);
         const int m0 = mb * kTM + static_cast<int>(rank) * Cfg::kHalfRows;
         const int n0 = nb * kTN;
+        if (!gate.tile(p, mb, abort)) {
+          ok = false;
+          break;
+        }
         for (int kb = u.kb0; kb < u.kb1; ++kb) {
           if (issued++ == p.stall_kb) {  // self-test: stop feeding the pipeline
+            ok = false;
+            break;
+          }
+          if (!gate.kblock(p, kb, abort)) {
             ok = false;
             break;
           }
@@ -1637,6 +1730,7 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
     tc_fence_after_sync();
     tmem_dealloc<2>(tmem, kTmemCols);
   }
+  stream_release(p, sh->abort != 0);
   if constexpr (CS) {
     // Every CTA's k-slice partial is in its slot (the cluster barrier above
     // orders the epilogue's stores before these reads).
@@ -1967,6 +2061,8 @@ struct LaunchPlan {
   CUtensorMap map_a, map_b;
   int smem_bytes = 0;
   size_t counter_bytes = 0, partial_bytes = 0;  // workspace, 0 if no tile is split
+  // Set before prepare() for a streamed launch (pair kernels, CS = false).
+  const StreamFeed *feed = nullptr;
 
   int prepare(const GemmArgs &a, int sm_count) {
     auto kernel = K::kernel;
@@ -2039,6 +2135,13 @@ struct LaunchPlan {
     p.sk_first = 0;
     p.sk_partials = nullptr;
     p.sk_counters = nullptr;
+    p.group_m = kGroupM;
+    p.stream_a_ready = nullptr;
+    p.stream_b_ready = nullptr;
+    p.stream_c_done = nullptr;
+    p.stream_epoch = 0;
+    p.stream_kb_split = 0;
+    p.stream_group = 1;
     if constexpr (CS) {
       // ks pairs per unit tile, if the problem has few enough tiles and all
       // its clusters of 2 ks CTAs can be resident at once (checked once per
@@ -2109,6 +2212,28 @@ struct LaunchPlan {
       }
       workers = workers_cached[dev];
     }
+    if (feed != nullptr) {
+      // Streamed launch: whole unit tiles dealt round-robin in row-major
+      // order (the order A arrives in), no tile split, no workspace.
+      if (!PAIR || !EXACT || CS) return kErrInvalidArg;
+      p.group_m = 1;
+      p.stream_a_ready = feed->a_ready;
+      p.stream_b_ready = feed->b_ready;
+      p.stream_c_done = feed->c_done;
+      p.stream_epoch = feed->epoch;
+      p.stream_kb_split = feed->kb_split;
+      p.stream_group = feed->group;
+      if (p.stream_group < 1) return kErrInvalidArg;
+      sch.grid = workers < p.num_tiles ? workers : p.num_tiles;
+      sch.dp_tiles = p.num_tiles;
+      sch.sk_share = 1;
+      sch.sk_ctas = 0;
+      sch.splits = false;
+      p.dp_tiles = p.num_tiles;
+      p.sk_share = 1;
+      p.sk_ctas = 0;
+      return kOk;
+    }
     sch = schedule_for(p, workers, BK, EXACT, PAIR);
     p.dp_tiles = sch.dp_tiles;
     p.sk_share = sch.sk_share;
@@ -2151,6 +2276,12 @@ struct LaunchPlan {
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = CL > 1 ? 2 : 1;
+    if (feed != nullptr && CL > 1) {
+      // A streamed launch follows the zeroing of its done counters in plain
+      // stream order.
+      cfg.attrs = attr + 1;
+      cfg.numAttrs = 1;
+    }
     return cudaLaunchKernelEx(&cfg, K::kernel, map_a, map_b, p) ==
                    cudaSuccess
                ? kOk
@@ -2392,6 +2523,19 @@ int tc_launch(const GemmArgs &a, bool exact, bool lsu, int sm_count, cudaStream_
   return launch_variant<32, 6, false, true, 1, false>(a, sm_count, stream);
 }
 
+static_assert(kStreamRows == kTM, "a ready word and a done counter cover one row of unit tiles");
+static_assert(kPairExactBK == kStreamKBlock, "B halves end on 3xTF32 pair k-blocks");
+
+int tc_launch_streamed(const GemmArgs &a, const StreamFeed &feed, int sm_count,
+                       cudaStream_t stream) {
+  if (a.opa || a.opb || !tc_tma_direct(a) || a.K < 1) return kErrInvalidArg;
+  LaunchPlan<kPairExactBK, kPairExactStages, true, false, 2, false, false, kPairExactBSlots, true>
+      plan;
+  plan.feed = &feed;
+  const int st = plan.prepare(a, sm_count);
+  return st != kOk ? st : plan.launch(stream);
+}
+
 GEMM_INDEX_FAULT_TAKE(tc_index_fault_take)
 
 int tc_poll_status(cudaStream_t stream) {
@@ -2563,6 +2707,7 @@ extern "C" int gemm_f32_schedule_check(int64_t M, int64_t N, int64_t K, int64_t 
   const int bk = kernel_kind == 0 ? kPairExactBK : (kernel_kind == 2 ? 16 : 32);
   TcParams p = {};
   set_tiles(p, M, N, K, bk, pair ? 2 : 1);
+  p.group_m = kGroupM;
   p.ks = 1;
   p.sk_first = 0;
   const int64_t cells = static_cast<int64_t>(p.num_tiles) * p.num_k_blocks;

@@ -197,19 +197,31 @@ int gemm_f32_select(int64_t M, int64_t N, int64_t K,
 /*
  * gemm_f32_host -- C = A x B for matrices in HOST memory (pageable or pinned).
  * Copies A and B to device buffers that the library owns and reuses (grown on
- * demand, one set per device, held until process exit), runs gemm_f32 on a
- * library-owned stream of the current device, copies C back and waits for
- * completion. Blocking. The work is split into row chunks (a quarter of M,
- * at least 1024 rows): B and then each chunk of A go to the device on
- * one stream, each chunk's GEMM starts when its rows have landed, and its
- * rows of C come back on another stream while later chunks compute, so
- * copies and compute overlap (page-locked host memory copies fastest). When
- * K >= 512, B goes in two halves of whole rows, the second after the first
- * chunk of A: that chunk's GEMM runs over the first half of K as soon as it
- * can and adds the second half when it has landed.
+ * demand, one set per device, held until process exit), computes on
+ * library-owned streams of the current device, copies C back and waits for
+ * completion. Blocking. Copies and compute overlap (page-locked host memory
+ * copies fastest); when K >= 512, B goes in two halves of whole rows, the
+ * second after the first rows of A, so that the first GEMM work runs over
+ * the first half of K while the second half is on its way.
+ *   GEMM_F32_EXACT with K >= 16 (the 3xTF32 kernel): one launch of the
+ *     kernel over all of C, started before any operand has landed. A goes
+ *     to the device in blocks of up to 1024 rows; after each block (and each
+ *     half of B) the copy stream writes a word in device memory, for which
+ *     the kernel waits (bounded, as its pipeline waits are) before it reads
+ *     those rows. The kernel counts the stored tiles of each block of C, and
+ *     the return stream copies a block to the host as soon as its count is
+ *     complete. Needs the driver's stream memory operations; without them,
+ *     the row chunks below.
+ *   Other modes and sizes: row chunks (a quarter of M, at least 1024 rows):
+ *     B and then each chunk of A go to the device on one stream, each
+ *     chunk's GEMM (a gemm_f32 call) starts when its rows have landed, and
+ *     its rows of C come back on another stream while later chunks compute;
+ *     with the two halves of B, the first chunk's GEMM adds the second half
+ *     of K (beta = 1) once it has landed.
  * Results meet the accuracy class of the mode; they may differ in the last
  * bits from one gemm_f32 call on the whole matrices, whose split of the work
- * differs. Same size, leading-dimension, mode and alias rules as gemm_f32
+ * differs. A kernel that gives up (GEMM_ERR_TIMEOUT) releases the copies of
+ * C, so the call returns; a wait by the host for them is bounded too. Same size, leading-dimension, mode and alias rules as gemm_f32
  * (alias checked on the host ranges). Device-side leading dimensions are
  * padded to multiples of 4 so the TMA-fed kernels apply at any K and N.
  * Calls on one device are serialised by a lock. On every return, success

@@ -335,6 +335,49 @@ def test_host_entry_point_long_k(g):
         assert np.all(wc[:, n:] == -7.0), "write outside C's columns"
 
 
+def test_host_entry_point_streamed(g):
+    # Exact mode from K = 16 runs as one GEMM launch fed while it runs (a
+    # ready word per block of up to 1024 rows of A and per half of B's k
+    # range, a done counter per block of C); tf32 mode takes the row chunks,
+    # checked here on the same shapes. Shapes: fewer rows than one block, a
+    # ragged last block, N not a multiple of 256, K just below and just above
+    # the 512 from which B goes in two halves, K = 16 in exact mode and K = 4
+    # in tf32 mode (random data meets the stated TF32 bound from K = 2 on:
+    # one truncated product may be off by 2**-9; K = 1 is checked on integers
+    # below); each shape twice (a new epoch each call), and a larger call
+    # after smaller ones (the words reallocated).
+    cases = [((100, 300, 16), "exact"), ((257, 513, 511), "exact"), ((257, 513, 512), "tf32"),
+             ((600, 100, 4), "tf32"), ((1300, 260, 544), "exact"), ((300, 40, 2100), "tf32"),
+             ((5200, 520, 700), "exact"), ((5200, 520, 700), "tf32")]
+    for (m, n, k), mode in cases:
+        a, b = operands(m, n, k, "normal", seed=m + n + k + 1)
+        c64, s = oracle.gemm(a, b)
+        for rep in range(2):
+            c = g.matmul_host(a, b, mode)
+            check_within_bound(c, c64, s, k, mode, f"host streamed {mode} {m}x{n}x{k} #{rep}")
+    # integers, bitwise, alternating modes back to back; and K = 1 in tf32 mode
+    for (m, n, k), modes in [((777, 300, 1000), ("exact", "tf32", "exact", "tf32")),
+                             ((600, 100, 1), ("tf32",))]:
+        a, b = synth.small_integers((m, k), 95), synth.small_integers((k, n), 96)
+        expect64 = oracle.gemm(a, b)[0]
+        for mode in modes:
+            c = g.matmul_host(a, b, mode).astype(np.float64)
+            assert np.array_equal(c, expect64), f"{mode} {m}x{n}x{k}"
+
+
+@pytest.mark.parametrize("mode", ["exact", "tf32"])
+def test_host_entry_point_full_size(g, mode):
+    # 4096^3 through gemm_f32_host, the bench's end-to-end workload: every
+    # 256-row block of C checked on its first and last row and one between,
+    # against the oracle's rows
+    a, b, _ = config_operands("c4")
+    c = g.matmul_host(a, b, mode)
+    rows = sorted({r for blk in range(0, 4096, 256) for r in (blk, blk + 131, blk + 255)})
+    c64, s = oracle.gemm_rows(a, b, rows)
+    check_within_bound(c[rows], c64, s, 4096, mode, f"host 4096^3 {mode}")
+    assert np.isfinite(c).all()
+
+
 def test_probe_peaks_are_plausible(g):
     # MMA-only and FFMA-only probe kernels: rates between half and twice the
     # nominal GB300 figures (1.1 PFLOP/s dense TF32; 152 SMs x 128 lanes x 2
