@@ -93,6 +93,8 @@ def _open(path):
     lib.gemm_f32_selftest_wait_timeout.restype = i32
     lib.gemm_f32_selftest_stalled_gemm.argtypes = sig + [i32, i64, p]
     lib.gemm_f32_selftest_stalled_gemm.restype = i32
+    lib.gemm_f32_selftest_host_missing_block.argtypes = sig + [i64]
+    lib.gemm_f32_selftest_host_missing_block.restype = i32
     lib.gemm_f32_schedule_check.argtypes = [i64, i64, i64, i64, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.gemm_f32_schedule_check.restype = i32
     lib.gemm_f32_checked_build.argtypes = []
@@ -235,6 +237,11 @@ def gemm_f32_selftest_index_check(M, N, K, A, lda, B, ldb, C, ldc, mode, kernel=
                                   stream=0, lib=None) -> int:
     return (lib or _load()).gemm_f32_selftest_index_check(M, N, K, A, lda, B, ldb, C, ldc, mode,
                                                          kernel, stream or None)
+
+
+def gemm_f32_selftest_host_missing_block(M, N, K, A, lda, B, ldb, C, ldc, timeout_ns) -> int:
+    return _load().gemm_f32_selftest_host_missing_block(M, N, K, A, lda, B, ldb, C, ldc,
+                                                        timeout_ns)
 
 
 SCHEDULE_KINDS = {"exact_pair": 0, "tf32_pair": 1, "exact_lsu": 2, "tf32_lsu": 3}

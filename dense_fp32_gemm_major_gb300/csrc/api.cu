@@ -257,8 +257,12 @@ const StreamValueOps &stream_value_ops() {
 // words few: each word written after a copy waits for that copy to drain
 // (about 3.5 us, and the next copy starts behind it), and 4 MiB copies moved
 // 192 GB/s against 209 for one of 64 MiB.
+// Self-test only: skip_block >= 0 leaves that block's ready word unwritten
+// and timeout_ns > 0 limits each of the kernel's waits (see
+// gemm_f32_selftest_host_missing_block).
 int host_streamed(HostState &hs, const GemmArgs &host, int sms, float *dA, int64_t dlda,
-                  float *dB, int64_t dldb, float *dC, int64_t dldc) {
+                  float *dB, int64_t dldb, float *dC, int64_t dldc, int64_t skip_block = -1,
+                  unsigned long long timeout_ns = 0) {
   const StreamValueOps &ops = stream_value_ops();
   const int64_t M = host.M, N = host.N, K = host.K;
   const int64_t rows = gemm::kStreamRows;
@@ -325,6 +329,7 @@ int host_streamed(HostState &hs, const GemmArgs &host, int sms, float *dA, int64
   feed.epoch = epoch;
   feed.kb_split = static_cast<int>((k1 + kblk - 1) / kblk);
   feed.group = static_cast<int>(per_copy);
+  feed.timeout_ns = timeout_ns;
   const GemmArgs d{M, N, K, dA, dlda, dB, dldb, dC, dldc};
   int st = gemm::tc_launch_streamed(d, feed, sms, hs.stream);
   if (st != gemm::kOk) return drain(st);
@@ -344,7 +349,7 @@ int host_streamed(HostState &hs, const GemmArgs &host, int sms, float *dA, int64
     const int64_t r0 = b0 * rows, n = (b1 * rows < M ? b1 * rows : M) - r0;
     if (cudaMemcpy2DAsync(dA + r0 * dlda, dlda * 4, host.A + r0 * host.lda, host.lda * 4, K * 4,
                           n, cudaMemcpyHostToDevice, hs.h2d) != cudaSuccess ||
-        !ready(a_ready + i))
+        (i != skip_block && !ready(a_ready + i)))
       return drain(gemm::kErrLaunch);
     if (i + 1 == lead && k1 < K && (!copy_b(k1, K - k1) || !ready(b_ready + 1)))
       return drain(gemm::kErrLaunch);
@@ -356,6 +361,7 @@ int host_streamed(HostState &hs, const GemmArgs &host, int sms, float *dA, int64
     group_rows(i, b0, b1);
     const int64_t r0 = b0 * rows, n = (b1 * rows < M ? b1 * rows : M) - r0;
     const unsigned target = gemm::tc_stream_done_target(N, b1 - b0);
+    if (target >= gemm::kStreamRelease) return drain(gemm::kErrInvalidArg);  // never: < 2^27
     if (ops.wait(hs.d2h, dptr(c_done + i), target, CU_STREAM_WAIT_VALUE_GEQ) != CUDA_SUCCESS)
       return drain(gemm::kErrLaunch);
     if (cudaMemcpy2DAsync(host.C + r0 * host.ldc, host.ldc * 4, dC + r0 * dldc, dldc * 4, N * 4, n,
@@ -367,14 +373,16 @@ int host_streamed(HostState &hs, const GemmArgs &host, int sms, float *dA, int64
   // not, after twice the kernel's own limit the counters are raised from the
   // copy stream (which waits on nothing) and the call reports a timeout.
   const auto t0 = std::chrono::steady_clock::now();
-  const double limit_s = 2.0 * (2.0 + 2e-6 * static_cast<double>(K)) + 1.0;
+  const double kernel_limit_s =
+      timeout_ns > 0 ? 1e-9 * static_cast<double>(timeout_ns) : 2.0 + 2e-6 * static_cast<double>(K);
+  const double limit_s = 2.0 * kernel_limit_s + 1.0;
   for (;;) {
     const cudaError_t q = cudaStreamQuery(hs.d2h);
     if (q == cudaSuccess) break;
     if (q != cudaErrorNotReady) return drain(gemm::kErrLaunch);
     if (std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count() > limit_s) {
       for (int64_t r = 0; r < tr; ++r)
-        ops.write(hs.h2d, dptr(c_done + r), 0xffffffffu, CU_STREAM_WRITE_VALUE_DEFAULT);
+        ops.write(hs.h2d, dptr(c_done + r), gemm::kStreamRelease, CU_STREAM_WRITE_VALUE_DEFAULT);
       drain(0);
       const int tst = gemm::tc_poll_status(hs.stream);
       return tst != gemm::kOk ? tst : gemm::kErrTimeout;
@@ -457,8 +465,34 @@ int gemm_f32_select(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda
   return select_kernel(a, mode, kernel);
 }
 
+// gemm_f32_host, and its failure self-test (skip_block, timeout_ns: see
+// host_streamed). Internal: not exported.
+static int gemm_f32_host_impl(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                              const float *B, int64_t ldb, float *C, int64_t ldc, int mode,
+                              int64_t skip_block, unsigned long long timeout_ns);
+
 int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
                   int64_t ldb, float *C, int64_t ldc, int mode) {
+  return gemm_f32_host_impl(M, N, K, A, lda, B, ldb, C, ldc, mode, -1, 0);
+}
+
+int gemm_f32_selftest_host_missing_block(int64_t M, int64_t N, int64_t K, const float *A,
+                                         int64_t lda, const float *B, int64_t ldb, float *C,
+                                         int64_t ldc, int64_t timeout_ns) {
+  if (timeout_ns < 1000000 || timeout_ns > 10000000000LL || K < 16) return GEMM_ERR_INVALID_ARG;
+  if (stream_value_ops().write == nullptr) return GEMM_ERR_INVALID_ARG;
+  // The last block of A: the kernel's waits for it run out.
+  const int64_t tiles_m = (M + gemm::kStreamRows - 1) / gemm::kStreamRows;
+  int64_t per_copy = (tiles_m + 3) / 4;
+  per_copy = per_copy > 4 ? 4 : (per_copy < 1 ? 1 : per_copy);
+  const int64_t last = (tiles_m + per_copy - 1) / per_copy - 1;
+  return gemm_f32_host_impl(M, N, K, A, lda, B, ldb, C, ldc, GEMM_F32_EXACT, last,
+                            static_cast<unsigned long long>(timeout_ns));
+}
+
+static int gemm_f32_host_impl(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                              const float *B, int64_t ldb, float *C, int64_t ldc, int mode,
+                              int64_t skip_block, unsigned long long timeout_ns) {
   const GemmArgs host{M, N, K, A, lda, B, ldb, C, ldc};
   bool noop = false;
   int st = validate(host, mode, &noop);
@@ -500,7 +534,7 @@ int gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, 
   // (0.90 against 0.92 ms), as do the FP32 SIMT mode, K == 0 and exact mode
   // below K = 16.
   if (mode == GEMM_F32_EXACT && K >= 16 && stream_value_ops().write != nullptr)
-    return host_streamed(hs, host, sms, dA, dlda, dB, dldb, dC, dldc);
+    return host_streamed(hs, host, sms, dA, dlda, dB, dldb, dC, dldc, skip_block, timeout_ns);
 
   // Row chunks pipelined over three streams: B, then A chunk by chunk, go
   // host to device on one; each chunk's GEMM starts on the compute stream as

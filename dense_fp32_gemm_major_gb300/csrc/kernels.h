@@ -72,8 +72,16 @@ struct StreamFeed {
   unsigned epoch = 0;
   int kb_split = 0;
   int group = 1;
+  // Limit of each device-side wait, 0 for the kernel's default (self-test).
+  unsigned long long timeout_ns = 0;
 };
 constexpr int kStreamRows = 256;     // rows of A and of C per row of unit tiles
+// Value to which a streamed launch that gives up (and the host, should it
+// ever have to) raises the done counters. The return stream's waits compare
+// cyclically, (int32_t)(counter - target) >= 0, so the value must stay at
+// least every target (below 2^27) and far from 2^31 when late increments
+// add to it: 2^30.
+constexpr unsigned kStreamRelease = 0x40000000u;
 constexpr int kStreamKBlock = 32;    // k per k-block of kb_split
 inline unsigned tc_stream_done_target(int64_t N, int64_t tile_rows) {
   // two CTAs per 256-column unit tile

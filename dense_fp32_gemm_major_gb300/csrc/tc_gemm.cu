@@ -133,8 +133,8 @@ struct TcParams {
   // they cover have completed. After storing a whole unit tile, each CTA
   // adds 1 to stream_c_done[mb / stream_group], so a group is in C when its
   // counter reaches cl * num_nu_blocks times its rows of unit tiles; a CTA
-  // that gives up raises every counter to the largest value, so the host's
-  // waits for C always end.
+  // that gives up raises every counter to kStreamRelease, which every
+  // target passes, so the host's waits for C always end.
   const unsigned *stream_a_ready, *stream_b_ready;
   unsigned *stream_c_done;
   unsigned stream_epoch;
@@ -280,13 +280,13 @@ struct StreamGate {
   }
 };
 
-// A streamed launch whose CTA gave up: raise every done counter to the
-// largest value, so that the host's copies of C (waiting on the counters) go
-// ahead and the call returns the recorded error.
+// A streamed launch whose CTA gave up: raise every done counter to
+// kStreamRelease, so that the host's copies of C (waiting on the counters)
+// go ahead and the call returns the recorded error.
 __device__ __forceinline__ void stream_release(const TcParams &p, bool aborted) {
   if (p.stream_c_done == nullptr || !aborted || threadIdx.x != 0) return;
   const int words = (p.num_m_blocks + p.stream_group - 1) / p.stream_group;
-  for (int r = 0; r < words; ++r) atomicMax(&p.stream_c_done[r], 0xffffffffu);
+  for (int r = 0; r < words; ++r) atomicMax(&p.stream_c_done[r], kStreamRelease);
 }
 
 // The work list of one cluster c (both CTAs of a cluster walk the same list),
@@ -2224,6 +2224,7 @@ struct LaunchPlan {
       p.stream_kb_split = feed->kb_split;
       p.stream_group = feed->group;
       if (p.stream_group < 1) return kErrInvalidArg;
+      if (feed->timeout_ns > 0) p.timeout_ns = feed->timeout_ns;
       sch.grid = workers < p.num_tiles ? workers : p.num_tiles;
       sch.dp_tiles = p.num_tiles;
       sch.sk_share = 1;

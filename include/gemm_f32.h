@@ -407,6 +407,25 @@ int gemm_f32_selftest_stalled_gemm(int64_t M, int64_t N, int64_t K,
                                    float *C, int64_t ldc,
                                    int mode, int64_t timeout_ns, void *stream);
 
+/*
+ * gemm_f32_selftest_host_missing_block -- failure-detection self-test of
+ * gemm_f32_host's fed launch (exact mode, K >= 16). Runs gemm_f32_host(M, N,
+ * K, A, lda, B, ldb, C, ldc, GEMM_F32_EXACT) with every device-side wait
+ * limited to `timeout_ns` (1e6 .. 1e10), except that the copy stream never
+ * writes the ready word of A's last block (the copy itself still runs). The
+ * kernel's waits for those rows run out: they record GEMM_ERR_TIMEOUT, the
+ * CTAs give up as in gemm_f32_selftest_stalled_gemm and raise every done
+ * counter, so the copies of C go ahead and the call returns. Returns what
+ * the call returns (GEMM_ERR_TIMEOUT when the mechanism works; C's contents
+ * are then unspecified); GEMM_ERR_INVALID_ARG for bad arguments, K < 16, or
+ * a driver without stream memory operations (no fed launch to test). The
+ * context stays usable.
+ */
+int gemm_f32_selftest_host_missing_block(int64_t M, int64_t N, int64_t K,
+                                         const float *A, int64_t lda,
+                                         const float *B, int64_t ldb,
+                                         float *C, int64_t ldc, int64_t timeout_ns);
+
 /* Kinds of tensor-core launch for gemm_f32_schedule_check. */
 typedef enum {
     GEMM_SCHEDULE_EXACT_PAIR = 0,  /* 3xTF32 on CTA pairs (TMA-fed, exact mode) */

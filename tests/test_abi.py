@@ -13,6 +13,7 @@ EXPECTED = {
     "gemm_f32_general", "reduce_f32_sum", "gemm_f32_measure_peaks", "gemm_f32_schedule_check",
     "gemm_f32_selftest_stalled_gemm", "gemm_f32_checked_build", "gemm_f32_take_index_fault",
     "gemm_f32_index_site_name", "gemm_f32_selftest_index_check",
+    "gemm_f32_selftest_host_missing_block",
 }
 
 # Fake, never dereferenced, 256-byte aligned "device" addresses for host-only paths.
@@ -301,3 +302,14 @@ def test_checked_build_without_gpu_fails_cleanly(gemm_lib, checked_lib):
     assert st in (g.ERR_LAUNCH, g.ERR_UNSUPPORTED_DEVICE)
     st, count, _, _, _ = g.gemm_f32_take_index_fault(lib=checked_lib)
     assert st in (g.ERR_LAUNCH, g.ERR_UNSUPPORTED_DEVICE) and count == 0
+
+
+def test_host_missing_block_self_test_validates_on_the_host(gemm_lib):
+    g = gemm_lib
+    args = (512, 512, 256, PA, 256, PB, 512, PC, 512)
+    assert g.gemm_f32_selftest_host_missing_block(*args, 10) == g.ERR_INVALID_ARG      # limit
+    assert g.gemm_f32_selftest_host_missing_block(*args, 1 << 40) == g.ERR_INVALID_ARG
+    assert g.gemm_f32_selftest_host_missing_block(512, 512, 8, PA, 8, PB, 512, PC, 512,
+                                                  20_000_000) == g.ERR_INVALID_ARG      # K < 16
+    assert g.gemm_f32_selftest_host_missing_block(512, 512, 256, PA, 255, PB, 512, PC, 512,
+                                                  20_000_000) == g.ERR_INVALID_ARG

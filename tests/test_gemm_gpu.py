@@ -365,6 +365,26 @@ def test_host_entry_point_streamed(g):
             assert np.array_equal(c, expect64), f"{mode} {m}x{n}x{k}"
 
 
+def test_host_fed_launch_missing_block_times_out(g):
+    # gemm_f32_host's fed launch with the ready word of A's last block never
+    # written: the kernel's waits for it run out (20 ms), its CTAs raise every
+    # done counter so the copies of C go ahead, and the call returns
+    # GEMM_ERR_TIMEOUT; a correct call follows on the same context
+    m, n, k = 1300, 520, 544
+    a, b = operands(m, n, k, "normal", seed=5)
+    # pinned host buffers: the copies are asynchronous, so the host's own
+    # bounded wait for them stays in force
+    ha = torch.from_numpy(a).pin_memory()
+    hb = torch.from_numpy(b).pin_memory()
+    hc = torch.full((m, n), float("nan"), dtype=torch.float32).pin_memory()
+    st = g.gemm_f32_selftest_host_missing_block(m, n, k, ha.data_ptr(), k, hb.data_ptr(), n,
+                                                hc.data_ptr(), n, 20_000_000)
+    assert st == g.ERR_TIMEOUT, g.gemm_f32_status_string(st)
+    c = g.matmul_host(a, b, "exact")
+    c64, s = oracle.gemm(a, b)
+    check_within_bound(c, c64, s, k, "exact", "host call after the missing-block self-test")
+
+
 @pytest.mark.parametrize("mode", ["exact", "tf32"])
 def test_host_entry_point_full_size(g, mode):
     # 4096^3 through gemm_f32_host, the bench's end-to-end workload: every
