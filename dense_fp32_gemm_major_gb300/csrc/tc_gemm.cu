@@ -383,6 +383,12 @@ __device__ __forceinline__ float scale_out(const TcParams &p, float acc, const f
   return p.beta != 0.0f ? v + p.beta * *c : v;
 }
 
+// The same with C's element already loaded (c is not used when beta == 0).
+__device__ __forceinline__ float scale_value(const TcParams &p, float acc, float c) {
+  const float v = p.alpha * acc;
+  return p.beta != 0.0f ? v + p.beta * c : v;
+}
+
 // Sum the partial tiles of split tile `sk_tile` in part order and store the
 // result to C. Run by `nthreads` threads of the CTA that finished last: the
 // four epilogue warps, or every warp of the CTA for its final unit. The tile
@@ -730,7 +736,8 @@ __device__ __forceinline__ void stage_cols_lsu(uint8_t *tile, int lo_offset, con
 // of a tile shared by the pairs of its cluster; its rows go ([m][n], kTN
 // floats per row) to this CTA's shared memory at own_smem if they are in the
 // band this CTA sums, else to its slot of sk_partials, for cluster_split_sum.
-template <int ACC_BUFS, int EPI_WARP0, bool PAIR, bool CS = false, class Shared>
+template <int ACC_BUFS, int EPI_WARP0, bool PAIR, bool CS = false, bool SCALED = true,
+          class Shared>
 __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uint32_t tmem,
                                               uint32_t warp, uint32_t lane, uint32_t rank,
                                               volatile int *abort, uint32_t pb = 0,
@@ -785,44 +792,80 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
       __syncwarp();
       if (lane == 0) release_acc(&sh->acc_empty[acc]);
     } else if (u.nparts == 1) {
-      // Whole tile: straight to C, two 32-column chunks per TMEM load wait.
-      auto store_chunk = [&](int c, const uint32_t (&r)[32]) {
-        const int gm0 = mb * kTM + c * 32;
-        if (gm0 >= p.M || !n_ok) return;
-        float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
-        const int rows = min(32, p.M - gm0);
-        // Index checks (checked build): each element's offset in C.
-        auto c_ok = [&](int j) {
-          return ptr_ok(kSiteCStore, dst + static_cast<long long>(j) * p.ldc, 1, p.C, p.c_extent);
-        };
-        if (p.alpha == 1.0f && p.beta == 0.0f) {
-          if (rows == 32) {
+      if constexpr (!SCALED) {
+        // Whole tile: straight to C, two 32-column chunks per TMEM load wait.
+        auto store_chunk = [&](int c, const uint32_t (&r)[32]) {
+          const int gm0 = mb * kTM + c * 32;
+          if (gm0 >= p.M || !n_ok) return;
+          float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
+          const int rows = min(32, p.M - gm0);
+          // Index checks (checked build): each element's offset in C.
+          auto c_ok = [&](int j) {
+            return ptr_ok(kSiteCStore, dst + static_cast<long long>(j) * p.ldc, 1, p.C, p.c_extent);
+          };
+          if (p.alpha == 1.0f && p.beta == 0.0f) {
+            if (rows == 32) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (c_ok(j)) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+              for (int j = 0; j < 32; ++j)
+                if (c_ok(j)) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < rows && c_ok(j)) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+            }
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (j < rows && c_ok(j)) dst[static_cast<long long>(j) * p.ldc] = __uint_as_float(r[j]);
+              if (j < rows && c_ok(j)) {
+                float *d = dst + static_cast<long long>(j) * p.ldc;
+                *d = scale_out(p, __uint_as_float(r[j]), d);
+              }
           }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < rows && c_ok(j)) {
-              float *d = dst + static_cast<long long>(j) * p.ldc;
-              *d = scale_out(p, __uint_as_float(r[j]), d);
-            }
-        }
-      };
+        };
 #pragma unroll 1
-      for (int c = 0; c < kTM / 32; c += 2) {
-        if (mb * kTM + c * 32 >= p.M) break;
-        uint32_t r0[32], r1[32];
-        tmem_load_32cols(t_lane + c * 32, r0);
-        tmem_load_32cols(t_lane + (c + 1) * 32, r1);
-        tmem_load_wait();
-        store_chunk(c, r0);
-        store_chunk(c + 1, r1);
+        for (int c = 0; c < kTM / 32; c += 2) {
+          if (mb * kTM + c * 32 >= p.M) break;
+          uint32_t r0[32], r1[32];
+          tmem_load_32cols(t_lane + c * 32, r0);
+          tmem_load_32cols(t_lane + (c + 1) * 32, r1);
+          tmem_load_wait();
+          store_chunk(c, r0);
+          store_chunk(c + 1, r1);
+        }
+      } else {
+        auto c_ok = [&](const float *d) {  // index check (checked build)
+          return ptr_ok(kSiteCStore, d, 1, p.C, p.c_extent);
+        };
+        // alpha * acc + beta * C, one 32-column chunk at a time: its 32
+        // elements of C are loaded first, all in flight together and under
+        // the TMEM load, then scaled and stored (with beta = 0 nothing is
+        // loaded). A load right after each store, which the compiler cannot
+        // move ahead of it (the addresses differ by an ldc it cannot see is
+        // non-zero), waited out a memory round trip per element. The pair
+        // kernels hold this code only in their build for alpha != 1 or
+        // beta != 0 (in the other it cost registers and 2.5 % at beta = 0);
+        // the plain-load kernel, built once, takes it for every call.
+#pragma unroll 1
+        for (int c = 0; c < kTM / 32; ++c) {
+          const int gm0 = mb * kTM + c * 32;
+          if (gm0 >= p.M) break;
+          const int rows = n_ok ? min(32, p.M - gm0) : 0;
+          float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
+          float cv[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float *d = dst + static_cast<long long>(j) * p.ldc;
+            cv[j] = (p.beta != 0.0f && j < rows && c_ok(d)) ? *d : 0.0f;
+          }
+          uint32_t r[32];
+          tmem_load_32cols(t_lane + c * 32, r);
+          tmem_load_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            float *d = dst + static_cast<long long>(j) * p.ldc;
+            if (j < rows && c_ok(d)) *d = scale_value(p, __uint_as_float(r[j]), cv[j]);
+          }
+        }
       }
       tc_fence_before_sync();
       __syncwarp();
@@ -1155,7 +1198,9 @@ __device__ __forceinline__ void pair_load_operand(uint8_t *dst, const CUtensorMa
 // CS: a cluster holds p.ks pairs that share one unit tile (TcParams::ks);
 // the pair of a CTA is its cluster rank with bit 0 cleared (pb), and its rank
 // within the pair is bit 0.
-template <int BK, int STAGES, bool OPA, bool OPB, bool CS = false>
+// SCALED: built for alpha != 1 or beta != 0 (the whole-tile epilogue's
+// scaled stores); the other instantiation stores the accumulators as they are.
+template <int BK, int STAGES, bool OPA, bool OPB, bool CS = false, bool SCALED = false>
 __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
     tc_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
@@ -1297,7 +1342,7 @@ __global__ void __launch_bounds__(PairConfig<BK, STAGES, OPA, OPB>::kThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------------- epilogue --
-    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, true, CS>(p, sh, tmem, warp, lane, rank, abort, pb,
+    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, true, CS, SCALED>(p, sh, tmem, warp, lane, rank, abort, pb,
                                                           reinterpret_cast<float *>(tiles));
   }
 
@@ -1426,7 +1471,8 @@ struct RingPos {
 };
 
 // CS: as for tc_pair_kernel, p.ks pairs per cluster share one unit tile.
-template <int BK, int AST, int BST, int XW, bool OPB, bool CS = false>
+// SCALED: as for tc_pair_kernel.
+template <int BK, int AST, int BST, int XW, bool OPB, bool CS = false, bool SCALED = false>
 __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThreads, 1)
     tc_pair_exact_kernel(const __grid_constant__ CUtensorMap tmap_a,
                          const __grid_constant__ CUtensorMap tmap_b, const TcParams p) {
@@ -1627,7 +1673,7 @@ __global__ void __launch_bounds__(PairExactConfig<BK, AST, BST, XW, OPB>::kThrea
     __syncwarp();
   } else if (warp < Cfg::kEpiWarp0 + 4) {
     // --------------------------------------------------------- epilogue --
-    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, true, CS>(p, sh, tmem, warp, lane, rank, abort, pb,
+    epilogue_role<Cfg::kAccBufs, Cfg::kEpiWarp0, true, CS, SCALED>(p, sh, tmem, warp, lane, rank, abort, pb,
                                                           reinterpret_cast<float *>(tiles));
   } else {
     // --------------------------------------------------------- transform --
@@ -1977,7 +2023,7 @@ Schedule schedule_for(const TcParams &p, int workers, int bk, bool exact, bool p
 // The kernel a launch plan runs: tc_lsu_kernel, or with PAIR a CTA-pair
 // kernel.
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST, bool PAIR,
-          bool CS = false>
+          bool CS = false, bool SCALED = false>
 struct KernelOf {
   static_assert(LSU && CL == 1 && BST == 0 && !CS,
                 "tc_lsu_kernel: plain-load producers, one SM per tile");
@@ -1988,20 +2034,20 @@ struct KernelOf {
   static constexpr auto kernel = tc_lsu_kernel<BK, STAGES, EXACT, OPB, OPA>;
 };
 
-template <int BK, int STAGES, bool OPA, bool OPB, bool CS>
+template <int BK, int STAGES, bool OPA, bool OPB, bool CS, bool SCALED>
 struct PairTf32Kernel {
   using Cfg = PairConfig<BK, STAGES, OPA, OPB>;
   static_assert(Cfg::kTileBytes >= kTM * kTN * 4, "a cluster-split band fits the stages");
   static constexpr int kThreads = Cfg::kThreads;
   static constexpr int kSmemBytes =
       Cfg::kTileBytes + static_cast<int>(sizeof(TcShared<STAGES>)) + 1024;
-  static constexpr auto kernel = tc_pair_kernel<BK, STAGES, OPA, OPB, CS>;
+  static constexpr auto kernel = tc_pair_kernel<BK, STAGES, OPA, OPB, CS, SCALED>;
 };
 
 // Transform warps per CTA of the 3xTF32 pair kernel (16 time the same).
 constexpr int kPairExactXform = 8;
 
-template <int BK, int AST, int BST, int XW, bool OPB, bool CS>
+template <int BK, int AST, int BST, int XW, bool OPB, bool CS, bool SCALED>
 struct PairExactKernel {
   using Cfg = PairExactConfig<BK, AST, BST, XW, OPB>;
   static_assert(Cfg::kBRingOffset >= kTM * kTN * 4, "a cluster-split band fits the A ring");
@@ -2009,17 +2055,18 @@ struct PairExactKernel {
   static constexpr int kSmemBytes =
       Cfg::kTileBytes +
       static_cast<int>(sizeof(PairExactShared<AST, BST, Cfg::kTmemSlots>)) + 1024;
-  static constexpr auto kernel = tc_pair_exact_kernel<BK, AST, BST, XW, OPB, CS>;
+  static constexpr auto kernel = tc_pair_exact_kernel<BK, AST, BST, XW, OPB, CS, SCALED>;
 };
 
 // PAIR: the CTA-pair kernels, one TF32 pass (every layout) or 3xTF32 (A
 // stored M x K, B in either storage).
 // With EXACT, STAGES counts A stages and BST the B slots.
 // CS: the cluster-split variant (TcParams::ks pairs per cluster and tile).
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST, bool CS>
-struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true, CS>
-    : std::conditional_t<EXACT, PairExactKernel<BK, STAGES, BST, kPairExactXform, OPB, CS>,
-                         PairTf32Kernel<BK, STAGES, OPA, OPB, CS>> {
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST, bool CS,
+          bool SCALED>
+struct KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, true, CS, SCALED>
+    : std::conditional_t<EXACT, PairExactKernel<BK, STAGES, BST, kPairExactXform, OPB, CS, SCALED>,
+                         PairTf32Kernel<BK, STAGES, OPA, OPB, CS, SCALED>> {
   static_assert(!LSU && CL == 2 && (EXACT ? BST > 0 : BST == 0), "the pair kernels are fed by TMA");
   static_assert(!EXACT || !OPA, "3xTF32 pairs: A stored M x K");
 };
@@ -2052,10 +2099,10 @@ __host__ __device__ inline int cluster_split_ks(int tiles, int kb, int pairs, in
 // cluster-split launch of a pair kernel; prepare() sets p.ks = 1 when the
 // problem does not take it, and the caller then launches the plain plan.
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
-          int BST = 0, bool PAIR = false, bool CS = false>
+          int BST = 0, bool PAIR = false, bool CS = false, bool SCALED = false>
 struct LaunchPlan {
   static_assert(!CS || PAIR, "cluster split: pair kernels only");
-  using K = KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, CS>;
+  using K = KernelOf<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, CS, SCALED>;
   TcParams p;
   Schedule sch;
   CUtensorMap map_a, map_b;
@@ -2344,20 +2391,30 @@ int launch_pooled(Plan &plan, cudaStream_t stream) {
   return st;
 }
 
-template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
-          int BST = 0, bool PAIR = false>
-int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA, int BST, bool PAIR,
+          bool SCALED>
+int launch_plans(const GemmArgs &a, int sm_count, cudaStream_t stream) {
   if constexpr (PAIR) {
     // Few unit tiles: pairs of one cluster share each tile.
-    LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, true> cs;
+    LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, true, SCALED> cs;
     const int cst = cs.prepare(a, sm_count);
     if (cst != kOk) return cst;
     if (cs.p.ks > 1) return launch_pooled(cs, stream);
   }
-  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR> plan;
+  LaunchPlan<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, false, SCALED> plan;
   const int st = plan.prepare(a, sm_count);
   if (st != kOk) return st;
   return launch_pooled(plan, stream);
+}
+
+// The pair kernels come in two builds, for C = A B as it is and for
+// alpha != 1 or beta != 0; the plain-load kernel handles both at run time.
+template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, bool OPA = false,
+          int BST = 0, bool PAIR = false>
+int launch_variant(const GemmArgs &a, int sm_count, cudaStream_t stream) {
+  if (PAIR && (a.alpha != 1.0f || a.beta != 0.0f))
+    return launch_plans<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, PAIR>(a, sm_count, stream);
+  return launch_plans<BK, STAGES, EXACT, LSU, CL, OPB, OPA, BST, PAIR, false>(a, sm_count, stream);
 }
 
 }  // namespace
@@ -2642,6 +2699,8 @@ int noalloc_scratch(int dev, void **out) {
 template <int BK, int STAGES, bool EXACT, bool LSU, int CL, bool OPB, int BST = 0,
           bool PAIR = false>
 int launch_variant_noalloc(const GemmArgs &a, int sm_count, cudaStream_t stream) {
+  // gemm_f32_noalloc computes C = A B: the pair kernels' unscaled build.
+  if (a.alpha != 1.0f || a.beta != 0.0f) return kErrInvalidArg;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return kErrLaunch;
   void *scratch = nullptr;
