@@ -845,6 +845,15 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
         // kernels hold this code only in their build for alpha != 1 or
         // beta != 0 (in the other it cost registers and 2.5 % at beta = 0);
         // the plain-load kernel, built once, takes it for every call.
+        if (p.beta != 0.0f && n_ok) {
+          // The whole tile's C into L2 first (the warp's 32 columns are one
+          // 128-byte line per row; lanes take every 32nd row), so that only
+          // the first chunk's loads wait on HBM.
+          const float *col = p.C + static_cast<long long>(mb) * kTM * p.ldc + gn;
+#pragma unroll 1
+          for (int m = lane; m < kTM && mb * kTM + m < p.M; m += 32)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(col + static_cast<long long>(m) * p.ldc));
+        }
 #pragma unroll 1
         for (int c = 0; c < kTM / 32; ++c) {
           const int gm0 = mb * kTM + c * 32;
