@@ -6,7 +6,8 @@ Two properties, on the GPU:
   kernels on whole tiles, stream-K split tiles and cluster-split tiles, the
   plain-load kernel, the SIMT kernel, the operand copy and transpose ahead of
   the pair kernels, alpha/beta, column-major storage, the allocation-free entry
-  point, the reduction) runs through the checked build with no check failing,
+  point, the host-buffer entry point in both of its forms, the reduction)
+  runs through the checked build with no check failing,
   and its results still agree with the fp64 oracle;
 * the checks fire: gemm_f32_selftest_index_check declares C one row short to
   the kernels, so every store to the last row fails its check and is skipped.
@@ -143,6 +144,24 @@ def test_checked_build_noalloc(libs):
     assert_clean(g, cl, "allocation-free entry point")
     c64, s = oracle.gemm(a, b)
     check_within_bound(dc.cpu().numpy(), c64, s, k, "exact", "checked build, noalloc")
+
+
+@pytest.mark.parametrize("mode", ["exact", "tf32"])
+def test_checked_build_host_entry_point(libs, mode):
+    # gemm_f32_host through the checked build: exact mode takes the fed launch
+    # (ready words, done counters), tf32 mode the row chunks
+    g, cl = libs
+    take(g, cl)
+    m, n, k = 1300, 520, 544
+    a, b = synth.draw("normal", (m, k), 71), synth.draw("normal", (k, n), 72)
+    ha, hb = torch.from_numpy(a).pin_memory(), torch.from_numpy(b).pin_memory()
+    hc = torch.full((m, n), float("nan"), dtype=torch.float32).pin_memory()
+    st = cl.gemm_f32_host(m, n, k, ha.data_ptr(), k, hb.data_ptr(), n, hc.data_ptr(), n,
+                          g.MODES[mode])
+    assert st == g.OK, g.gemm_f32_status_string(st)
+    assert_clean(g, cl, f"host entry point, {mode}")
+    c64, s = oracle.gemm(a, b)
+    check_within_bound(hc.numpy(), c64, s, k, mode, f"checked build, host {mode}")
 
 
 @pytest.mark.parametrize("n,offset", [((1 << 20) + 3, 0), ((1 << 20) + 5, 1), (1000, 0)])
