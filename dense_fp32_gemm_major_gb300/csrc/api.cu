@@ -165,11 +165,11 @@ int run(const GemmArgs &a, int mode, int kernel, cudaStream_t stream) {
     GemmArgs s = a;
     s.K = 0;
     s.alpha = 0.0f;
-    return gemm::simt_launch(s, stream);
+    return gemm::simt_launch(s, sms, true, stream);
   }
   switch (k) {
     case GEMM_KERNEL_SIMT:
-      return gemm::simt_launch(a, stream);
+      return gemm::simt_launch(a, sms, true, stream);
     case GEMM_KERNEL_TC_TMA:
       return gemm::tc_launch(a, mode == GEMM_F32_EXACT, /*lsu=*/false, sms, stream);
     default:
@@ -622,7 +622,7 @@ int gemm_f32_noalloc(int64_t M, int64_t N, int64_t K, const float *A, int64_t ld
       return gemm::kErrLaunch;
     return gemm::kOk;
   }
-  if (k == GEMM_KERNEL_SIMT) return gemm::simt_launch(a, s);  // needs no scratch
+  if (k == GEMM_KERNEL_SIMT) return gemm::simt_launch(a, sms, false, s);  // no workspace
   return gemm::tc_launch_noalloc(a, mode == GEMM_F32_EXACT, k == GEMM_KERNEL_TC_LSU, sms, s);
 }
 

@@ -140,8 +140,11 @@ int pack_rows_launch(const PackJob &first, const PackJob &second, int sm_count,
 int probe_peaks(int sm_count, double *tf32_tflops, double *fp32_tflops, double *tf32_mhz,
                 double *fp32_mhz, cudaStream_t stream);
 
-// SIMT FP32 GEMM. Requires K >= 1, M >= 1, N >= 1.
-int simt_launch(const GemmArgs &a, cudaStream_t stream);
+// SIMT FP32 GEMM. Requires M >= 1, N >= 1 (K = 0 stores beta * C).
+// may_alloc: A stored M x K may first be transposed into a workspace from
+// the library's pool (see simt_gemm.cu); false where nothing may be
+// allocated (gemm_f32_noalloc).
+int simt_launch(const GemmArgs &a, int sm_count, bool may_alloc, cudaStream_t stream);
 
 // Synchronise `stream`, then read and clear the device status word.
 int tc_poll_status(cudaStream_t stream);

@@ -335,6 +335,27 @@ def test_host_entry_point_long_k(g):
         assert np.all(wc[:, n:] == -7.0), "write outside C's columns"
 
 
+@pytest.mark.parametrize("m,n,k", [(260, 1028, 70), (516, 2048, 300), (258, 1028, 70)])
+def test_simt_transposed_staging(g, m, n, k):
+    # exact_simt with A stored M x K and N >= 1024 first transposes A into a
+    # pooled workspace and stages it K x M (16-byte copies); the result must
+    # equal, bit for bit, the kernel run directly on A stored K x M (the same
+    # k order per output), and meet the FP32 bound. M not a multiple of 4
+    # (258) keeps the direct path.
+    a, b = operands(m, n, k, "normal", seed=m + n)
+    c, _ = run(g, a, b, "exact_simt")
+    c64, s = oracle.gemm(a, b)
+    check_within_bound(c, c64, s, k, "exact_simt", f"simt {m}x{n}x{k}")
+    da_t = to_dev(np.ascontiguousarray(a.T))
+    db = to_dev(b)
+    dc = torch.full((m, n), float("nan"), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    st = g.gemm_f32_general(g.ROW_MAJOR, 1, 0, m, n, k, 1.0, da_t.data_ptr(), m, db.data_ptr(), n,
+                            0.0, dc.data_ptr(), n, g.EXACT_SIMT, g.KERNEL_AUTO, stream)
+    assert st == g.OK, g.gemm_f32_status_string(st)
+    assert np.array_equal(dc.cpu().numpy(), c), "transposed staging changed the result"
+
+
 def test_host_entry_point_streamed(g):
     # Exact mode from K = 16 runs as one GEMM launch fed while it runs (a
     # ready word per block of up to 1024 rows of A and per half of B's k
