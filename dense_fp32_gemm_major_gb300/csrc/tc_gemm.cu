@@ -860,19 +860,22 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
           if (gm0 >= p.M) break;
           const int rows = n_ok ? min(32, p.M - gm0) : 0;
           float *dst = p.C + static_cast<long long>(gm0) * p.ldc + gn;
-          float cv[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float *d = dst + static_cast<long long>(j) * p.ldc;
-            cv[j] = (p.beta != 0.0f && j < rows && c_ok(d)) ? *d : 0.0f;
-          }
           uint32_t r[32];
           tmem_load_32cols(t_lane + c * 32, r);
-          tmem_load_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            float *d = dst + static_cast<long long>(j) * p.ldc;
-            if (j < rows && c_ok(d)) *d = scale_value(p, __uint_as_float(r[j]), cv[j]);
+          for (int j0 = 0; j0 < 32; j0 += 16) {
+            float cv[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float *d = dst + static_cast<long long>(j0 + j) * p.ldc;
+              cv[j] = (p.beta != 0.0f && j0 + j < rows && c_ok(d)) ? *d : 0.0f;
+            }
+            if (j0 == 0) tmem_load_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              float *d = dst + static_cast<long long>(j0 + j) * p.ldc;
+              if (j0 + j < rows && c_ok(d)) *d = scale_value(p, __uint_as_float(r[j0 + j]), cv[j]);
+            }
           }
         }
       }
