@@ -220,8 +220,9 @@ def test_stream_k_splits(g, mode, kernel, m, n, k):
     ("tf32", 256, 128, 4096),
 ])
 def test_cluster_split(g, mode, m, n, k):
-    # few unit tiles: pairs of one cluster take k-slices of a tile and sum
-    # them through distributed shared memory, in pair order
+    # few unit tiles: pairs of one cluster take k-slices of a tile; after a
+    # cluster barrier each CTA sums its band of rows over the slices, in pair
+    # order (its own slice from shared memory, the others' through L2)
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     st, stats = g.gemm_f32_schedule_check(m, n, k, sms // 2, mode + "_pair")
     assert st == g.OK and stats["cluster_split"] >= 2, stats
