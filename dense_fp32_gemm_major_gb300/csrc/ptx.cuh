@@ -404,6 +404,23 @@ __device__ __forceinline__ void tmem_load_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// No instruction: marks the 32 registers a tcgen05.ld wrote as read and
+// rewritten here. Placed after tmem_load_wait (volatile asm statements keep
+// their order), it stops the compiler from moving any use of them above the
+// wait: the values of a tcgen05.ld are defined only once tcgen05.wait::ld has
+// completed, and the wait's memory clobber orders memory accesses but not
+// arithmetic on the loaded registers (an alpha * acc computed early read
+// whatever the registers held before the load landed).
+__device__ __forceinline__ void tmem_regs_ready(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31]));
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets (all >> 4), the fixed descriptor version 1 at bit
 // 46, base offset 0 (stage tiles are 1024-byte aligned) and the layout type

@@ -783,6 +783,8 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
         tmem_load_32cols(t_lane + c * 32, r0);
         tmem_load_32cols(t_lane + (c + 1) * 32, r1);
         tmem_load_wait();
+        tmem_regs_ready(r0);
+        tmem_regs_ready(r1);
 #pragma unroll
         for (int j = 0; j < 32; ++j) put(c * 32 + j, r0[j]);
 #pragma unroll
@@ -829,6 +831,8 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
           tmem_load_32cols(t_lane + c * 32, r0);
           tmem_load_32cols(t_lane + (c + 1) * 32, r1);
           tmem_load_wait();
+          tmem_regs_ready(r0);
+          tmem_regs_ready(r1);
           store_chunk(c, r0);
           store_chunk(c + 1, r1);
         }
@@ -870,7 +874,10 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
               const float *d = dst + static_cast<long long>(j0 + j) * p.ldc;
               cv[j] = (p.beta != 0.0f && j0 + j < rows && c_ok(d)) ? *d : 0.0f;
             }
-            if (j0 == 0) tmem_load_wait();
+            if (j0 == 0) {
+              tmem_load_wait();
+              tmem_regs_ready(r);
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               float *d = dst + static_cast<long long>(j0 + j) * p.ldc;
@@ -903,6 +910,8 @@ __device__ __forceinline__ void epilogue_role(const TcParams &p, Shared *sh, uin
         tmem_load_32cols(t_lane + c * 32, r0);
         tmem_load_32cols(t_lane + (c + 1) * 32, r1);
         tmem_load_wait();
+        tmem_regs_ready(r0);
+        tmem_regs_ready(r1);
         float *dst = slot + (c * 32) * kTN + n_loc;
 #pragma unroll
         for (int j = 0; j < 32; ++j)

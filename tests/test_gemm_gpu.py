@@ -239,6 +239,30 @@ def test_cluster_split(g, mode, m, n, k):
     assert np.array_equal(ci.astype(np.float64), oracle.gemm(ai, bi)[0])
 
 
+@pytest.mark.parametrize("mode", ["exact", "tf32"])
+@pytest.mark.parametrize("m,n,k", [
+    (256, 256, 65536),   # one pair tile, k sliced over a cluster: 512 k-blocks per slice
+    (1024, 768, 40000),  # 12 tiles, cluster split, ragged k (40000 = 1250 k-blocks)
+    (4096, 2560, 12288), # 160 tiles: two whole waves, the rest stream-K parts
+])
+def test_long_k(g, mode, m, n, k):
+    # many k-blocks accumulated per tile, in one accumulator and across the
+    # parts of split tiles. Integer inputs in [-8, 8] keep every partial sum an
+    # integer below 2^24 (|sum| <= 64 K), exact in fp32 and TF32 alike, so the
+    # sampled rows must equal the fp64 oracle bit for bit; random inputs must
+    # stay within the mode's bound.
+    rows = np.unique(np.concatenate([np.arange(0, m, max(1, m // 23)), [m - 1]]))
+    ai = synth.small_integers((m, k), 21 + k)
+    bi = synth.small_integers((k, n), 22 + k)
+    ci, _ = run(g, ai, bi, mode, "auto")
+    ci64, _ = oracle.gemm_rows(ai, bi, rows)
+    assert np.array_equal(ci[rows].astype(np.float64), ci64), f"long k {mode} {m}x{n}x{k}"
+    a, b = operands(m, n, k, "uniform", seed=k + n)
+    c, _ = run(g, a, b, mode, "auto")
+    c64, s = oracle.gemm_rows(a, b, rows)
+    check_within_bound(c[rows], c64, s, k, mode, f"long k {mode} {m}x{n}x{k}")
+
+
 def test_nan_prefilled_output_fully_written(g):
     for mode, kernel in VARIANTS:
         a, b = operands(385, 519, 96, "uniform", seed=9)
