@@ -235,3 +235,27 @@ def test_general_full_size(g, mode, transa, transb):
     out64, s_rows = expect(a, b, transa, transb, alpha, beta, c0, rows=rows)
     check_within_bound(c[rows], out64, abs(alpha) * s_rows, k, mode, f"4096^3 T{transa}{transb}",
                        extra=general_slack(s_rows, alpha, beta, c0[rows]))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("mode", ["exact", "tf32"])
+def test_general_full_size_reruns_bitwise(g, mode):
+    # alpha * A B + beta * C at 4096^3, five calls on the same inputs: the
+    # scaled epilogue computes alpha * acc from registers that a TMEM load
+    # fills asynchronously, so a use scheduled before the load's wait would
+    # read stale values in some calls and not others. Every call must give
+    # the same bits, and the first must meet the bound against the oracle.
+    m = n = k = 4096
+    a = synth.uniform_pm1((m, k), 1008)
+    b = synth.uniform_pm1((k, n), 1009)
+    c0 = synth.uniform_pm1((m, n), 1010)
+    alpha, beta = 1.25, -0.5
+    first = run_general(g, a, b, 0, 0, alpha, beta, c0, mode, "auto")
+    for _ in range(4):
+        c = run_general(g, a, b, 0, 0, alpha, beta, c0, mode, "auto")
+        assert np.array_equal(c.view(np.uint32), first.view(np.uint32)), \
+            f"{mode}: {int((c != first).sum())} outputs differ between calls"
+    c64, s = _full_product(a, b)
+    full64 = alpha * c64 + beta * c0.astype(np.float64)
+    check_within_bound(first, full64, abs(alpha) * s, k, mode, "4096^3 reruns",
+                       extra=general_slack(s, alpha, beta, c0))
