@@ -1,6 +1,6 @@
 """Pins for the fp64 oracle (CPU only).
 
-The oracle must be right before it can judge the CUDA path, so it is checked
+The oracle must be right before it can vouch for the CUDA path, so it is checked
 here against things other than itself: hand-worked products, algebraic
 structure (identity, permutation, diagonal, transpose, linearity, scaling),
 the all-ones closed form, exact rational brute force, the integer-valued
